@@ -1,0 +1,485 @@
+"""Benchmark: striped absorbed-MLA decode + exact LSE merge on one GB300 (per rank).
+
+One step = the whole hot path over one batch: slot map + KV append of the
+step's new tokens, the shard-local decode over all c shards, and the LSE
+merge.  Inputs are resident in HBM when the timed region starts; the KV cache
+of every workload except "tiny" is larger than L2, and for "tiny" L2 is
+flushed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config dsv3] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU: requests are independent and the path
+has no exchange step, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import dcp_workloads as W  # noqa: E402
+
+METRIC = "KV GB/s & % of HBM roofline for striped MLA decode+LSE merge; tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# Accounting (algorithmic bytes and FLOPs)
+# ---------------------------------------------------------------------------
+def flops_per_key_head() -> int:
+    """FLOPs per (visible key, query row): 576-d dot product + 512-d weighted sum."""
+    return 2 * W.D_K + 2 * W.D_LATENT
+
+
+def q_o_bytes_per_head(q_bytes=2, o_bytes=2) -> int:
+    return W.D_K * q_bytes + W.D_LATENT * o_bytes
+
+
+def visible_keys(w: W.Workload, lens) -> int:
+    """Sum over requests and query rows of the keys each row attends (causal for Tq > 1)."""
+    tot = 0
+    for L in lens:
+        for t in range(w.Tq):
+            tot += (L - w.Tq + t + 1) * w.H
+    return tot
+
+
+def accounting(w: W.Workload, lens, max_pages: int) -> dict:
+    kv = sum(lens) * w.kv_bytes_per_token()
+    q = w.B * w.Tq * w.H * W.D_K * 2
+    out = w.B * w.Tq * w.H * (W.D_LATENT + 1) * 4
+    tables = w.B * max_pages * 4 + w.B * 4
+    append_rows = w.B * w.Tq * (w.kv_bytes_per_token() + 4 + 8)
+    flops = visible_keys(w, lens) * flops_per_key_head()
+    return dict(kv_bytes=kv, q_bytes=q, out_bytes=out, table_bytes=tables,
+                append_bytes=append_rows,
+                decode_bytes=kv + q + tables,
+                step_bytes=kv + q + tables + out + append_rows,
+                flops=flops)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        window = "timed region"
+        if not rows and self.samples:
+            rows = [s for (_, s) in self.samples]
+            window = "whole run (timed region shorter than the sampling interval)"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# Helpers
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}/{workload}")
+    if not e:
+        return None
+    if e.get("source_sha") != kernel_source_sha(e.get("sources", [])):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_fma.cu",
+                  "decode_context_mla_gb300/csrc/decode.cu",
+                  "decode_context_mla_gb300/csrc/decode.cuh",
+                  "decode_context_mla_gb300/csrc/common.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_sample(w: W.Workload, budget_s: float, max_requests: int = 64):
+    """Time the fp64 oracle (striped decode + merge) on whole requests until the budget is spent."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_ref import OracleWorkload
+    ow = OracleWorkload(w)
+    lens = ow.lens
+    order = sorted(range(w.B), key=lambda b: lens[b])
+    pick = [order[len(order) // 2]] + [b for b in order if b != order[len(order) // 2]]
+    done_bytes, t_sum, n = 0, 0.0, 0
+    wall0 = time.perf_counter()
+    for b in pick[:max_requests]:
+        if n and time.perf_counter() - wall0 > 2 * budget_s:
+            break
+        ow.load(b)
+        t0 = time.perf_counter()
+        ow.decode(b)
+        t_sum += time.perf_counter() - t0
+        done_bytes += lens[b] * w.kv_bytes_per_token()
+        n += 1
+        if t_sum >= budget_s:
+            break
+    return done_bytes, t_sum, n
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, w: W.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_ref import OracleWorkload
+    ow = OracleWorkload(w)
+    lens = ow.lens
+    # each step: the oracle on one whole request (cycling over two requests)
+    reqs = sorted(range(w.B), key=lambda b: lens[b])[: min(2, w.B)]
+    for b in reqs:
+        ow.load(b)
+    for i in range(args.warmup):
+        ow.decode(reqs[i % len(reqs)])
+    t, nbytes, toks = 0.0, 0, 0
+    for i in range(args.steps):
+        b = reqs[i % len(reqs)]
+        t0 = time.perf_counter()
+        ow.decode(b)
+        t += time.perf_counter() - t0
+        nbytes += lens[b] * w.kv_bytes_per_token()
+        toks += lens[b] * w.Tq
+    gbs = nbytes / t / 1e9
+    sample = (f"{args.steps} steps, each the fp64 oracle on one whole request "
+              f"(requests {reqs}, {[lens[b] for b in reqs]} tokens) of the {w.name} workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_obj(w), "attended_tokens_per_s": round(toks / t, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_obj(w: W.Workload) -> dict:
+    return {"workload": w.name, "description": w.description, "B": w.B, "H": w.H, "Tq": w.Tq,
+            "c": w.c, "P": w.P, "kv_dtype": w.kv_dtype, "lse_base": w.lse_base,
+            "seq_len": w.L if w.L else "bimodal", "parallelism": "replicas (one per GPU)",
+            "l2": ("KV cache larger than L2" if sum(w.seq_lens()) * w.kv_bytes_per_token()
+                   > 4 * L2_BYTES else "L2 flushed between timed steps")}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w: W.Workload):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from __graft_entry__ import build
+    build()
+    import dcp_harness as Hn
+
+    dw = Hn.build(w)
+    step = dw.step
+    lens = dw.lens
+    acc = accounting(w, lens, step.page_table.shape[1])
+    small = acc["kv_bytes"] <= 4 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    # warm-up eagerly once (sets kernel attributes), then capture the step and the decode alone
+    with torch.cuda.stream(stream):
+        step.run()
+    torch.cuda.synchronize()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        step.run()
+    from decode_context_mla_gb300 import binding as B
+    c = dw.cache
+
+    def decode_only():
+        B.dcpmla_decode(step.q, c.pools, c.scales, c.kv_dtype, step.page_table, step.seq_lens,
+                        c.P, c.c, 0, c.c, step.sm_scale, step.lse_base, step.o_part,
+                        step.lse_part, step.workspace, c.err)
+
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec, stream=stream):
+        decode_only()
+    torch.cuda.synchronize()
+
+    def timed(graph, k):
+        """Sum of per-step device times (ms) over k replays, flushing L2 between steps if small."""
+        with torch.cuda.stream(stream):
+            if flush is None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(k):
+                    graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                return e0.elapsed_time(e1)
+            tot = 0.0
+            for _ in range(k):
+                flush.add_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            g_step.replay()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ms_total = timed(g_step, args.steps)
+    t_wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(ws)
+    # the dominant kernel alone, same stream
+    ms_dec = timed(g_dec, max(args.steps, 5)) / max(args.steps, 5)
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    err = c.check_errors()
+    if err:
+        raise RuntimeError(f"device error bits {err}")
+
+    ms_step = max_over_ranks(ms_total / args.steps, ws)
+    total_kv = acc["kv_bytes"] * ws
+    value = total_kv / (ms_step * 1e-3) / 1e9
+    peaks = measured_peaks()
+    achieved = acc["decode_bytes"] / (ms_dec * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic(w.name, "decode"),
+                "kernel": "dcpmla decode (all c shards, one launch)",
+                "kernel_ms": round(ms_dec, 4),
+                "algorithmic_bytes": acc["decode_bytes"],
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
+    tflops = acc["flops"] / (ms_dec * 1e-3) / 1e12
+    tensor_info = {"achieved_tflops": round(tflops, 2), "peak_tflops": peaks["bf16_tflops"],
+                   "frac": round(tflops / peaks["bf16_tflops"], 4)}
+
+    # end to end through the public API from pinned host buffers
+    e2e = run_e2e(args, w, dw, g_step, stream, acc, ws)
+
+    # CPU baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        nb, t, n = oracle_sample(w, args.cpu_budget_s)
+        cpu = {"value": round(nb / t / 1e9, 4), "unit": "GB/s", "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": f"fp64 oracle (striped decode + merge) on {n} whole request(s) of the "
+                         f"{w.name} workload, {t:.1f} s of CPU work"}
+
+    launches_per_step = 4 if step.do_append else 3
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
+            "config": config_obj(w),
+            "attended_tokens_per_s": round(sum(lens) * w.Tq * ws / (ms_step * 1e-3), 1),
+            "decode_tokens_per_s": round(w.B * w.Tq * ws / (ms_step * 1e-3), 1),
+            "step_hbm_frac": round(acc["step_bytes"] / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "roofline": roofline, "tensor": tensor_info, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, dw, g_step, stream, acc, ws):
+    """Same metric through the public step call from pinned host buffers (copies timed)."""
+    import dcp_harness as Hn
+    step = dw.step
+    q_h = W.q_tensor(w, "cpu").pin_memory()
+    rows, scales = Hn.new_rows_host(w, dw.lens)
+    ckv_h = rows[:, :W.D_LATENT].contiguous().pin_memory()
+    krope_h = rows[:, W.D_LATENT:].contiguous().pin_memory()
+    sc_h = None if scales is None else scales.pin_memory()
+    o_h = torch.empty(step.o.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+
+    def one():
+        with torch.cuda.stream(stream):
+            step.q.copy_(q_h, non_blocking=True)
+            step.new_ckv.copy_(ckv_h, non_blocking=True)
+            step.new_krope.copy_(krope_h, non_blocking=True)
+            if sc_h is not None:
+                step.new_scales.copy_(sc_h, non_blocking=True)
+            g_step.replay()
+            o_h.copy_(step.o, non_blocking=True)
+            lse_h.copy_(step.lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    barrier(ws)
+    k = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k):
+        one()
+    e1.record(stream)
+    e1.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / k, ws)
+    return {"value": round(acc["kv_bytes"] * ws / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": step.h2d_bytes(),
+            "d2h_bytes_per_step": step.d2h_bytes()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dsv3", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = W.WORKLOADS[args.config]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

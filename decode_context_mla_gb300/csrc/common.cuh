@@ -1,0 +1,48 @@
+// Shared device/host helpers for the libdcpmla CUDA sources.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dcpmla.h"
+
+namespace dcpmla {
+
+constexpr int kDL = DCPMLA_D_LATENT;   // 512
+constexpr int kDR = DCPMLA_D_ROPE;     // 64
+constexpr int kDK = DCPMLA_D_K;        // 576
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct ShardPtrs {
+  void* pool[DCPMLA_MAX_SHARDS];
+  float* scale[DCPMLA_MAX_SHARDS];
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
+// SM count of the current device (cached per device id).
+int device_sm_count();
+
+__device__ __forceinline__ void set_err(int32_t* err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Shard-local token j of request b lives on shard r at this physical slot:
+// virtual page j / P of the request (one widened page of P*c positions is one
+// physical page of P slots per shard), offset j % P.  Returns -1 for a page
+// entry outside [0, num_pages).
+__device__ __forceinline__ int64_t shard_slot(const int32_t* pt_row, int32_t j, int32_t P,
+                                              int64_t num_pages) {
+  const int32_t g = __ldg(pt_row + j / P);
+  if (g < 0 || (int64_t)g >= num_pages) return -1;
+  return (int64_t)g * P + (j % P);
+}
+
+}  // namespace dcpmla

@@ -1,0 +1,95 @@
+// C entry points of the shard-local decode: argument checks and dispatch.
+//
+// SGLang "Decode Context Parallelism" docs, MLA decode dataflow and DCP x
+// speculative decoding: each shard's kernel gets the rank-local page table,
+// cp_world (c), cp_rank (r) and the global KV length, and returns the
+// rank-local (output, LSE).
+#include "decode.cuh"
+
+using namespace dcpmla;
+
+namespace {
+
+int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* scale_pools,
+              int32_t kv_dtype, int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+              const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+              int32_t shard_begin, int32_t shard_count, float sm_scale, int32_t lse_base,
+              float* d_o_part, float* d_lse_part, int32_t* d_err, bool check_ptrs) {
+  if (B < 0 || Tq < 1 || H < 1 || P < 1 || c < 1 || c > DCPMLA_MAX_SHARDS || max_pages < 1 ||
+      pool_rows < 0 || shard_begin < 0 || shard_count < 1 || shard_begin + shard_count > c)
+    return DCPMLA_ERR_INVALID;
+  if (lse_base != DCPMLA_LSE_E && lse_base != DCPMLA_LSE_2) return DCPMLA_ERR_INVALID;
+  if (kv_dtype != DCPMLA_KV_BF16 && kv_dtype != DCPMLA_KV_E4M3) return DCPMLA_ERR_UNSUPPORTED;
+  if (Tq > 16 || (int64_t)Tq * H > 1024) return DCPMLA_ERR_UNSUPPORTED;
+  if (!(sm_scale > 0.f) || !(sm_scale < 1e30f)) return DCPMLA_ERR_INVALID;
+  a = DecodeArgs{};
+  a.q = static_cast<const __nv_bfloat16*>(d_q);
+  a.fp8 = kv_dtype == DCPMLA_KV_E4M3;
+  a.pool_rows = pool_rows;
+  a.num_pages = pool_rows / P;
+  a.pt = d_page_table;
+  a.max_pages = max_pages;
+  a.seq_lens = d_seq_lens;
+  a.B = B; a.Tq = Tq; a.H = H; a.R = Tq * H; a.P = P; a.c = c;
+  a.shard_begin = shard_begin;
+  a.shard_count = shard_count;
+  a.sm_scale = sm_scale;
+  a.base2 = lse_base == DCPMLA_LSE_2;
+  a.o_part = d_o_part;
+  a.lse_part = d_lse_part;
+  a.err = d_err;
+  if (!check_ptrs) return DCPMLA_OK;
+  if (!d_q || !pools || !d_page_table || !d_seq_lens || !d_o_part || !d_lse_part)
+    return DCPMLA_ERR_INVALID;
+  if (!aligned16(d_q) || !aligned16(d_o_part)) return DCPMLA_ERR_INVALID;
+  if (a.fp8 && !scale_pools) return DCPMLA_ERR_INVALID;
+  for (int r = shard_begin; r < shard_begin + shard_count; ++r) {
+    if (!pools[r] || !aligned16(pools[r])) return DCPMLA_ERR_INVALID;
+    a.kv.pool[r] = pools[r];
+    if (a.fp8) {
+      if (!scale_pools[r]) return DCPMLA_ERR_INVALID;
+      a.kv.scale[r] = scale_pools[r];
+    }
+  }
+  return DCPMLA_OK;
+}
+
+size_t workspace_for(const DecodeArgs& a, int sm) { return fma_workspace_bytes(a, sm); }
+
+}  // namespace
+
+extern "C" {
+
+int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+                                 int32_t shard_count, int32_t kv_dtype, int32_t max_pages,
+                                 size_t* out) {
+  if (!out) return DCPMLA_ERR_INVALID;
+  DecodeArgs a;
+  const int st = fill_args(a, nullptr, nullptr, nullptr, kv_dtype, 0, nullptr, max_pages, nullptr,
+                           B, Tq, H, P, c, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
+                           nullptr, false);
+  if (st != DCPMLA_OK) return st;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  *out = workspace_for(a, sm);
+  return DCPMLA_OK;
+}
+
+int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools, int32_t kv_dtype,
+                  int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+                  const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P,
+                  int32_t c, int32_t shard_begin, int32_t shard_count, float sm_scale,
+                  int32_t lse_base, float* d_o_part, float* d_lse_part, void* d_workspace,
+                  size_t ws_bytes, int32_t* d_err, void* stream) {
+  DecodeArgs a;
+  int st = fill_args(a, d_q, pools, scale_pools, kv_dtype, pool_rows, d_page_table, max_pages,
+                     d_seq_lens, B, Tq, H, P, c, shard_begin, shard_count, sm_scale, lse_base,
+                     d_o_part, d_lse_part, d_err, true);
+  if (st != DCPMLA_OK) return st;
+  if (B == 0) return DCPMLA_OK;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  return launch_decode_fma(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// Arguments of one dcpmla_decode call after host-side validation, shared by
+// the decode kernels.
+#pragma once
+#include "common.cuh"
+
+namespace dcpmla {
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;   // [B, Tq, H, 576]
+  ShardPtrs kv;             // indexed by absolute shard id
+  bool fp8;
+  int64_t pool_rows;
+  int64_t num_pages;        // pool_rows / P
+  const int32_t* pt;        // [B, max_pages]
+  int32_t max_pages;
+  const int32_t* seq_lens;  // [B], global lengths
+  int32_t B, Tq, H, R, P, c, shard_begin, shard_count;
+  float sm_scale;
+  bool base2;
+  float* o_part;            // [shard_count, B, R, 512]
+  float* lse_part;          // [shard_count, B, R]
+  int32_t* err;
+};
+
+// Generic CUDA-core path (any head count, bf16 or e4m3).
+size_t fma_workspace_bytes(const DecodeArgs& a, int sm_count);
+int launch_decode_fma(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count,
+                      cudaStream_t st);
+
+}  // namespace dcpmla

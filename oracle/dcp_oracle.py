@@ -236,12 +236,28 @@ class ShardPools:
 
 def append_tokens(pools: ShardPools, rmap: RequestTokenMap, b: int, positions,
                   rows: np.ndarray, row_scales: Optional[np.ndarray] = None) -> None:
-    """Compacting write: each new token goes only to the rank that owns its slot, at physical(v)."""
+    """Compacting write: each new token goes only to the rank that owns its slot, at physical(v).
+
+    Rows are written page by page (a page of one rank at a time); within the
+    call, a later row for the same slot overwrites an earlier one.
+    """
     positions = np.asarray(positions, dtype=np.int64)
+    rows = np.asarray(rows)
     v, r, s = map_positions(rmap, b, positions)
-    for i in range(len(positions)):
-        sc = None if row_scales is None else float(row_scales[i])
-        pools.write(int(r[i]), int(s[i]), rows[i], sc)
+    P = pools.P
+    for rank in np.unique(r):
+        idx = np.nonzero(r == rank)[0]
+        idx = idx[np.argsort(s[idx] // P, kind="stable")]     # group by physical page
+        pages = s[idx] // P
+        ids, starts = np.unique(pages, return_index=True)
+        bounds = list(starts[1:]) + [len(idx)]
+        for g, lo, hi in zip(ids, starts, bounds):
+            sel = idx[lo:hi]
+            page, sc = pools._page(int(rank), int(g))
+            page[s[sel] % P] = rows[sel]
+            if row_scales is not None:
+                sc[s[sel] % P] = np.asarray(row_scales)[sel]
+            pools.written[int(rank)].update(s[sel].tolist())
 
 
 def shard_view(rmap: RequestTokenMap, b: int, L: int, r: int) -> Tuple[np.ndarray, np.ndarray]:

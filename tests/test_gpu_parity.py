@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Integers (page tables, slot maps, the appended cache) must match bit for bit;
+the fp32 outputs within the stated tolerance: max row-relative error 2e-3 for
+bf16 KV and 1e-2 for e4m3 KV (against the oracle on the dequantised values).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dcp_harness as Hn
+import dcp_workloads as W
+import oracle as O
+from decode_context_mla_gb300 import binding as B
+from oracle_ref import TOL, OracleWorkload, bits, lse_err, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    from decode_context_mla_gb300.build import build
+    build()
+
+
+# Scaled-down workloads with the structure of the five configurations, plus
+# edge cases: c = 1, odd c and page size, lengths below c and at page edges.
+SMALL = {
+    "tiny": W.WORKLOADS["tiny"],
+    "dsv3_s": W.scaled(W.WORKLOADS["dsv3"], B=3, L=2000),
+    "long_s": W.scaled(W.WORKLOADS["long"], B=2, L=40000),
+    "bimodal_s": W.scaled(W.WORKLOADS["bimodal"], B=12, lengths_mix=(6, 3000, 9000, 1, 40)),
+    "fp8_s": W.scaled(W.WORKLOADS["fp8"], B=2, L=3000),
+    "c1": W.Workload("c1", B=2, H=16, Tq=1, c=1, P=16, kv_dtype="bf16", lse_base="e", seed=11,
+                     L=1500),
+    "c3_p5_tq2": W.Workload("c3", B=3, H=8, Tq=2, c=3, P=5, kv_dtype="bf16", lse_base="2",
+                            seed=12, L=777),
+    "c16_short": W.Workload("c16", B=9, H=16, Tq=1, c=16, P=4, kv_dtype="bf16", lse_base="e",
+                            seed=13, lengths_mix=(3, 64, 200, 1, 15)),
+    "fp8_h16_tq4": W.Workload("f8", B=2, H=16, Tq=4, c=4, P=16, kv_dtype="e4m3", lse_base="e",
+                              seed=14, L=517),
+}
+
+SENTINEL = 0xA5
+
+
+def _compare_pools(dw, ow: OracleWorkload):
+    w = dw.w
+    for b in range(w.B):
+        ow.load(b)
+    for r in range(w.c):
+        dev = dw.cache.pools[r].view(torch.uint8).cpu().numpy().reshape(dw.cache.pool_rows, -1)
+        written = sorted(ow.pools.written[r])
+        if written:
+            rows, scs = ow.pools.read(r, np.array(written))
+            want = rows.view(np.uint8).reshape(len(written), -1)
+            assert np.array_equal(dev[written], want), f"shard {r} rows differ"
+            if w.kv_dtype == "e4m3":
+                got_s = dw.cache.scales[r].cpu().numpy()[written]
+                assert np.array_equal(got_s.view(np.uint32), scs.view(np.uint32))
+        untouched = np.ones(dw.cache.pool_rows, dtype=bool)
+        untouched[written] = False
+        assert np.all(dev[untouched] == SENTINEL), f"shard {r}: a row outside the owner set was written"
+
+
+@needs_cuda
+@pytest.mark.parametrize("name", list(SMALL))
+def test_step_parity_small(name):
+    w = SMALL[name]
+    dw = Hn.build(w, fill_byte=SENTINEL)
+    dw.step.run()
+    torch.cuda.synchronize()
+    assert dw.cache.check_errors() == 0
+    ow = OracleWorkload(w)
+    # page table bit-exact
+    assert np.array_equal(dw.step.page_table.cpu().numpy(), ow.page_table())
+    # appended cache bit-exact (including the step's own appends)
+    _compare_pools(dw, ow)
+    tol = TOL[w.kv_dtype]
+    o_part = dw.step.o_part.cpu().numpy()
+    lse_part = dw.step.lse_part.cpu().numpy()
+    o = dw.step.o.cpu().numpy()
+    lse = dw.step.lse.cpu().numpy()
+    for b in range(w.B):
+        op, lp, o_ref, l_ref = ow.decode(b)
+        R = w.Tq * w.H
+        assert row_rel_err(o_part[:, b].reshape(w.c, R, 512), op) < tol, (name, b, "o_part")
+        assert lse_err(lse_part[:, b].reshape(w.c, R), lp) < tol, (name, b, "lse_part")
+        assert row_rel_err(o[b].reshape(R, 512), o_ref) < tol, (name, b, "o")
+        assert lse_err(lse[b].reshape(R), l_ref) < tol, (name, b, "lse")
+
+
+@needs_cuda
+def test_dcp1_merge_is_bit_identical():
+    """dcp_size = 1: the merge returns the shard's (o, lse) unchanged, in both bases."""
+    for base in ("e", "2"):
+        w = W.Workload("c1b", B=2, H=16, Tq=1, c=1, P=16, kv_dtype="bf16", lse_base=base,
+                       seed=21, L=700)
+        dw = Hn.build(w)
+        dw.step.run()
+        torch.cuda.synchronize()
+        assert torch.equal(dw.step.o.view(-1), dw.step.o_part.view(-1))
+        assert torch.equal(dw.step.lse.view(-1), dw.step.lse_part.view(-1))
+
+
+@needs_cuda
+@pytest.mark.parametrize("base", [B.LSE_E, B.LSE_2])
+@pytest.mark.parametrize("c", [1, 2, 3, 8, 16])
+def test_lse_merge_parity(base, c):
+    g = torch.Generator().manual_seed(c * 7 + base)
+    rows = 257
+    o_part = torch.randn((c, rows, 512), generator=g, dtype=torch.float32)
+    lse_part = torch.randn((c, rows), generator=g, dtype=torch.float32) * 8
+    lse_part[:, 5] = -math.inf                        # an all-empty row
+    if c > 1:
+        lse_part[0, 7] = -math.inf                    # one empty shard
+        lse_part[1, 9] = 80.0                         # a dominant shard
+    o = torch.empty((rows, 512), device="cuda")
+    lse = torch.empty(rows, device="cuda")
+    B.dcpmla_lse_merge(o_part.cuda(), lse_part.cuda(), c, rows, base, o, lse)
+    torch.cuda.synchronize()
+    bname = "2" if base == B.LSE_2 else "e"
+    o_ref, l_ref = O.lse_merge(o_part.double().numpy(), lse_part.double().numpy(), bname)
+    assert row_rel_err(o.cpu().numpy(), o_ref) < 1e-5
+    assert lse_err(lse.cpu().numpy(), l_ref) < 1e-6
+    if c == 1:
+        assert torch.equal(o.cpu(), o_part[0]) and torch.equal(lse.cpu(), lse_part[0])
+
+
+@needs_cuda
+def test_slot_map_bit_exact_and_error_bits():
+    w = SMALL["c3_p5_tq2"]
+    ow = OracleWorkload(w)
+    pt = torch.from_numpy(ow.page_table()).cuda()
+    lens = ow.lens
+    req = torch.cat([torch.full((L,), b, dtype=torch.int32) for b, L in enumerate(lens)])
+    pos = torch.cat([torch.arange(L, dtype=torch.int64) for L in lens])
+    n = pos.numel()
+    v = torch.empty(n, dtype=torch.int64, device="cuda")
+    own = torch.empty(n, dtype=torch.int32, device="cuda")
+    ph = torch.empty(n, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dcpmla_slot_map(pt, ow.alloc.num_pages, w.c, w.P, req.cuda(), pos.cuda(), v, own, ph, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for b in range(w.B):
+        sel = (req == b).numpy()
+        wv, wo, wp = O.map_positions(ow.rmap, b, pos.numpy()[sel])
+        assert np.array_equal(v.cpu().numpy()[sel], wv)
+        assert np.array_equal(own.cpu().numpy()[sel], wo)
+        assert np.array_equal(ph.cpu().numpy()[sel], wp)
+    # bad inputs: request out of range, position past the table, page id out of range
+    pt_bad = pt.clone()
+    pt_bad[0, 0] = ow.alloc.num_pages + 5
+    req_b = torch.tensor([0, 1, 7, 2], dtype=torch.int32, device="cuda")
+    pos_b = torch.tensor([0, 10**6, 0, 3], dtype=torch.int64, device="cuda")
+    v4 = torch.zeros(4, dtype=torch.int64, device="cuda")
+    o4 = torch.zeros(4, dtype=torch.int32, device="cuda")
+    p4 = torch.zeros(4, dtype=torch.int64, device="cuda")
+    err.zero_()
+    B.dcpmla_slot_map(pt_bad, ow.alloc.num_pages, w.c, w.P, req_b, pos_b, v4, o4, p4, err)
+    torch.cuda.synchronize()
+    assert err.item() == (B.DERR_PAGE | B.DERR_POSITION)
+    assert o4.tolist()[:3] == [-1, -1, -1] and o4.tolist()[3] >= 0
+
+
+@needs_cuda
+def test_decode_flags_bad_page_and_short_length_without_faulting():
+    w = SMALL["dsv3_s"]
+    dw = Hn.build(w)
+    st = dw.step
+    pt_good = st.page_table.clone()
+    st.page_table[1, 0] = 10**8                      # request 1 points outside the pools
+    st.seq_lens[2] = 0                               # request 2 shorter than its query block
+    dw.cache.err.zero_()
+    B.dcpmla_decode(st.q, dw.cache.pools, None, B.KV_BF16, st.page_table, st.seq_lens, w.P, w.c, 0,
+                    w.c, w.sm_scale, B.LSE_2, st.o_part, st.lse_part, st.workspace, dw.cache.err)
+    torch.cuda.synchronize()
+    e = dw.cache.check_errors()
+    assert e & B.DERR_PAGE and e & B.DERR_LENGTH
+    # the bad requests' shards that needed the bad page / length are empty, request 0 is fine
+    assert torch.all(torch.isneginf(st.lse_part[:, 2]))
+    assert torch.all(st.o_part[:, 2] == 0)
+    assert torch.all(torch.isneginf(st.lse_part[:, 1])) and torch.all(st.o_part[:, 1] == 0)
+    ow = OracleWorkload(w)
+    op, lp, _, _ = ow.decode(0)
+    assert row_rel_err(st.o_part[:, 0].cpu().numpy().reshape(w.c, -1, 512), op) < TOL["bf16"]
+    st.page_table.copy_(pt_good)
+
+
+@needs_cuda
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "long", "bimodal", "fp8"])
+def test_input_generator_is_device_independent(name):
+    """The counter-based generator gives the same bits on the GPU and the CPU."""
+    w = W.WORKLOADS[name]
+    L = w.seq_lens()[-1]
+    for (p0, p1) in ((0, 300), (max(0, L - 300), L)):
+        rc, sc = W.kv_rows(w, w.B - 1, p0, p1, "cpu")
+        rg, sg = W.kv_rows(w, w.B - 1, p0, p1, "cuda")
+        assert np.array_equal(bits(rc), bits(rg))
+        if sc is not None:
+            assert torch.equal(sc, sg.cpu())
+    qc = W.q_tensor(w, "cpu", requests=[0, w.B - 1])
+    qg = W.q_tensor(w, "cuda", requests=[0, w.B - 1])
+    assert np.array_equal(bits(qc), bits(qg))
