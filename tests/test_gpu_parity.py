@@ -115,7 +115,8 @@ def test_lse_merge_parity(base, c):
     rows = 257
     o_part = torch.randn((c, rows, 512), generator=g, dtype=torch.float32)
     lse_part = torch.randn((c, rows), generator=g, dtype=torch.float32) * 8
-    lse_part[:, 5] = -math.inf                        # an all-empty row
+    lse_part[:, 5] = -math.inf                        # an all-empty row (o = 0 by convention)
+    o_part[:, 5] = 0.0
     if c > 1:
         lse_part[0, 7] = -math.inf                    # one empty shard
         lse_part[1, 9] = 80.0                         # a dominant shard
@@ -173,6 +174,8 @@ def test_decode_flags_bad_page_and_short_length_without_faulting():
     w = SMALL["dsv3_s"]
     dw = Hn.build(w)
     st = dw.step
+    st.run()                                         # append the step's new tokens first
+    torch.cuda.synchronize()
     pt_good = st.page_table.clone()
     st.page_table[1, 0] = 10**8                      # request 1 points outside the pools
     st.seq_lens[2] = 0                               # request 2 shorter than its query block
