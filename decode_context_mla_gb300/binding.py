@@ -236,6 +236,30 @@ def dcpmla_decode(q: torch.Tensor, pools: Sequence[torch.Tensor],
         _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_decode")
 
 
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def dcpmla_decode_noalloc(q: torch.Tensor, pools: Sequence[torch.Tensor],
+                          scale_pools: Optional[Sequence[torch.Tensor]], kv_dtype: int,
+                          page_table: torch.Tensor, seq_lens: torch.Tensor, P: int, c: int,
+                          shard_begin: int, shard_count: int, sm_scale: float, lse_base: int,
+                          o_part: torch.Tensor, lse_part: torch.Tensor,
+                          err: Optional[torch.Tensor], stream=None) -> None:
+    """dcpmla_decode without a caller workspace (scratch is the library's static device array)."""
+    B_, Tq, H, _ = q.shape
+    if len(pools) != c:
+        raise ValueError("need one pool per shard")
+    parr = _ptr_array(pools, "pools")
+    sarr = None if scale_pools is None else _ptr_array(scale_pools, "scale_pools", torch.float32)
+    _check(lib().dcpmla_decode_noalloc(
+        _dev(q, "q", torch.bfloat16), parr, sarr, kv_dtype, pools[0].shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), B_, Tq, H, P, c, shard_begin, shard_count,
+        float(sm_scale), lse_base, _dev(o_part, "o_part", torch.float32),
+        _dev(lse_part, "lse_part", torch.float32), _dev(err, "err", torch.int32, True),
+        _stream(stream)), "dcpmla_decode_noalloc")
+
+
 def dcpmla_lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, c: int, rows: int,
                      lse_base: int, o: torch.Tensor, lse: Optional[torch.Tensor],
                      err: Optional[torch.Tensor] = None, stream=None) -> None:

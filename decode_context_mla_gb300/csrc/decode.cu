@@ -4,6 +4,8 @@
 // speculative decoding: each shard's kernel gets the rank-local page table,
 // cp_world (c), cp_rank (r) and the global KV length, and returns the
 // rank-local (output, LSE).
+#include <mutex>
+
 #include "decode.cuh"
 
 using namespace dcpmla;
@@ -93,3 +95,59 @@ int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// For callers that cannot hand the decode a workspace: the split-KV partials
+// and arrival counters live in this file-scope device array instead.  Every
+// GPU that loads the library reserves it (DCPMLA_NOALLOC_SCRATCH_BYTES) until
+// the process exits.  In host code `g_noalloc_scratch` is only a host-side
+// stand-in for the symbol, so its device address is looked up once per
+// device (with that device current) and cached; kernels get that address.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DCPMLA_NOALLOC_SCRATCH_BYTES];
+
+int noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DCPMLA_ERR_CUDA;
+  if (dev < 0 || dev >= 256) return DCPMLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DCPMLA_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return DCPMLA_OK;
+}
+
+}  // namespace
+
+extern "C" int dcpmla_decode_noalloc(const void* d_q, void* const* pools,
+                                     float* const* scale_pools, int32_t kv_dtype,
+                                     int64_t pool_rows, const int32_t* d_page_table,
+                                     int32_t max_pages, const int32_t* d_seq_lens, int32_t B,
+                                     int32_t Tq, int32_t H, int32_t P, int32_t c,
+                                     int32_t shard_begin, int32_t shard_count, float sm_scale,
+                                     int32_t lse_base, float* d_o_part, float* d_lse_part,
+                                     int32_t* d_err, void* stream) {
+  DecodeArgs a;
+  int st = fill_args(a, d_q, pools, scale_pools, kv_dtype, pool_rows, d_page_table, max_pages,
+                     d_seq_lens, B, Tq, H, P, c, shard_begin, shard_count, sm_scale, lse_base,
+                     d_o_part, d_lse_part, d_err, true);
+  if (st != DCPMLA_OK) return st;
+  if (B == 0) return DCPMLA_OK;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  if (fma_workspace_bytes(a, sm) > (size_t)DCPMLA_NOALLOC_SCRATCH_BYTES) return DCPMLA_ERR_CAPACITY;
+  void* scratch = nullptr;
+  st = noalloc_scratch_address(&scratch);
+  if (st != DCPMLA_OK) return st;
+  return launch_decode_fma(a, scratch, (size_t)DCPMLA_NOALLOC_SCRATCH_BYTES, sm,
+                           (cudaStream_t)stream);
+}

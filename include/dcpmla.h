@@ -215,6 +215,38 @@ int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, in
                                  size_t* out);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free decode.  The pages have no counterpart to this call: it is
+ * a library convenience.
+ *
+ * Some callers cannot allocate device memory where they run the decode: a
+ * plugin whose host framework owns all device memory and forbids allocation
+ * in its enqueue path, a process whose memory is already fully reserved by a
+ * caching allocator, or a latency-critical loop in which cudaMalloc/cudaFree
+ * would synchronise the device.  This call takes the same arguments as
+ * dcpmla_decode minus the workspace and computes the same result with the
+ * CUDA-core decode kernel; its split-KV scratch is a static device array of
+ * DCPMLA_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *   - Shapes whose scratch need exceeds DCPMLA_NOALLOC_SCRATCH_BYTES are
+ *     rejected with DCPMLA_ERR_CAPACITY before anything is enqueued (use
+ *     dcpmla_decode with a caller workspace for those).
+ *   - The first call on each device looks up the scratch array's device
+ *     address (with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array; the call clears what must start at zero.
+ *     Calls that overlap on the GPU (other streams, other threads) race on it:
+ *     order them on one stream or synchronise between them.
+ * ------------------------------------------------------------------------ */
+#define DCPMLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int dcpmla_decode_noalloc(const void* d_q, void* const* pools, float* const* scale_pools,
+                          int32_t kv_dtype, int64_t pool_rows, const int32_t* d_page_table,
+                          int32_t max_pages, const int32_t* d_seq_lens, int32_t B, int32_t Tq,
+                          int32_t H, int32_t P, int32_t c, int32_t shard_begin,
+                          int32_t shard_count, float sm_scale, int32_t lse_base, float* d_o_part,
+                          float* d_lse_part, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Exact LSE merge (SGLang DCP docs, MLA decode dataflow): for every row,
  *   lse = log_b sum_r b^{lse_r},   o = sum_r b^{lse_r - lse} * o_r,
  * with b = e or 2 (the decode's LSE base); the maximum is factored out so no
