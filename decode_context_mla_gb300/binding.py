@@ -19,7 +19,7 @@ MAX_SHARDS = 64
 KV_BF16, KV_E4M3 = 0, 1
 LSE_E, LSE_2 = 0, 1
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-DERR_PAGE, DERR_POSITION, DERR_SLOT, DERR_LENGTH = 1, 2, 4, 8
+DERR_PAGE, DERR_POSITION, DERR_SLOT, DERR_LENGTH, DERR_TIMEOUT = 1, 2, 4, 8, 16
 
 
 class DcpmlaError(RuntimeError):

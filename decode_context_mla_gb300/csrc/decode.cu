@@ -56,7 +56,11 @@ int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* 
   return DCPMLA_OK;
 }
 
-size_t workspace_for(const DecodeArgs& a, int sm) { return fma_workspace_bytes(a, sm); }
+// Shapes whose query rows fill 128-row tensor-core tiles run on tcgen05; the
+// rest (few heads, e4m3 KV for now) on the CUDA-core kernel.
+size_t workspace_for(const DecodeArgs& a, int sm) {
+  return tc_supported(a) ? tc_workspace_bytes(a, sm) : fma_workspace_bytes(a, sm);
+}
 
 }  // namespace
 
@@ -91,6 +95,7 @@ int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools
   if (B == 0) return DCPMLA_OK;
   const int sm = device_sm_count();
   if (sm <= 0) return DCPMLA_ERR_CUDA;
+  if (tc_supported(a)) return launch_decode_tc(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
   return launch_decode_fma(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
 }
 

@@ -22,6 +22,11 @@ struct DecodeArgs {
   int32_t* err;
 };
 
+// Tensor-core path (tcgen05 / TMEM / TMA): 128-row query tiles, bf16 KV.
+bool tc_supported(const DecodeArgs& a);
+size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count);
+int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st);
+
 // Generic CUDA-core path (any head count, bf16 or e4m3).
 size_t fma_workspace_bytes(const DecodeArgs& a, int sm_count);
 int launch_decode_fma(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count,

@@ -54,6 +54,7 @@ extern "C" {
 #define DCPMLA_DERR_POSITION 2  /* a position lies outside the request's pages                */
 #define DCPMLA_DERR_SLOT 4      /* an owner / physical slot handed to kv_append is out of range */
 #define DCPMLA_DERR_LENGTH 8    /* seq_len < Tq, or longer than max_pages * P * c             */
+#define DCPMLA_DERR_TIMEOUT 16  /* a bounded wait inside a kernel gave up; outputs are invalid */
 
 /* KV storage formats. */
 #define DCPMLA_KV_BF16 0 /* row = 576 bf16 (512 latent then 64 rope), 1152 B                 */

@@ -43,6 +43,12 @@ SMALL = {
                             seed=13, lengths_mix=(3, 64, 200, 1, 15)),
     "fp8_h16_tq4": W.Workload("f8", B=2, H=16, Tq=4, c=4, P=16, kv_dtype="e4m3", lse_base="e",
                               seed=14, L=517),
+    # tensor-core path: split-KV combine, 16-token pages, two causal query tokens per tile
+    "dsv3_split": W.scaled(W.WORKLOADS["dsv3"], B=1, L=40000),
+    "h64_tq2_p16": W.Workload("h64", B=2, H=64, Tq=2, c=4, P=16, kv_dtype="bf16", lse_base="2",
+                              seed=15, L=1500),
+    "h128_c1_short": W.Workload("h128c1", B=3, H=128, Tq=1, c=1, P=64, kv_dtype="bf16",
+                                lse_base="e", seed=16, lengths_mix=(1, 100, 200, 1, 70)),
 }
 
 SENTINEL = 0xA5
