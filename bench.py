@@ -358,6 +358,10 @@ def run_ours(args, w: W.Workload):
     sampler = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
     sampler.start()
     time.sleep(0.3)
+    for _ in range(args.warmup):        # bring the clocks back up after the pause
+        with torch.cuda.stream(stream):
+            g_step.replay()
+    torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     t_wall0 = time.time()

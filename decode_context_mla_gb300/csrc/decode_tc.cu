@@ -8,25 +8,32 @@
 // position j*c + r).  vLLM GLM-5.3 serving post, footnote arithmetic: scores
 // over the 576-d key, values over the 512-d latent.
 //
-// One CTA = (request b, shard r, KV split, 128 query rows, one half of the
-// 512 value dims).  The two halves of a row tile are adjacent CTAs that read
-// the same KV tiles (the second read hits L2); each computes the full scores
-// (the 128 x 512 fp32 output accumulator alone would fill all of TMEM).
+// One CLUSTER of two CTAs = (request b, shard r, KV split, 128 query rows).
+// The key dims are split between the pair: CTA h = 0 owns dims [0, 256), CTA
+// h = 1 owns [256, 576) (latent 256..511 plus the 64 rope dims).  Each CTA
+// streams only its dims of every KV row, computes a partial score tile over
+// them, and the two partials are summed after an exchange through
+// distributed shared memory.  The latent dims a CTA owns are also its half
+// of the value dims, so O += P V needs no further data.  Both CTAs form the
+// same sum in the same order, so both see bit-identical scores and softmax.
 //
-//   warp 0     TMA producer: Q dims 256..575 once, then 64-token KV tiles
-//              (9 column chunks of 64 bf16, 128-byte swizzle) into 2 stages.
+//   warp 0     TMA producer: 64-token KV tiles of this CTA's dims (4 or 5
+//              column chunks of 64 bf16, 128-byte swizzle) into a 3-deep ring;
+//              CTA 1 also loads the rope part of Q once.
 //   warp 1     allocates TMEM; one thread issues the MMAs:
-//                S  = Q K^T   (M 128, N 64, K 576; Q dims 0..255 from TMEM)
-//                O += P V     (M 128, N 256, K 64;  P from TMEM, V MN-major;
-//                              P as a bf16 hi + lo pair, so two MMAs per k-step)
-//   warps 2-5  softmax: one query row per thread; online softmax in base 2
-//              with a lazily updated reference max (O is rescaled only when a
-//              tile's max exceeds the reference by more than 8), P written
-//              back to TMEM as bf16 hi/lo; epilogue normalises O and writes it.
+//                S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; Q_h latent dims from TMEM)
+//                O_h += P V_h     (M 128, N 256, K 64; P from TMEM as a bf16 hi + lo
+//                                 pair, V MN-major)
+//   warps 2-9  softmax, two warpgroups; a query row's 64 tile columns are split
+//              between one thread of each: read S_h from TMEM, st.async it
+//              into the peer's exchange buffer, add the peer's partial, online
+//              softmax in base 2 with a lazily moved reference max (O is
+//              rescaled only when a tile's max exceeds it by more than 8),
+//              P back to TMEM; epilogue normalises O_h and writes it.
 //
-// TMEM columns: O [0,256), S/P double buffer [256,384), Q dims 0..255 [384,512).
+// TMEM columns: O_h [0,256), S/P double buffer [256,384), Q_h latent [384,512).
 // Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all
-// roles drain, TMEM is freed and the CTA returns.
+// roles drain, both CTAs meet at the final cluster barrier, TMEM is freed.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -41,36 +48,38 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kMaxTcShards = 16;
+constexpr int kMaxTcShards = 8;
 constexpr int kRows = 128;
 constexpr int kTileTok = 64;
-constexpr int kChunks = 9;                           // 576 / 64
-constexpr int kChunkBytes = kTileTok * 128;          // 64 tokens x 128 B
-constexpr int kStageBytes = kChunks * kChunkBytes;   // 72 KB
-constexpr int kStages = 2;
-constexpr int kQLoChunks = 4;                        // Q dims 0..255 in TMEM
-constexpr int kQHiChunks = kChunks - kQLoChunks;     // Q dims 256..575 in SMEM
-constexpr int kQHiBytes = kQHiChunks * kRows * 128;  // 80 KB
-constexpr int kThreads = 192;
+constexpr int kChunkBytes = kTileTok * 128;          // 64 tokens x 64 bf16
+constexpr int kStageBytes = 5 * kChunkBytes;         // room for CTA 1's five chunks
+constexpr int kStages = 4;
+constexpr int kQropeBytes = kRows * 128;             // 64 rope dims x 128 rows
+constexpr int kXBytes = kRows * kTileTok * 4;        // one fp32 partial score tile
+constexpr int kThreads = 352;   // warps: 0 TMA, 1 MMA, 2-9 softmax, 10 release relay
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
-constexpr size_t kSmemBytes = 1024 + kQHiBytes + kStages * kStageBytes;
+constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBytes;
 constexpr long long kWaitCycles = 2000000000LL;     // about one second
 
 struct TcParams {
   CUtensorMap tm_q;                   // Q as [B*R, 576] bf16, box {64, 128}
   CUtensorMap tm_kv[kMaxTcShards];    // pool (shard_begin + i) as [pool_rows, 576], box {64, box_rows}
+  CUtensorMap tm_kv3[kMaxTcShards];   // same pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
   DecodeArgs a;
   int32_t box_rows;                   // rows per TMA box: min(P, 64)
+  int32_t use3d;                      // 1: one 3-D box per 4 chunks (needs box_rows == 64)
   int32_t num_splits, chunk, row_tiles;
   float* ws_o;
   float* ws_lse;
   uint32_t* ws_cnt;
 };
 
+template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -84,20 +93,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ TcParams p) {
   const DecodeArgs& a = p.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + kQHiBytes;
-  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full[2], bar_p_full[2];
-  __shared__ uint64_t bar_q_full, bar_o, bar_drain;
+  uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
+  uint8_t* sKV = smem + kQropeBytes;                     // kStages x kStageBytes
+  uint8_t* sX = sKV + kStages * kStageBytes;             // the peer's partial scores
+  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
+  __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
+  __shared__ uint64_t bar_q_full, bar_o, bar_drain, bar_l;
+  __shared__ float xmax_s[2][2][kRows];
+  __shared__ float l_s[2][kRows];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s, bad_s, last_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int vh = blockIdx.x & 1, split = blockIdx.x >> 1, rt = blockIdx.y, bz = blockIdx.z;
+  const uint32_t h = cluster_ctarank();                 // which key dims this CTA owns
+  const uint32_t peer = h ^ 1u;
+  const int nck = h ? 5 : 4;                             // 64-wide key chunks owned
+  const int split = blockIdx.x >> 1, rt = blockIdx.y, bz = blockIdx.z;
   const int b = bz / a.shard_count, sr = bz % a.shard_count, r = a.shard_begin + sr;
   const int L = a.seq_lens[b];
   const int64_t R = a.R;
@@ -110,9 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bar_s_full[s]), 1);
-      mbar_init(smem_u32(&bar_p_full[s]), 128);
+      mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);
+      mbar_init(smem_u32(&bar_max[s]), kSoftmaxThreads);
     }
-    mbar_init(smem_u32(&bar_q_full), 128 + 1);
+    mbar_init(smem_u32(&bar_x_full), 1);
+    mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
+    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads + 1);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_s = 0;
@@ -124,21 +147,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
-  // Range of this split and validation of every page the request uses.
-  int j0 = 0, j1 = 0;
+  int j0 = 0, j1 = 0, npages = 0;
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
     if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
   } else {
     const int n = L > r ? (L - r + a.c - 1) / a.c : 0;
     j0 = min(split * p.chunk, n);
     j1 = min(n, j0 + p.chunk);
-    const int npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
+    npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
     for (int pg = tid; pg < npages; pg += kThreads) {
       const int32_t g = pt_row[pg];
       if (g < 0 || (int64_t)g >= a.num_pages) atomicOr(&bad_s, DCPMLA_DERR_PAGE);
     }
   }
   __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_arrive();
+  cluster_wait();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   if (bad_s) {
@@ -150,39 +175,63 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
-    if (lane == 0 && ntiles > 0) {
+    // The whole warp keeps a window of 32 page ids; lane 0 issues the copies.
+    if (ntiles > 0) {
       const CUtensorMap* kvmap = &p.tm_kv[sr];
-      prefetch_tmap(kvmap);
-      const uint32_t qb = smem_u32(&bar_q_full);
-      mbar_arrive_expect_tx(qb, kQHiBytes);
-      for (int c = 0; c < kQHiChunks; ++c)
-        tma_load_2d(smem_u32(sQ + c * kRows * 128), &p.tm_q, (kQLoChunks + c) * 64,
-                    (int)(b * R + rt * kRows), qb);
-      int issued = 0;
+      const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
+      if (lane == 0) {
+        prefetch_tmap(kvmap);
+        if (p.use3d) prefetch_tmap(kvmap3);
+        const uint32_t qb = smem_u32(&bar_q_full);
+        if (h) {
+          mbar_arrive_expect_tx(qb, kQropeBytes);
+          tma_load_2d(smem_u32(sQr), &p.tm_q, 512, (int)(b * R + rt * kRows), qb);
+        } else {
+          mbar_arrive(qb);
+        }
+      }
+      int win_base = -64, win_val = 0, issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i & 1;
-        if (i >= kStages && !wait_bar(smem_u32(&bar_kv_empty[st]), ((i >> 1) - 1) & 1, abort_flag))
-          break;
+        const int st = i % kStages;
+        if (i >= kStages) {
+          bool okw = true;
+          if (lane == 0)
+            okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
+        }
         const int t0 = j0 + i * kTileTok;
         const int ntok = min(kTileTok, j1 - t0);
         const int box = p.box_rows;
         const int nbox = box >= kTileTok ? 1 : (ntok + box - 1) / box;
         const uint32_t full = smem_u32(&bar_kv_full[st]);
-        mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * kChunks));
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * nck));
         for (int pb = 0; pb < nbox; ++pb) {
           const int tok = t0 + pb * box;
-          const int64_t g = pt_row[tok / a.P];
-          const int y = (int)(g * a.P + (tok % a.P));
-          const uint32_t dst = smem_u32(sKV + st * kStageBytes + pb * box * 128);
-          for (int c = 0; c < kChunks; ++c) tma_load_2d(dst + c * kChunkBytes, kvmap, c * 64, y, full);
+          const int pidx = tok / a.P;
+          if (pidx < win_base || pidx >= win_base + 32) {      // uniform across the warp
+            win_base = pidx;
+            win_val = pidx + lane < npages ? pt_row[pidx + lane] : 0;
+          }
+          const int g = __shfl_sync(0xffffffffu, win_val, pidx - win_base);
+          if (lane == 0) {
+            const int y = (int)((int64_t)g * a.P + (tok % a.P));
+            const uint32_t dst = smem_u32(sKV + st * kStageBytes + pb * box * 128);
+            if (p.use3d) {
+              tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
+              if (h) tma_load_2d(dst + 4 * kChunkBytes, kvmap, 512, y, full);
+            } else {
+              for (int cl = 0; cl < nck; ++cl)
+                tma_load_2d(dst + cl * kChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
+            }
+          }
         }
         issued = i + 1;
       }
-      if (*abort_flag) {
+      if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
         for (int i = max(0, issued - kStages); i < issued; ++i) {
           const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&bar_kv_full[i & 1]), (i >> 1) & 1) &&
+          while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
                  clock64() - t0 < kWaitCycles / 8) {
           }
         }
@@ -191,40 +240,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0 && ntiles > 0) {
-      const uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
-      const uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
-      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
-      bool ok = wait_bar(smem_u32(&bar_q_full), 0, abort_flag);
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
+      // Base descriptors; the start-address field is the low 14 bits (address >> 4),
+      // so a constant byte offset is added as (offset >> 4) without carries.
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);            // K-major keys
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunkBytes, 1024);   // MN-major values
+      const uint64_t qd0 = desc_sw128(smem_u32(sQr), 16, 1024);            // rope part of Q
+      const uint32_t tq = tmem + kColQ, to = tmem + kColO;
+      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
       tc_fence_after();
       for (int i = 0; ok && i <= ntiles; ++i) {
         if (i < ntiles) {
-          const int st = i & 1, sb = i & 1;
-          if (!wait_bar(smem_u32(&bar_kv_full[st]), (i >> 1) & 1, abort_flag)) break;
+          const int st = i % kStages, sb = i & 1;
+          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
           tc_fence_after();
           const uint32_t d = tmem + kColS + sb * kTileTok;
-          const uint32_t kbase = skv + st * kStageBytes;
-          for (int c = 0; c < kChunks; ++c)
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t bd = desc_sw128(kbase + c * kChunkBytes + k * 32, 16, 1024);
-              const uint32_t acc = (c | k) != 0;
-              if (c < kQLoChunks)
-                mma_ts(d, tmem + kColQ + c * 32 + k * 8, bd, idesc_qk, acc);
-              else
-                mma_ss(d, desc_sw128(sq + (c - kQLoChunks) * kRows * 128 + k * 32, 16, 1024), bd,
-                       idesc_qk, acc);
-            }
+          const uint64_t kd = kd0 + (uint64_t)((st * kStageBytes) >> 4);
+#pragma unroll
+          for (int cl = 0; cl < 4; ++cl)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(d, tq + cl * 32 + k * 8, kd + ((cl * kChunkBytes + k * 32) >> 4), idesc_qk,
+                     (cl | k) != 0);
+          if (h) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(d, qd0 + ((k * 32) >> 4), kd + ((4 * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
+          }
           mma_commit(smem_u32(&bar_s_full[sb]));
         }
         if (i >= 1) {
-          const int pi = i - 1, st = pi & 1, sb = pi & 1;
-          if (!wait_bar(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
+          const int pi = i - 1, st = pi % kStages, sb = pi & 1;
+          if (!wait_bar<false>(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
           tc_fence_after();
-          const uint32_t vbase = skv + st * kStageBytes + vh * 4 * kChunkBytes;
-          for (int k = 0; k < 8; ++k) {          // k < 4: P_hi, k >= 4: P_lo, same V rows
-            const uint64_t bd = desc_sw128(vbase + (k & 3) * 2048, kChunkBytes, 1024);
-            mma_ts(tmem + kColO, tmem + kColS + sb * kTileTok + k * 8, bd, idesc_pv,
-                   (pi > 0 || k > 0) ? 1u : 0u);
-          }
+          const uint64_t vd = vd0 + (uint64_t)((st * kStageBytes) >> 4);
+          const uint32_t pa = tmem + kColS + sb * kTileTok;
+          mma_ts(to, pa, vd, idesc_pv, pi > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 1; k < 8; ++k)          // k < 4: P_hi, k >= 4: P_lo, same V rows
+            mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, 1u);
           mma_commit(smem_u32(&bar_kv_empty[st]));
           mma_commit(smem_u32(&bar_o));
         }
@@ -235,74 +290,131 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
       }
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ relay
+    // Once all softmax threads have read the peer's partial for a tile, tell
+    // the peer its next partial may overwrite our exchange buffer.  This
+    // thread has no stores in flight, so its cluster-scope release is cheap.
+    if (lane == 0) {
+      const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
+      for (int i = 0; i < ntiles; ++i) {
+        if (!wait_bar<false>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
+        mbar_arrive_remote(xe_peer);
+      }
+    }
   } else {
     // -------------------------------------------------------------- softmax
+    // Warps 2..9: two warpgroups; warpgroup g handles tile columns [32g, 32g + 32)
+    // of every query row (TMEM lane quarter = warp % 4).
+    const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const int stid = g * kRows + row;                        // 0..255
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
     const int qpos = L - a.Tq + (int)(grow / a.H);
+    const int qpos_min = L - a.Tq;                           // earliest query of the request
     const float qscale = a.sm_scale * kLog2e;
+    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
+    const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     if (ntiles > 0) {
-      // Q dims 0..255 of this row into TMEM as packed bf16 pairs
-      const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK);
-      for (int c16 = 0; c16 < 8; ++c16) {
+      // this CTA's latent dims of the query row into TMEM as packed bf16 pairs
+      const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK +
+                                                         h * 256 + g * 128);
+      for (int c16 = 0; c16 < 4; ++c16) {
         uint32_t rr[16];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const uint4 u = __ldg(qsrc + c16 * 4 + v);
           rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
         }
-        tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
+        tmem_st16(tmem + lane_off + kColQ + g * 64 + c16 * 16, rr);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_q_full));
     }
     for (int i = 0; i < ntiles; ++i) {
-      const int sb = i & 1;
+      const int sb = i & 1, st = i % kStages;
       const int t0 = j0 + i * kTileTok;
       const int ntok = min(kTileTok, j1 - t0);
-      ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      float x[kTileTok];
-      {
-        uint32_t u[16];
+      uint32_t own[32];
+      tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
+      tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
+                *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
+      tmem_ld_wait();
+      // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
+      // float4), once the peer has read the previous one
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + q * 16, u);
-          tmem_ld_wait();
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
+                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
+      if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
+      ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), i & 1, abort_flag));
+      if (!ok) break;
+      float x[32];
+      const float4* xin = reinterpret_cast<const float4*>(sX);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) x[q * 16 + k] = __uint_as_float(u[k]);
+      for (int c = 0; c < 8; ++c) {
+        const float4 pv = xin[(8 * g + c) * kRows + row];
+        const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
+        const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
+        // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+        x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
+        x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
+        x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
+        x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
+      }
+      mbar_arrive(smem_u32(&bar_x_read));
+      // causal / tail mask on raw scores (only tiles that need it)
+      const bool full_vis = ntok == kTileTok && (t0 + kTileTok - 1) * a.c + r <= qpos_min;
+      if (!full_vis) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int kk = 32 * g + k;
+          const bool vis = kk < ntok && (t0 + kk) * a.c + r <= qpos;
+          x[k] = vis ? x[k] : -INFINITY;
         }
       }
-      float tmax = -INFINITY;
+      float tmax = fmaxf(x[0], x[1]);
 #pragma unroll
-      for (int k = 0; k < kTileTok; ++k) {
-        const bool vis = (k < ntok) && ((t0 + k) * a.c + r <= qpos);
-        x[k] = vis ? x[k] * qscale : -INFINITY;
-        tmax = fmaxf(tmax, x[k]);
-      }
+      for (int k = 2; k < 32; ++k) tmax = fmaxf(tmax, x[k]);
+      // row max across the two warpgroups; this sync also orders every thread's
+      // S reads before any P write into the same TMEM columns
+      xmax_s[i & 1][g][row] = tmax;
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_max[i & 1]));
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
       // Lazy reference max: move it only when this tile's max exceeds it by more
       // than 8 (so every weight 2^(x - m_ref) stays <= 256).  Rows that move it
-      // after O holds data rescale O; the TMEM traffic is done warp-wide.
+      // after O holds data rescale O (each warpgroup its 128 columns).
       const bool move = tmax > m_ref + 8.f;
       const bool rescale_me = move && m_ref != -INFINITY;
       if (__any_sync(0xffffffffu, rescale_me)) {
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const float alpha = rescale_me ? exp2f(m_ref - tmax) : 1.f;
-        for (int q = 0; q < 16; ++q) {
+        const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+        for (int q = 0; q < 8; ++q) {
           uint32_t u[16];
-          tmem_ld16(tmem + lane_off + kColO + q * 16, u);
+          const uint32_t oc = tmem + lane_off + kColO + g * 128 + q * 16;
+          tmem_ld16(oc, u);
           tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-          tmem_st16(tmem + lane_off + kColO + q * 16, u);
+          tmem_st16(oc, u);
         }
         l *= alpha;
       }
@@ -311,28 +423,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       // P goes to the MMA as a bf16 pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)):
       // one bf16 rounding of the weights alone would cost ~1e-3 relative error in O.
       float ps = 0.f;
-      uint32_t hi[32], lo[32];
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int k = 0; k < kTileTok; k += 2) {
-        const float p0 = exp2f(x[k] - mr);
-        const float p1 = exp2f(x[k + 1] - mr);
+      for (int k = 0; k < 32; k += 2) {
+        const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+        const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
         ps += p0 + p1;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        const float2 hf = __bfloat1622float2(h);
-        hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+        const float2 hf = __bfloat1622float2(hh);
+        hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
         lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
       }
       l += ps;
       const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
-      tmem_st16(pcol, *reinterpret_cast<uint32_t(*)[16]>(&hi[0]));
-      tmem_st16(pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&hi[16]));
-      tmem_st16(pcol + 32, *reinterpret_cast<uint32_t(*)[16]>(&lo[0]));
-      tmem_st16(pcol + 48, *reinterpret_cast<uint32_t(*)[16]>(&lo[16]));
+      tmem_st16(pcol + 16 * g, hi);
+      tmem_st16(pcol + 32 + 16 * g, lo);
       if (ntok < kTileTok) {
-        // rows past the split's last token hold stale data: zero this half's V rows
-        uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStageBytes + vh * 4 * kChunkBytes);
+        // rows past the split's last token hold stale data: zero this CTA's V rows
+        uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
         const int tail = kTileTok - ntok;
-        for (int e = row; e < 4 * tail * 8; e += 128) {
+        for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
           const int cch = e / (tail * 8), rem = e % (tail * 8);
           v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
         }
@@ -344,19 +454,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
     // ---- epilogue ----
     if (ok && ntiles > 0)
-      ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bar_o), (ntiles - 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (ntiles - 1) & 1, abort_flag));
+    l_s[g][row] = l;
+    mbar_arrive(smem_u32(&bar_l));
+    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
+    ok = ok && l_ok;
+    const float l_tot = l_s[0][row] + l_s[1][row];
     tc_fence_after();
     const bool direct = p.num_splits == 1;
-    float* dst = direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL + vh * 256
-                        : p.ws_o + (((int64_t)split * a.B * a.shard_count + bz) * R + grow) * kDL +
-                              vh * 256;
+    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL
+                         : p.ws_o + (((int64_t)split * a.B * a.shard_count + bz) * R + grow) * kDL) +
+                 h * 256 + g * 128;
     const bool read_o = ok && ntiles > 0;                   // uniform across the warp
-    const bool live = read_o && l > 0.f;
-    const float inv = live ? 1.f / l : 0.f;
-    for (int q = 0; q < 16; ++q) {
+    const bool live = read_o && l_tot > 0.f;
+    const float inv = live ? 1.f / l_tot : 0.f;
+    for (int q = 0; q < 8; ++q) {
       uint32_t u[16];
       if (read_o) {
-        tmem_ld16(tmem + lane_off + kColO + q * 16, u);
+        tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
         tmem_ld_wait();
       }
       float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
@@ -366,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                                    __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (vh == 0) {
-      const float lse2 = live ? m_ref + log2f(l) : -INFINITY;
+    if (h == 0 && g == 0) {
+      const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
       if (direct)
         a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
       else
@@ -381,6 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the peer may still be writing into this CTA's exchange buffer or barriers
+  cluster_arrive();
+  cluster_wait();
   if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
   if (p.num_splits == 1) return;
 
@@ -437,6 +555,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   }
   return fn;
+}
+
+// The same pool viewed as {64 elements, rows, 9 column chunks} (a chunk is 128 B of
+// a row): one box {64, 64 rows, 4 chunks} lands as four [64 x 128 B] chunk tiles.
+int encode_rows_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return DCPMLA_ERR_CUDA;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 9};
+  cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileTok, 4};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
 
 int encode_rows_576(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
@@ -510,6 +643,10 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
     rc = encode_rows_576(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
                          (uint32_t)p.box_rows);
+  p.use3d = p.box_rows == kTileTok;
+  for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
+    if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
+      p.use3d = 0;   // fall back to one 2-D box per chunk
   if (rc == DCPMLA_OK && plan.splits > 1) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
