@@ -51,24 +51,39 @@ using namespace sm100;
 constexpr int kMaxTcShards = 8;
 constexpr int kRows = 128;
 constexpr int kTileTok = 64;
-constexpr int kChunkBytes = kTileTok * 128;          // 64 tokens x 64 bf16
+constexpr int kChunkBytes = kTileTok * 128;          // 64 tokens x 64 16-bit values
 constexpr int kStageBytes = 5 * kChunkBytes;         // room for CTA 1's five chunks
-constexpr int kStages = 4;
+constexpr int kRawChunkBytes = kTileTok * 64;        // 64 tokens x 64 E4M3 codes
+constexpr int kRawScaleOff = 5 * kRawChunkBytes;     // then the tile's 64 fp32 scales
+constexpr int kRawStageBytes = kRawScaleOff + kTileTok * 4;
+constexpr int kRawStages = 2;
 constexpr int kQropeBytes = kRows * 128;             // 64 rope dims x 128 rows
 constexpr int kXBytes = kRows * kTileTok * 4;        // one fp32 partial score tile
-constexpr int kThreads = 352;   // warps: 0 TMA, 1 MMA, 2-9 softmax, 10 release relay
 constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
-constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBytes;
 constexpr long long kWaitCycles = 2000000000LL;     // about one second
+
+// Layout per KV format.  bf16: warps 0 TMA, 1 MMA (lane 1 relays exchange-buffer
+// releases), 2-9 softmax, and a 4-deep ring of bf16 stages.  E4M3: warps 10-11
+// convert a 2-deep ring of raw E4M3 stages (codes + per-token scales) into a
+// 3-deep ring of fp16 stages, and all MMAs run in fp16.
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kStages = kFp8 ? 3 : 4;
+  static constexpr int kThreads = kFp8 ? 384 : 320;   // <= 3 warps per SM sub-partition
+  static constexpr int kConvThreads = 64;
+  static constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBytes +
+                                       (kFp8 ? kRawStages * kRawStageBytes : 0);
+};
 
 struct TcParams {
   CUtensorMap tm_q;                   // Q as [B*R, 576] bf16, box {64, 128}
-  CUtensorMap tm_kv[kMaxTcShards];    // pool (shard_begin + i) as [pool_rows, 576], box {64, box_rows}
-  CUtensorMap tm_kv3[kMaxTcShards];   // same pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
+  CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
+                                      // E4M3 pool as [pool_rows, 576] bytes, box {64, box_rows}
+  CUtensorMap tm_kv3[kMaxTcShards];   // bf16 pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
   DecodeArgs a;
   int32_t box_rows;                   // rows per TMA box: min(P, 64)
-  int32_t use3d;                      // 1: one 3-D box per 4 chunks (needs box_rows == 64)
+  int32_t use3d;                      // 1: one 3-D box per 4 chunks (bf16, needs box_rows == 64)
   int32_t num_splits, chunk, row_tiles;
   float* ws_o;
   float* ws_lse;
@@ -92,22 +107,35 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half)
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ TcParams p) {
+template <bool kFp8>
+__device__ __forceinline__ void decode_tc_body(const TcParams& p) {
+  using C = Cfg<kFp8>;
+  constexpr int kStages = C::kStages;
+  constexpr int kThreads = C::kThreads;
   const DecodeArgs& a = p.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
-  uint8_t* sKV = smem + kQropeBytes;                     // kStages x kStageBytes
+  uint8_t* sKV = smem + kQropeBytes;                     // kStages x kStageBytes (16-bit values)
   uint8_t* sX = sKV + kStages * kStageBytes;             // the peer's partial scores
+  uint8_t* sRaw = sX + kXBytes;                          // E4M3 only: raw stages
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
+  __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
   __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
-  __shared__ uint64_t bar_q_full, bar_o, bar_drain, bar_l;
+  __shared__ uint64_t bar_qr, bar_q_full, bar_o, bar_drain, bar_l;
   __shared__ float xmax_s[2][2][kRows];
   __shared__ float l_s[2][kRows];
+  __shared__ float kscale_s[kFp8 ? kStages : 1][kTileTok];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s, bad_s, last_s;
 
@@ -123,8 +151,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_full[s]), kFp8 ? C::kConvThreads : 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(smem_u32(&bar_raw_full[s]), 1);
+      mbar_init(smem_u32(&bar_raw_empty[s]), C::kConvThreads);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bar_s_full[s]), 1);
@@ -135,7 +167,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
     mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
-    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads + 1);
+    mbar_init(smem_u32(&bar_qr), 1);
+    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_s = 0;
@@ -181,8 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
       if (lane == 0) {
         prefetch_tmap(kvmap);
-        if (p.use3d) prefetch_tmap(kvmap3);
-        const uint32_t qb = smem_u32(&bar_q_full);
+        if (!kFp8 && p.use3d) prefetch_tmap(kvmap3);
+        const uint32_t qb = smem_u32(&bar_qr);
         if (h) {
           mbar_arrive_expect_tx(qb, kQropeBytes);
           tma_load_2d(smem_u32(sQr), &p.tm_q, 512, (int)(b * R + rt * kRows), qb);
@@ -190,21 +223,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive(qb);
         }
       }
+      // E4M3 tiles go to the raw ring; bf16 tiles straight to the MMA ring.
+      constexpr int ring = kFp8 ? kRawStages : kStages;
       int win_base = -64, win_val = 0, issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages) {
+        const int st = i % ring;
+        if (i >= ring) {
           bool okw = true;
           if (lane == 0)
-            okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
+            okw = wait_bar<false>(kFp8 ? smem_u32(&bar_raw_empty[st]) : smem_u32(&bar_kv_empty[st]),
+                                  ((i / ring) - 1) & 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
         }
         const int t0 = j0 + i * kTileTok;
         const int ntok = min(kTileTok, j1 - t0);
         const int box = p.box_rows;
         const int nbox = box >= kTileTok ? 1 : (ntok + box - 1) / box;
-        const uint32_t full = smem_u32(&bar_kv_full[st]);
-        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * nck));
+        const uint32_t full = kFp8 ? smem_u32(&bar_raw_full[st]) : smem_u32(&bar_kv_full[st]);
+        const int row_bytes = kFp8 ? 64 : 128;
+        // E4M3 also brings each box's per-token scales (box * 4 bytes)
+        if (lane == 0)
+          mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (row_bytes * nck + (kFp8 ? 4 : 0))));
         for (int pb = 0; pb < nbox; ++pb) {
           const int tok = t0 + pb * box;
           const int pidx = tok / a.P;
@@ -215,13 +254,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int g = __shfl_sync(0xffffffffu, win_val, pidx - win_base);
           if (lane == 0) {
             const int y = (int)((int64_t)g * a.P + (tok % a.P));
-            const uint32_t dst = smem_u32(sKV + st * kStageBytes + pb * box * 128);
-            if (p.use3d) {
-              tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
-              if (h) tma_load_2d(dst + 4 * kChunkBytes, kvmap, 512, y, full);
-            } else {
+            if (kFp8) {
+              const uint32_t dst = smem_u32(sRaw + st * kRawStageBytes + pb * box * 64);
               for (int cl = 0; cl < nck; ++cl)
-                tma_load_2d(dst + cl * kChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
+                tma_load_2d(dst + cl * kRawChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
+              bulk_load(smem_u32(sRaw + st * kRawStageBytes + kRawScaleOff + pb * box * 4),
+                        a.kv.scale[r] + y, (uint32_t)(box * 4), full);
+            } else {
+              const uint32_t dst = smem_u32(sKV + st * kStageBytes + pb * box * 128);
+              if (p.use3d) {
+                tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
+                if (h) tma_load_2d(dst + 4 * kChunkBytes, kvmap, 512, y, full);
+              } else {
+                for (int cl = 0; cl < nck; ++cl)
+                  tma_load_2d(dst + cl * kChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
+              }
             }
           }
         }
@@ -229,10 +276,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
+        for (int i = max(0, issued - ring); i < issued; ++i) {
+          const uint32_t full = kFp8 ? smem_u32(&bar_raw_full[i % ring]) : smem_u32(&bar_kv_full[i % ring]);
           const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
-                 clock64() - t0 < kWaitCycles / 8) {
+          while (!mbar_try_wait(full, (i / ring) & 1) && clock64() - t0 < kWaitCycles / 8) {
           }
         }
       }
@@ -240,8 +287,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
+      constexpr uint32_t idesc_qk =
+          kFp8 ? idesc_f16(kRows, kTileTok, false, false) : idesc_bf16(kRows, kTileTok, false, false);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(kRows, 256, false, true) : idesc_bf16(kRows, 256, false, true);
+      constexpr int kPvSteps = kFp8 ? 4 : 8;   // bf16: P as hi + lo, two MMAs per 16 tokens
       // Base descriptors; the start-address field is the low 14 bits (address >> 4),
       // so a constant byte offset is added as (offset >> 4) without carries.
       const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);            // K-major keys
@@ -278,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t pa = tmem + kColS + sb * kTileTok;
           mma_ts(to, pa, vd, idesc_pv, pi > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 1; k < 8; ++k)          // k < 4: P_hi, k >= 4: P_lo, same V rows
+          for (int k = 1; k < kPvSteps; ++k)
             mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, 1u);
           mma_commit(smem_u32(&bar_kv_empty[st]));
           mma_commit(smem_u32(&bar_o));
@@ -290,16 +339,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
       }
     }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ relay
-    // Once all softmax threads have read the peer's partial for a tile, tell
-    // the peer its next partial may overwrite our exchange buffer.  This
-    // thread has no stores in flight, so its cluster-scope release is cheap.
-    if (lane == 0) {
+    if (lane == 1) {
+      // relay: once all softmax threads have read the peer's partial for a tile,
+      // tell the peer its next partial may overwrite our exchange buffer.  This
+      // thread has no stores in flight, so its cluster-scope release is cheap.
       const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
       for (int i = 0; i < ntiles; ++i) {
         if (!wait_bar<false>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
         mbar_arrive_remote(xe_peer);
+      }
+    }
+  } else if (warp >= 10) {
+    // --------------------------------------------------- E4M3 -> fp16 convert
+    // Each 8 codes of a raw row become one 16-byte unit of the fp16 row, placed
+    // at its 128-byte-swizzle position; rows past the tile's last token are
+    // written as zeros.  Also stages the tile's per-token scales.
+    if (kFp8 && ntiles > 0) {
+      const int ct = tid - 10 * 32;                           // 0..63
+      for (int i = 0; i < ntiles; ++i) {
+        const int rs = i % kRawStages, st = i % kStages;
+        const int t0 = j0 + i * kTileTok;
+        const int ntok = min(kTileTok, j1 - t0);
+        if (!__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_raw_full[rs]), (i / kRawStages) & 1, abort_flag)))
+          break;
+        if (i >= kStages &&
+            !__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag)))
+          break;
+        const uint8_t* raw = sRaw + rs * kRawStageBytes;
+        uint8_t* dst = sKV + st * kStageBytes;
+        for (int u = ct; u < nck * kTileTok * 8; u += C::kConvThreads) {
+          const int cl = u / (kTileTok * 8), rem = u % (kTileTok * 8);
+          const int t = rem >> 3, e8 = rem & 7;
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (t < ntok) {
+            const uint2 w = *reinterpret_cast<const uint2*>(raw + cl * kRawChunkBytes + t * 64 + e8 * 8);
+            o.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFF));
+            o.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+            o.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFF));
+            o.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+          }
+          *reinterpret_cast<uint4*>(dst + cl * kChunkBytes + t * 128 + ((e8 ^ (t & 7)) << 4)) = o;
+        }
+        for (int t = ct; t < kTileTok; t += C::kConvThreads)
+          kscale_s[st][t] = t < ntok ? reinterpret_cast<const float*>(raw + kRawScaleOff)[t] : 0.f;
+        fence_proxy_async();
+        mbar_arrive(smem_u32(&bar_raw_empty[rs]));
+        mbar_arrive(smem_u32(&bar_kv_full[st]));
       }
     }
   } else {
@@ -320,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     if (ntiles > 0) {
-      // this CTA's latent dims of the query row into TMEM as packed bf16 pairs
+      // this CTA's latent dims of the query row into TMEM as packed 16-bit pairs
       const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK +
                                                          h * 256 + g * 128);
       for (int c16 = 0; c16 < 4; ++c16) {
@@ -330,13 +415,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint4 u = __ldg(qsrc + c16 * 4 + v);
           rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
         }
+        if (kFp8) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) rr[k] = bf16x2_to_f16x2(rr[k]);
+        }
         tmem_st16(tmem + lane_off + kColQ + g * 64 + c16 * 16, rr);
+      }
+      // CTA 1: the rope part of Q arrives by TMA; E4M3 runs convert it to fp16 in place
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_qr), 0, abort_flag));
+      if (kFp8 && h && ok) {
+        uint4* q4 = reinterpret_cast<uint4*>(sQr);
+        for (int u = stid; u < kQropeBytes / 16; u += kSoftmaxThreads) {
+          uint4 v = q4[u];
+          v.x = bf16x2_to_f16x2(v.x); v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z); v.w = bf16x2_to_f16x2(v.w);
+          q4[u] = v;
+        }
+        fence_proxy_async();
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_q_full));
     }
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = 0; ok && i < ntiles; ++i) {
       const int sb = i & 1, st = i % kStages;
       const int t0 = j0 + i * kTileTok;
       const int ntok = min(kTileTok, j1 - t0);
@@ -375,6 +476,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
       }
       mbar_arrive(smem_u32(&bar_x_read));
+      const float* ks = kscale_s[kFp8 ? st : 0] + 32 * g;
+      if (kFp8) {
+        // E4M3: the key's per-token scale multiplies its score
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] *= ks[k];
+      }
       // causal / tail mask on raw scores (only tiles that need it)
       const bool full_vis = ntok == kTileTok && (t0 + kTileTok - 1) * a.c + r <= qpos_min;
       if (!full_vis) {
@@ -420,34 +527,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (move) m_ref = tmax;
       const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
-      // P goes to the MMA as a bf16 pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)):
-      // one bf16 rounding of the weights alone would cost ~1e-3 relative error in O.
+      const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
       float ps = 0.f;
-      uint32_t hi[16], lo[16];
+      if (kFp8) {
+        // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
+        uint32_t pp[16];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
-        const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
-        ps += p0 + p1;
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-        const float2 hf = __bfloat1622float2(hh);
-        hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
-        lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+          const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
+          ps += p0 + p1;
+          pp[k >> 1] = pack_f16(p0 * ks[k], p1 * ks[k + 1]);
+        }
+        tmem_st16(pcol + 16 * g, pp);
+      } else {
+        // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
+        // rounding of the weights alone would cost ~1e-3 relative error in O.
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+          const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
+          ps += p0 + p1;
+          const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(hh);
+          hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+        }
+        tmem_st16(pcol + 16 * g, hi);
+        tmem_st16(pcol + 32 + 16 * g, lo);
+        if (ntok < kTileTok) {
+          // rows past the split's last token hold stale data: zero this CTA's V rows
+          uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
+          const int tail = kTileTok - ntok;
+          for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
+            const int cch = e / (tail * 8), rem = e % (tail * 8);
+            v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
       }
       l += ps;
-      const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
-      tmem_st16(pcol + 16 * g, hi);
-      tmem_st16(pcol + 32 + 16 * g, lo);
-      if (ntok < kTileTok) {
-        // rows past the split's last token hold stale data: zero this CTA's V rows
-        uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
-        const int tail = kTileTok - ntok;
-        for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
-          const int cch = e / (tail * 8), rem = e % (tail * 8);
-          v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async();
-      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_p_full[sb]));
@@ -540,6 +660,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<false>::kThreads, 1)
+    decode_tc_bf16_kernel(const __grid_constant__ TcParams p) {
+  decode_tc_body<false>(p);
+}
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<true>::kThreads, 1)
+    decode_tc_e4m3_kernel(const __grid_constant__ TcParams p) {
+  decode_tc_body<true>(p);
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::mutex mu;
@@ -568,6 +697,20 @@ int encode_rows_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
+// E4M3 pool as [rows, 576] bytes; a box {64 codes, box_rows} lands unswizzled.
+int encode_rows_576_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return DCPMLA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDK};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
@@ -619,7 +762,10 @@ TcPlan plan_tc(const DecodeArgs& a, int sm_count) {
 }  // namespace
 
 bool tc_supported(const DecodeArgs& a) {
-  if (a.fp8) return false;
+  // E4M3 scales arrive by 16-byte bulk copies: their pools must be 16-byte aligned
+  if (a.fp8)
+    for (int i = a.shard_begin; i < a.shard_begin + a.shard_count; ++i)
+      if (a.kv.scale[i] && !aligned16(a.kv.scale[i])) return false;
   if (a.R % kRows != 0 || a.shard_count > kMaxTcShards) return false;
   if (!(a.P % kTileTok == 0 || (kTileTok % a.P == 0 && a.P % 8 == 0))) return false;
   if ((int64_t)a.B * a.R > INT32_MAX || a.pool_rows > INT32_MAX) return false;
@@ -627,6 +773,19 @@ bool tc_supported(const DecodeArgs& a) {
 }
 
 size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_tc(a, sm_count).bytes; }
+
+template <bool kFp8>
+int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
+  using C = Cfg<kFp8>;
+  auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes) !=
+      cudaSuccess)
+    return DCPMLA_ERR_CUDA;
+  const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
+                  (unsigned)(p.a.B * p.a.shard_count));
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(p);
+  return launch_status();
+}
 
 int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
   const TcPlan plan = plan_tc(a, sm_count);
@@ -640,10 +799,12 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   p.chunk = plan.chunk;
   p.row_tiles = plan.row_tiles;
   int rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
-  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
-    rc = encode_rows_576(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
-                         (uint32_t)p.box_rows);
-  p.use3d = p.box_rows == kTileTok;
+  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
+    const void* pool = a.kv.pool[a.shard_begin + i];
+    rc = a.fp8 ? encode_rows_576_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows)
+               : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+  }
+  p.use3d = !a.fp8 && p.box_rows == kTileTok;
   for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
     if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
       p.use3d = 0;   // fall back to one 2-D box per chunk
@@ -659,16 +820,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     const int64_t z = (int64_t)a.B * a.shard_count;
     if (z > 65535 || plan.row_tiles > 65535 || 2LL * plan.splits > INT32_MAX) rc = DCPMLA_ERR_UNSUPPORTED;
   }
-  if (rc == DCPMLA_OK &&
-      cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes) != cudaSuccess)
-    rc = DCPMLA_ERR_CUDA;
-  if (rc == DCPMLA_OK) {
-    const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
-                    (unsigned)(a.B * a.shard_count));
-    decode_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
-    rc = launch_status();
-  }
+  if (rc == DCPMLA_OK) rc = a.fp8 ? launch_tc<true>(p, plan, st) : launch_tc<false>(p, plan, st);
   delete tp;
   return rc;
 }
