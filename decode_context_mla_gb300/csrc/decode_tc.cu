@@ -18,8 +18,7 @@
 // same sum in the same order, so both see bit-identical scores and softmax.
 //
 //   warp 0     TMA producer: 64-token KV tiles of this CTA's dims (4 or 5
-//              column chunks of 64 bf16, 128-byte swizzle) into a 3-deep ring;
-//              CTA 1 also loads the rope part of Q once.
+//              column chunks of 64 bf16, 128-byte swizzle) into the stage ring.
 //   warp 1     allocates TMEM; one thread issues the MMAs:
 //                S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; Q_h latent dims from TMEM)
 //                O_h += P V_h     (M 128, N 256, K 64; P from TMEM as a bf16 hi + lo
@@ -77,7 +76,6 @@ struct Cfg {
 };
 
 struct TcParams {
-  CUtensorMap tm_q;                   // Q as [B*R, 576] bf16, box {64, 128}
   CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
                                       // E4M3 pool as [pool_rows, 576] bytes, box {64, box_rows}
   CUtensorMap tm_kv3[kMaxTcShards];   // bf16 pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
@@ -132,7 +130,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
   __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
-  __shared__ uint64_t bar_qr, bar_q_full, bar_o, bar_drain, bar_l;
+  __shared__ uint64_t bar_q_full, bar_o, bar_drain, bar_l;
   __shared__ float xmax_s[2][2][kRows];
   __shared__ float l_s[2][kRows];
   __shared__ float kscale_s[kFp8 ? kStages : 1][kTileTok];
@@ -167,7 +165,6 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
     mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
-    mbar_init(smem_u32(&bar_qr), 1);
     mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 1);
@@ -215,13 +212,6 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
       if (lane == 0) {
         prefetch_tmap(kvmap);
         if (!kFp8 && p.use3d) prefetch_tmap(kvmap3);
-        const uint32_t qb = smem_u32(&bar_qr);
-        if (h) {
-          mbar_arrive_expect_tx(qb, kQropeBytes);
-          tma_load_2d(smem_u32(sQr), &p.tm_q, 512, (int)(b * R + rt * kRows), qb);
-        } else {
-          mbar_arrive(qb);
-        }
       }
       // E4M3 tiles go to the raw ring; bf16 tiles straight to the MMA ring.
       constexpr int ring = kFp8 ? kRawStages : kStages;
@@ -397,6 +387,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     const int stid = g * kRows + row;                        // 0..255
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
+    const bool real = grow < R;                              // rows past R pad the tile
     const int qpos = L - a.Tq + (int)(grow / a.H);
     const int qpos_min = L - a.Tq;                           // earliest query of the request
     const float qscale = a.sm_scale * kLog2e;
@@ -412,7 +403,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
         uint32_t rr[16];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 u = __ldg(qsrc + c16 * 4 + v);
+          const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
           rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
         }
         if (kFp8) {
@@ -421,15 +412,18 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
         }
         tmem_st16(tmem + lane_off + kColQ + g * 64 + c16 * 16, rr);
       }
-      // CTA 1: the rope part of Q arrives by TMA; E4M3 runs convert it to fp16 in place
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_qr), 0, abort_flag));
-      if (kFp8 && h && ok) {
-        uint4* q4 = reinterpret_cast<uint4*>(sQr);
-        for (int u = stid; u < kQropeBytes / 16; u += kSoftmaxThreads) {
-          uint4 v = q4[u];
-          v.x = bf16x2_to_f16x2(v.x); v.y = bf16x2_to_f16x2(v.y);
-          v.z = bf16x2_to_f16x2(v.z); v.w = bf16x2_to_f16x2(v.w);
-          q4[u] = v;
+      // CTA 1: the rope part of the query row (64 dims) into shared memory in the
+      // 128-byte-swizzle layout the MMA reads (fp16 for E4M3 runs); pad rows get zeros
+      if (h && g == 0) {
+        const uint4* rsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK + 512);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 v = real ? __ldg(rsrc + u) : make_uint4(0, 0, 0, 0);
+          if (kFp8) {
+            v.x = bf16x2_to_f16x2(v.x); v.y = bf16x2_to_f16x2(v.y);
+            v.z = bf16x2_to_f16x2(v.z); v.w = bf16x2_to_f16x2(v.w);
+          }
+          *reinterpret_cast<uint4*>(sQr + row * 128 + ((u ^ (row & 7)) << 4)) = v;
         }
         fence_proxy_async();
       }
@@ -594,6 +588,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
         tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
         tmem_ld_wait();
       }
+      if (!real) continue;
       float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
 #pragma unroll
       for (int v = 0; v < 4; ++v)
@@ -601,7 +596,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
                                    __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (h == 0 && g == 0) {
+    if (h == 0 && g == 0 && real) {
       const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
       if (direct)
         a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
@@ -633,7 +628,8 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   if (!last_s) return;
   __threadfence();
   const int64_t sstride = (int64_t)a.B * a.shard_count * R;
-  for (int e = tid; e < kRows * (kDL / 4); e += kThreads) {
+  const int rows_here = (int)min((long long)kRows, (long long)(R - (int64_t)rt * kRows));
+  for (int e = tid; e < rows_here * (kDL / 4); e += kThreads) {
     const int rrow = e / (kDL / 4), d4 = e % (kDL / 4);
     const int64_t base = (int64_t)bz * R + (int64_t)rt * kRows + rrow;
     float m = -INFINITY;
@@ -737,13 +733,26 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 TcPlan plan_tc(const DecodeArgs& a, int sm_count) {
   TcPlan p{};
-  p.row_tiles = a.R / kRows;
-  const int64_t units = (int64_t)a.B * a.shard_count * p.row_tiles;   // pairs of CTAs
-  const int64_t n_max = (int64_t)a.max_pages * a.P;
-  const int64_t want = std::max<int64_t>(1, (sm_count + units - 1) / std::max<int64_t>(units, 1));
-  const int64_t max_splits = std::max<int64_t>(1, n_max / 256);
-  const int64_t splits = std::min(want, max_splits);
-  int64_t chunk = (n_max + splits - 1) / splits;
+  p.row_tiles = (a.R + kRows - 1) / kRows;
+  const int64_t units = (int64_t)a.B * a.shard_count * p.row_tiles;   // clusters per split
+  const int64_t pairs = std::max(1, sm_count / 2);                    // clusters resident at once
+  const int64_t n_max = (int64_t)a.max_pages * a.P;                   // shard tokens bound
+  const int64_t tiles = std::max<int64_t>(1, (n_max + kTileTok - 1) / kTileTok);
+  // Pick the split count that minimises (waves) x (tiles per CTA + setup), with at
+  // most 256 tiles per CTA so that long and short contexts balance.
+  int64_t best = 1;
+  double best_cost = 1e300;
+  for (int64_t s = 1; s <= std::min<int64_t>(64, std::max<int64_t>(1, tiles / 4)); ++s) {
+    const int64_t per = (tiles + s - 1) / s;
+    if (per > 256 && s < std::min<int64_t>(64, tiles / 4)) continue;
+    const int64_t waves = (units * s + pairs - 1) / pairs;
+    const double cost = (double)waves * (double)(per + 16);   // setup + combine ~ 16 tiles
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  int64_t chunk = (n_max + best - 1) / best;
   chunk = (chunk + kTileTok - 1) / kTileTok * kTileTok;
   p.chunk = (int32_t)chunk;
   p.splits = (int32_t)((n_max + chunk - 1) / chunk);
@@ -766,7 +775,7 @@ bool tc_supported(const DecodeArgs& a) {
   if (a.fp8)
     for (int i = a.shard_begin; i < a.shard_begin + a.shard_count; ++i)
       if (a.kv.scale[i] && !aligned16(a.kv.scale[i])) return false;
-  if (a.R % kRows != 0 || a.shard_count > kMaxTcShards) return false;
+  if (a.shard_count > kMaxTcShards) return false;
   if (!(a.P % kTileTok == 0 || (kTileTok % a.P == 0 && a.P % 8 == 0))) return false;
   if ((int64_t)a.B * a.R > INT32_MAX || a.pool_rows > INT32_MAX) return false;
   return true;
@@ -798,7 +807,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   p.num_splits = plan.splits;
   p.chunk = plan.chunk;
   p.row_tiles = plan.row_tiles;
-  int rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
+  int rc = DCPMLA_OK;
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
     const void* pool = a.kv.pool[a.shard_begin + i];
     rc = a.fp8 ? encode_rows_576_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows)
