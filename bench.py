@@ -196,7 +196,9 @@ def recorded_traffic(workload: str, kernel: str):
     return e.get("dram_bytes_per_launch")
 
 
-DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_fma.cu",
+DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_tc.cu",
+                  "decode_context_mla_gb300/csrc/sm100.cuh",
+                  "decode_context_mla_gb300/csrc/decode_fma.cu",
                   "decode_context_mla_gb300/csrc/decode.cu",
                   "decode_context_mla_gb300/csrc/decode.cuh",
                   "decode_context_mla_gb300/csrc/common.cuh"]
@@ -308,51 +310,54 @@ def run_ours(args, w: W.Workload):
 
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
-    # warm-up eagerly once (sets kernel attributes), then capture the step and the decode alone
+    # warm-up eagerly once (sets kernel attributes), then capture the step's three phases as
+    # graphs: slot map + append, the decode (the dominant kernel), the merge
     with torch.cuda.stream(stream):
         step.run()
     torch.cuda.synchronize()
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=stream):
-        step.run()
-    from decode_context_mla_gb300 import binding as B
+    graphs = []
+    for phase in (step.run_append, step.run_decode, step.run_merge):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            phase()
+        graphs.append(g)
+    g_pre, g_dec, g_post = graphs
     c = dw.cache
-
-    def decode_only():
-        B.dcpmla_decode(step.q, c.pools, c.scales, c.kv_dtype, step.page_table, step.seq_lens,
-                        c.P, c.c, 0, c.c, step.sm_scale, step.lse_base, step.o_part,
-                        step.lse_part, step.workspace, c.err)
-
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dec, stream=stream):
-        decode_only()
     torch.cuda.synchronize()
 
-    def timed(graph, k):
-        """Sum of per-step device times (ms) over k replays, flushing L2 between steps if small."""
+    def replay_step():
+        g_pre.replay()
+        g_dec.replay()
+        g_post.replay()
+
+    def timed(k):
+        """(step ms summed over k steps, decode-launch ms summed over k steps), device clocks.
+
+        Events on the launching stream bracket every step and, inside it, the decode
+        launch; with a small cache L2 is flushed between steps, outside the brackets."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(k)]
         with torch.cuda.stream(stream):
-            if flush is None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(k):
-                    graph.replay()
-                e1.record(stream)
-                e1.synchronize()
-                return e0.elapsed_time(e1)
-            tot = 0.0
-            for _ in range(k):
-                flush.add_(1)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-                e1.synchronize()
-                tot += e0.elapsed_time(e1)
-            return tot
+            for i in range(k):
+                if flush is not None:
+                    flush.add_(1)
+                ev[i][0].record(stream)
+                g_pre.replay()
+                ev[i][1].record(stream)
+                g_dec.replay()
+                ev[i][2].record(stream)
+                g_post.replay()
+                ev[i][3].record(stream)
+        ev[-1][3].synchronize()
+        dec = sum(e[1].elapsed_time(e[2]) for e in ev)
+        if flush is None:
+            tot = ev[0][0].elapsed_time(ev[-1][3])
+        else:
+            tot = sum(e[0].elapsed_time(e[3]) for e in ev)
+        return tot, dec
 
     for _ in range(args.warmup):
         with torch.cuda.stream(stream):
-            g_step.replay()
+            replay_step()
     torch.cuda.synchronize()
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     sampler = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
@@ -360,17 +365,16 @@ def run_ours(args, w: W.Workload):
     time.sleep(0.3)
     for _ in range(args.warmup):        # bring the clocks back up after the pause
         with torch.cuda.stream(stream):
-            g_step.replay()
+            replay_step()
     torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    ms_total = timed(g_step, args.steps)
+    ms_total, ms_dec_total = timed(args.steps)
     t_wall1 = time.time()
     torch.cuda.synchronize()
     barrier(ws)
-    # the dominant kernel alone, same stream
-    ms_dec = timed(g_dec, max(args.steps, 5)) / max(args.steps, 5)
+    ms_dec = ms_dec_total / args.steps
     time.sleep(0.15)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
@@ -395,7 +399,7 @@ def run_ours(args, w: W.Workload):
                    "frac": round(tflops / peaks["bf16_tflops"], 4)}
 
     # end to end through the public API from pinned host buffers
-    e2e = run_e2e(args, w, dw, g_step, stream, acc, ws)
+    e2e = run_e2e(args, w, dw, stream, acc, ws)
 
     # CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -426,7 +430,7 @@ def run_ours(args, w: W.Workload):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, dw, g_step, stream, acc, ws):
+def run_e2e(args, w, dw, stream, acc, ws):
     """Same metric through the public step call from pinned host buffers (copies timed)."""
     import dcp_harness as Hn
     step = dw.step
@@ -440,14 +444,7 @@ def run_e2e(args, w, dw, g_step, stream, acc, ws):
 
     def one():
         with torch.cuda.stream(stream):
-            step.q.copy_(q_h, non_blocking=True)
-            step.new_ckv.copy_(ckv_h, non_blocking=True)
-            step.new_krope.copy_(krope_h, non_blocking=True)
-            if sc_h is not None:
-                step.new_scales.copy_(sc_h, non_blocking=True)
-            g_step.replay()
-            o_h.copy_(step.o, non_blocking=True)
-            lse_h.copy_(step.lse, non_blocking=True)
+            step.run_host(q_h, ckv_h, krope_h, sc_h, o_h, lse_h)
 
     for _ in range(max(3, args.warmup)):
         one()
@@ -463,7 +460,9 @@ def run_e2e(args, w, dw, g_step, stream, acc, ws):
     ms = max_over_ranks(e0.elapsed_time(e1) / k, ws)
     return {"value": round(acc["kv_bytes"] * ws / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": step.h2d_bytes(),
-            "d2h_bytes_per_step": step.d2h_bytes()}
+            "d2h_bytes_per_step": step.d2h_bytes(),
+            "path": "DecodeStep.run_host: pinned host inputs -> slot map, append, decode, merge "
+                    "-> pinned host outputs, eager launches"}
 
 
 def main():
@@ -475,10 +474,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this many requests (small profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = W.WORKLOADS[args.config]
+    if args.batch:
+        w = W.scaled(w, B=args.batch, name=f"{w.name}_b{args.batch}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -125,13 +125,27 @@ class DecodeStep:
 
     def run(self, stream=None) -> None:
         """Enqueue one step on the current (or given) stream."""
+        self.run_append(stream)
+        self.run_decode(stream)
+        self.run_merge(stream)
+
+    def run_append(self, stream=None) -> None:
+        """Slot map + KV append of the step's new tokens (nothing when append is off)."""
         c = self.cache
         if self.do_append:
             c.append(self.page_table, self.new_req, self.new_pos, self.new_ckv, self.new_krope,
                      self.new_scales, self.owner, self.phys, None, stream)
+
+    def run_decode(self, stream=None) -> None:
+        """Shard-local decode of all c shards: o_part, lse_part."""
+        c = self.cache
         B.dcpmla_decode(self.q, c.pools, c.scales, c.kv_dtype, self.page_table, self.seq_lens, c.P,
                         c.c, 0, c.c, self.sm_scale, self.lse_base, self.o_part, self.lse_part,
                         self.workspace, c.err, stream)
+
+    def run_merge(self, stream=None) -> None:
+        """Exact LSE merge of the c partials into o, lse."""
+        c = self.cache
         B.dcpmla_lse_merge(self.o_part, self.lse_part, c.c, self.Bn * self.R, self.lse_base,
                            self.o, self.lse, c.err, stream)
 
