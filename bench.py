@@ -196,7 +196,12 @@ def recorded_traffic(workload: str, kernel: str):
     return e.get("dram_bytes_per_launch")
 
 
-DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_tc.cu",
+DECODE_KERNELS = {1: "decode_fh_bf16_kernel + fh_combine_kernel (tokens as MMA M)",
+                  2: "decode_tc_bf16/e4m3_kernel (128-row tiles)",
+                  3: "decode_fma_kernel (CUDA cores)"}
+
+DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_fewhead.cu",
+                  "decode_context_mla_gb300/csrc/decode_tc.cu",
                   "decode_context_mla_gb300/csrc/sm100.cuh",
                   "decode_context_mla_gb300/csrc/decode_fma.cu",
                   "decode_context_mla_gb300/csrc/decode.cu",
@@ -323,6 +328,9 @@ def run_ours(args, w: W.Workload):
         graphs.append(g)
     g_pre, g_dec, g_post = graphs
     c = dw.cache
+    from decode_context_mla_gb300 import binding as B
+    path, dec_launches = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, c.kv_dtype,
+                                              step.page_table.shape[1])
     torch.cuda.synchronize()
 
     def replay_step():
@@ -390,7 +398,7 @@ def run_ours(args, w: W.Workload):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": recorded_traffic(w.name, "decode"),
-                "kernel": "dcpmla decode (all c shards, one launch)",
+                "kernel": "dcpmla_decode (all c shards): " + DECODE_KERNELS[path],
                 "kernel_ms": round(ms_dec, 4),
                 "algorithmic_bytes": acc["decode_bytes"],
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
@@ -410,7 +418,8 @@ def run_ours(args, w: W.Workload):
                "sample": f"fp64 oracle (striped decode + merge) on {n} whole request(s) of the "
                          f"{w.name} workload, {t:.1f} s of CPU work"}
 
-    launches_per_step = 4 if step.do_append else 3
+    # slot map + append (when the step appends), the decode's kernels, the merge
+    launches_per_step = (2 if step.do_append else 0) + dec_launches + 1
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,

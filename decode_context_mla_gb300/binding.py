@@ -213,6 +213,18 @@ def dcpmla_decode_workspace_size(B: int, Tq: int, H: int, P: int, c: int, shard_
     return out.value
 
 
+PATH_TC_FEWHEAD, PATH_TC_ROWS, PATH_CUDA_CORE = 1, 2, 3
+
+
+def dcpmla_decode_path(B: int, Tq: int, H: int, P: int, c: int, shard_count: int,
+                       kv_dtype: int, max_pages: int) -> tuple:
+    """(path, kernel launches per dcpmla_decode call) for this shape on the current device."""
+    path, n = C.c_int32(), C.c_int32()
+    _check(lib().dcpmla_decode_path(B, Tq, H, P, c, shard_count, kv_dtype, max_pages,
+                                    C.byref(path), C.byref(n)), "dcpmla_decode_path")
+    return path.value, n.value
+
+
 def dcpmla_decode(q: torch.Tensor, pools: Sequence[torch.Tensor],
                   scale_pools: Optional[Sequence[torch.Tensor]], kv_dtype: int,
                   page_table: torch.Tensor, seq_lens: torch.Tensor, P: int, c: int,

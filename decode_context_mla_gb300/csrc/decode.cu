@@ -56,9 +56,11 @@ int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* 
   return DCPMLA_OK;
 }
 
-// Shapes whose query rows fill 128-row tensor-core tiles run on tcgen05; the
-// rest (few heads, e4m3 KV for now) on the CUDA-core kernel.
+// Few query rows (<= 16, bf16 KV) run on the token-major tensor-core kernel;
+// other shapes the tensor cores take run on the 128-row-tile kernel; the rest
+// on the CUDA-core kernel.
 size_t workspace_for(const DecodeArgs& a, int sm) {
+  if (fh_supported(a, sm)) return fh_workspace_bytes(a, sm);
   return tc_supported(a) ? tc_workspace_bytes(a, sm) : fma_workspace_bytes(a, sm);
 }
 
@@ -81,6 +83,27 @@ int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, in
   return DCPMLA_OK;
 }
 
+int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, int32_t shard_count,
+                       int32_t kv_dtype, int32_t max_pages, int32_t* path, int32_t* kernel_launches) {
+  DecodeArgs a;
+  const int st = fill_args(a, nullptr, nullptr, nullptr, kv_dtype, 0, nullptr, max_pages, nullptr,
+                           B, Tq, H, P, c, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
+                           nullptr, false);
+  if (st != DCPMLA_OK) return st;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  int pth = DCPMLA_PATH_CUDA_CORE, n = 1;
+  if (fh_supported(a, sm)) {
+    pth = DCPMLA_PATH_TC_FEWHEAD;
+    n = 2;   // decode + merge of split units
+  } else if (tc_supported(a)) {
+    pth = DCPMLA_PATH_TC_ROWS;
+  }
+  if (path) *path = pth;
+  if (kernel_launches) *kernel_launches = B == 0 ? 0 : n;
+  return DCPMLA_OK;
+}
+
 int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools, int32_t kv_dtype,
                   int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
                   const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P,
@@ -95,6 +118,7 @@ int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools
   if (B == 0) return DCPMLA_OK;
   const int sm = device_sm_count();
   if (sm <= 0) return DCPMLA_ERR_CUDA;
+  if (fh_supported(a, sm)) return launch_decode_fh(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
   if (tc_supported(a)) return launch_decode_tc(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
   return launch_decode_fma(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
 }

@@ -1,6 +1,8 @@
 // Arguments of one dcpmla_decode call after host-side validation, shared by
 // the decode kernels.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace dcpmla {
@@ -22,7 +24,16 @@ struct DecodeArgs {
   int32_t* err;
 };
 
-// Tensor-core path (tcgen05 / TMEM / TMA): 128-row query tiles, bf16 KV.
+// 2-D tensor map over a row-major bf16 matrix [rows, cols] with 128-byte swizzle.
+int tma_encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                       uint32_t box_rows);
+
+// Tensor-core path for few query rows (<= 16): KV tokens are the MMA's M dimension.
+bool fh_supported(const DecodeArgs& a, int sm_count);
+size_t fh_workspace_bytes(const DecodeArgs& a, int sm_count);
+int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st);
+
+// Tensor-core path (tcgen05 / TMEM / TMA): 128-row query tiles, bf16 or e4m3 KV.
 bool tc_supported(const DecodeArgs& a);
 size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count);
 int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st);

@@ -1,0 +1,856 @@
+// Shard-local absorbed-MLA decode on the 5th-generation tensor cores for few
+// query rows (heads x query tokens <= 16), where the rows are too few to fill an
+// MMA's M dimension but the KV tokens are not: the contractions run transposed.
+//
+// SGLang "Decode Context Parallelism" docs, MLA decode dataflow: each shard
+// returns its locally normalised o_r and lse_r; DCP x speculative decoding:
+// the causal test uses global positions (shard-local token j of shard r is
+// position j*c + r).  vLLM GLM-5.3 serving post, footnote arithmetic: scores
+// over the 576-d key, values over the 512-d latent.
+//
+//   S^T [128 tokens x 16 rows]  = K [128 x 576] Q^T          (M = tokens, N = rows)
+//   O^T [512 dims x 16 rows]   += V^T [512 x 128] P^T         (M = dims,  N = rows)
+//
+// One CLUSTER of two CTAs streams one work unit at a time: a run of 128-token
+// tiles of one (request, shard).  CTA h = 0 owns key dims [0, 256), CTA 1 owns
+// [256, 576); each computes a partial S^T over its dims and the partials are
+// exchanged through distributed shared memory, so both CTAs hold the same
+// scores.  The latent dims a CTA owns are its half of the value dims.
+//
+// The grid is persistent: each CTA computes the same split of all (request,
+// shard) token ranges into units of equal tile count (about 16 units per
+// cluster), and cluster k takes units k, k + G, k + 2G, ...  The units of a
+// (request, shard) cut into several write fp32 partials that a small second
+// kernel merges.
+//
+//   warp 0     TMA producer: Q^T of the unit (one 16-row box per 64-dim chunk),
+//              then 128-token KV tiles (one 2-D box per page and 64-dim chunk)
+//              into a 2-deep stage ring.
+//   warp 1     lane 0 issues the MMAs, lane 1 relays "exchange buffer read" to
+//              the peer.  QK: M 128, N 16; PV: M 128 (V^T MN-major), N 32 = P as a
+//              bf16 hi part (rows 0-15) and lo part (rows 16-31).
+//   warps 2-9  softmax, one thread per token lane, two warpgroups of 8 query
+//              rows each: base-2 online softmax with a lazily moved per-row
+//              reference max, P^T to shared memory, unit epilogue.
+//
+// TMEM columns: S^T double buffer [0, 32), O^T double buffer (by unit) [64, 192):
+// buffer o, value block m (128 dims): hi rows at 64 + 64o + 32m, lo rows 16 later.
+// Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all roles
+// drain, both CTAs meet at the final cluster barrier, TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "decode.cuh"
+#include "sm100.cuh"
+
+namespace dcpmla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kMaxFhShards = 8;
+constexpr int kTok = 128;                      // tokens per tile = MMA M of the score product
+constexpr int kRp = 16;                        // query rows per tile (MMA N); rows >= R are padding
+constexpr int kChunk = kTok * 128;             // one 64-dim column chunk of a tile: 16 KB
+constexpr int kStage = 5 * kChunk;             // room for CTA 1's five chunks
+constexpr int kStages = 2;
+constexpr int kQChunk = kRp * 128;             // Q^T chunk [16 rows x 64 dims]
+constexpr int kQBuf = 5 * kQChunk;
+constexpr int kPChunk = 2 * kRp * 128;         // P^T chunk [32 rows (hi, lo) x 64 tokens]
+constexpr int kPBuf = 2 * kPChunk;             // 128 tokens
+constexpr int kXBytes = kTok * kRp * 4;        // one fp32 partial S^T tile
+constexpr int kMaxItems = 2048;                // (request, shard) pairs per launch
+constexpr int kUnitsPerCluster = 16;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr uint32_t kColS = 0, kColO = 64, kTmemCols = 256;
+constexpr long long kWaitCycles = 2000000000LL;   // about one second
+
+constexpr int kOffKV = 0;
+constexpr int kOffQ = kOffKV + kStages * kStage;
+constexpr int kOffP = kOffQ + 2 * kQBuf;
+constexpr int kOffX = kOffP + 2 * kPBuf;
+constexpr int kOffPre = kOffX + kXBytes;
+constexpr size_t kSmemBytes = 1024 + kOffPre + (kMaxItems + 1) * 4;
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffX % 1024 == 0, "1 KB aligned buffers");
+
+struct FhParams {
+  CUtensorMap tm_kv[kMaxFhShards];   // pool as [pool_rows, 576] bf16, box {64, box_rows}
+  CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
+  DecodeArgs a;
+  int32_t box_rows;                  // rows per TMA box: min(P, 128)
+  int32_t max_units;
+  float* ws_o;                       // [max_units, R, 512]
+  float* ws_lse;                     // [max_units, R] (base 2)
+  int32_t* ws_bad;                   // [max_units]: the unit needed a page outside the pools
+  int32_t* ws_pre;                   // [B * shard_count + 1]: first unit of each (request, shard)
+};
+
+template <bool kCluster>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (true) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Tokens of request b on shard r (0 for a length the launch rejects).
+__device__ __forceinline__ int shard_tokens(const DecodeArgs& a, int L, int r) {
+  if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) return 0;
+  return L > r ? (L - r + a.c - 1) / a.c : 0;
+}
+
+struct Unit {
+  int item, b, sr, r, L;
+  int j0, j1, ntiles;   // shard-local token range and its 128-token tiles
+  int nch, first;       // units of the item, and the item's first unit
+};
+
+__device__ __forceinline__ Unit get_unit(const DecodeArgs& a, const int* pre, int nitems, int chunk_tiles,
+                                         int u) {
+  int lo = 0, hi = nitems;   // pre[lo] <= u < pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  Unit x;
+  x.item = lo;
+  x.b = lo / a.shard_count;
+  x.sr = lo % a.shard_count;
+  x.r = a.shard_begin + x.sr;
+  x.L = __ldg(a.seq_lens + x.b);
+  const int n = shard_tokens(a, x.L, x.r);
+  const int tiles = (n + kTok - 1) / kTok;
+  x.first = pre[lo];
+  x.nch = pre[lo + 1] - pre[lo];
+  const int tb = (u - x.first) * chunk_tiles;
+  const int te = min(tiles, tb + chunk_tiles);
+  x.ntiles = max(0, te - tb);
+  x.j0 = min(n, tb * kTok);
+  x.j1 = min(n, te * kTok);
+  return x;
+}
+
+// Byte offset of element (row, token t64) in a K-major, 128-byte-swizzled
+// [rows x 64] bf16 tile (8-row atoms of 1 KB).
+__device__ __forceinline__ uint32_t sw128_off(int row, int t64) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((t64 >> 3) ^ (row & 7))) << 4) + (t64 & 7) * 2);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_fh_bf16_kernel(const __grid_constant__ FhParams p) {
+  const DecodeArgs& a = p.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sKV = smem + kOffKV;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sP = smem + kOffP;
+  uint8_t* sX = smem + kOffX;
+  int* sPre = reinterpret_cast<int*>(smem + kOffPre);
+  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
+  __shared__ uint64_t bar_q_full[2], bar_q_free[2];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_p_free[2], bar_o_free[2];
+  __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
+  __shared__ uint64_t bar_o, bar_drain;
+  __shared__ __align__(16) float red_s[2][2][4][8];     // [tile parity][warpgroup][quarter][row]
+  __shared__ __align__(16) float lsum_s[2][2][4][8];   // [unit parity][warpgroup][quarter][row]
+  __shared__ int seg_s[kThreads];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s, total_s, ubad_s[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t h = cluster_ctarank();
+  const uint32_t peer = h ^ 1u;
+  const int nck = h ? 5 : 4;
+  const int G = (int)(gridDim.x >> 1), cl = (int)(blockIdx.x >> 1);
+  const int nitems = a.B * a.shard_count;
+  const int64_t R = a.R;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_q_full[s]), 1);
+      mbar_init(smem_u32(&bar_q_free[s]), 1);
+      mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);
+      mbar_init(smem_u32(&bar_p_free[s]), 1);
+      mbar_init(smem_u32(&bar_o_free[s]), kSoftmaxThreads);
+    }
+    mbar_init(smem_u32(&bar_x_full), 1);
+    mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
+    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_s = 0;
+    total_s = 0;
+    ubad_s[0] = ubad_s[1] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+
+  // ---- work split, computed identically by every CTA ----
+  // tiles per item into sPre[item + 1], then units per item, then the prefix sum
+  {
+    int local = 0;
+    for (int it = tid; it < nitems; it += kThreads) {
+      const int b = it / a.shard_count, r = a.shard_begin + it % a.shard_count;
+      const int L = __ldg(a.seq_lens + b);
+      if (blockIdx.x == 0 && (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c))
+        set_err(a.err, DCPMLA_DERR_LENGTH);
+      const int t = (shard_tokens(a, L, r) + kTok - 1) / kTok;
+      sPre[it + 1] = t;
+      local += t;
+    }
+    atomicAdd(&total_s, local);
+  }
+  __syncthreads();
+  const int chunk_tiles =
+      max(1, (int)(((int64_t)total_s + (int64_t)G * kUnitsPerCluster - 1) / ((int64_t)G * kUnitsPerCluster)));
+  const int seg = (nitems + kThreads - 1) / kThreads;
+  const int s0 = min(nitems, tid * seg), s1 = min(nitems, s0 + seg);
+  {
+    int sum = 0;
+    for (int it = s0; it < s1; ++it) {
+      const int units = max(1, (sPre[it + 1] + chunk_tiles - 1) / chunk_tiles);
+      sPre[it + 1] = units;
+      sum += units;
+    }
+    seg_s[tid] = sum;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kPer = kThreads / 32;
+    int tot = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) tot += seg_s[lane * kPer + k];
+    int incl = tot;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - tot;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int v = seg_s[lane * kPer + k];
+      seg_s[lane * kPer + k] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  {
+    int run = seg_s[tid];
+    if (tid == 0) sPre[0] = 0;
+    for (int it = s0; it < s1; ++it) {
+      run += sPre[it + 1];
+      sPre[it + 1] = run;
+    }
+  }
+  __syncthreads();
+  const int units = sPre[nitems];
+  if (blockIdx.x == 0)
+    for (int it = tid; it <= nitems; it += kThreads) p.ws_pre[it] = sPre[it];
+
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[i]);
+    }
+    bool ok = true;
+    int gi = 0, kk = 0, issued = 0;
+    for (int u = cl; ok && u < units; u += G) {
+      const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
+      if (x.ntiles == 0) continue;
+      const int qb = kk & 1;
+      const int32_t* pt_row = a.pt + (int64_t)x.b * a.max_pages;
+      const CUtensorMap* kvmap = &p.tm_kv[x.sr];
+      bool okq = true;
+      if (lane == 0) {
+        if (kk >= 2) okq = wait_bar<false>(smem_u32(&bar_q_free[qb]), ((kk >> 1) - 1) & 1, abort_flag);
+        if (okq) {
+          const uint32_t qf = smem_u32(&bar_q_full[qb]);
+          mbar_arrive_expect_tx(qf, (uint32_t)(nck * kQChunk));
+          for (int c = 0; c < nck; ++c)
+            tma_load_2d(smem_u32(sQ + qb * kQBuf + c * kQChunk), &p.tm_q, (int)(4 * h + c) * 64,
+                        (int)(x.b * R), qf);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, (int)okq, 0) != 0;
+      for (int i = 0; ok && i < x.ntiles; ++i, ++gi) {
+        const int st = gi & 1;
+        const int t0 = x.j0 + i * kTok;
+        const int ntok = min(kTok, x.j1 - t0);
+        const int box = p.box_rows;
+        const int nbox = (ntok + box - 1) / box;
+        // page of each box (lane < nbox); a bad page id is reported and read as page 0
+        int y = 0;
+        if (lane < nbox) {
+          const int tok = t0 + lane * box;
+          int g = __ldg(pt_row + tok / a.P);
+          if (g < 0 || (int64_t)g >= a.num_pages) {
+            set_err(a.err, DCPMLA_DERR_PAGE);
+            g = 0;
+          }
+          y = g * a.P + tok % a.P;
+        }
+        bool okw = true;
+        if (lane == 0 && gi >= kStages)
+          okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((gi >> 1) - 1) & 1, abort_flag);
+        ok = __shfl_sync(0xffffffffu, (int)okw, 0) != 0;
+        if (!ok) break;
+        const uint32_t full = smem_u32(&bar_kv_full[st]);
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * nck));
+        __syncwarp();
+        if (lane < nbox) {
+          const uint32_t dst = smem_u32(sKV + st * kStage + lane * box * 128);
+          for (int c = 0; c < nck; ++c) tma_load_2d(dst + c * kChunk, kvmap, (int)(4 * h + c) * 64, y, full);
+        }
+        issued = gi + 1;
+      }
+      ++kk;
+    }
+    if (lane == 0 && *abort_flag) {
+      // let copies already in flight land before the CTA's shared memory goes away
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&bar_kv_full[i & 1]), (i >> 1) & 1) && clock64() - t0 < kWaitCycles / 8) {
+        }
+      }
+      for (int q = 0; q < 2; ++q) {
+        const int k = kk - 1 - q;   // the last two Q loads
+        if (k < 0) break;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&bar_q_full[k & 1]), (k >> 1) & 1) && clock64() - t0 < kWaitCycles / 8) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA
+      // Polls its barriers and issues whichever is ready: the oldest tile's PV (its
+      // P is written; first, since it frees the tile's stage for the next load) or
+      // the next tile's QK (its KV landed, and the score buffer it overwrites was
+      // consumed: at most one tile ahead of the oldest PV).
+      constexpr uint32_t idesc_qk = idesc_bf16(kTok, kRp, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, false);
+      // Base descriptors; the start-address field is the low 14 bits (address >> 4),
+      // so a constant byte offset is added as (offset >> 4) without carries.
+      const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, 1024);        // keys, K-major
+      const uint64_t vA0 = desc_sw128(smem_u32(sKV), kChunk, 1024);    // values, MN-major
+      const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
+      const uint64_t pB0 = desc_sw128(smem_u32(sP), 16, 1024);         // P^T, K-major
+      int total = 0;
+      for (int u = cl; u < units; u += G) total += get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
+      // QK cursor over this cluster's non-empty units
+      int uq = cl, iq = 0, kkq = 0, ntq = 0;
+      bool q_ready = false;
+      while (uq < units && (ntq = get_unit(a, sPre, nitems, chunk_tiles, uq).ntiles) == 0) uq += G;
+      int gq = 0, gp = 0;                 // next tile to QK / to PV
+      int pv_ob[2], pv_kk[2];
+      bool pv_first[2];
+      long long t_idle = clock64();
+      while (gp < total) {
+        bool progressed = false;
+        if (gp < gq) {
+          const int sb = gp & 1;
+          const bool first = pv_first[sb];
+          const int ob = pv_ob[sb], kk = pv_kk[sb];
+          if (mbar_test_wait(smem_u32(&bar_p_full[sb]), (gp >> 1) & 1) &&
+              (!first || kk < 2 || mbar_test_wait(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1))) {
+            tc_fence_after();
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+              const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * kChunk + ks * 2048) >> 4);
+                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + (ks >> 2) * kPChunk + (ks & 3) * 32) >> 4);
+                mma_ss(d, ad, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
+              }
+            }
+            mma_commit(smem_u32(&bar_kv_empty[sb]));
+            mma_commit(smem_u32(&bar_p_free[sb]));
+            mma_commit(smem_u32(&bar_o));
+            ++gp;
+            progressed = true;
+          }
+        }
+        if (gq < total && gq - gp < 2) {
+          const int qb = kkq & 1;
+          if (!q_ready) q_ready = mbar_test_wait(smem_u32(&bar_q_full[qb]), (kkq >> 1) & 1);
+          const int sb = gq & 1;
+          if (q_ready && mbar_test_wait(smem_u32(&bar_kv_full[sb]), (gq >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
+#pragma unroll
+            for (int c = 0; c < 5; ++c) {
+              if (c >= nck) break;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ss(d, kA0 + (uint64_t)((sb * kStage + c * kChunk + k * 32) >> 4),
+                       qB0 + (uint64_t)((qb * kQBuf + c * kQChunk + k * 32) >> 4), idesc_qk, (c | k) != 0);
+            }
+            mma_commit(smem_u32(&bar_s_full[sb]));
+            pv_ob[sb] = kkq & 1;
+            pv_kk[sb] = kkq;
+            pv_first[sb] = iq == 0;
+            if (++iq == ntq) {               // last tile of the unit: its Q buffer may be refilled
+              mma_commit(smem_u32(&bar_q_free[qb]));
+              iq = 0;
+              ++kkq;
+              q_ready = false;
+              uq += G;
+              while (uq < units && (ntq = get_unit(a, sPre, nitems, chunk_tiles, uq).ntiles) == 0) uq += G;
+            }
+            ++gq;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_idle = clock64();
+        } else if (*abort_flag) {
+          break;
+        } else if (clock64() - t_idle > kWaitCycles) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+      // drain: every MMA issued above completes before TMEM is released
+      mma_commit(smem_u32(&bar_drain));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    } else if (lane == 1) {
+      // relay: once all softmax threads have read the peer's partial for a tile,
+      // tell the peer its next partial may overwrite this CTA's exchange buffer
+      int total = 0;
+      for (int u = cl; u < units; u += G) total += get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
+      const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
+      for (int gi = 0; gi < total; ++gi) {
+        if (!wait_bar<false>(smem_u32(&bar_x_read), gi & 1, abort_flag)) break;
+        mbar_arrive_remote(xe_peer);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    // Warps 2..9: warpgroup g handles query rows [8g, 8g + 8); the thread's TMEM
+    // lane is its token within the tile (for S^T) and its value dim (for O^T).
+    const int g = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int tok = quarter * 32 + lane;
+    const int stid = g * 128 + tok;                          // 0..255
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float qscale = a.sm_scale * kLog2e;
+    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
+    const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
+    bool ok = true;
+    int gi = 0, kk = 0, uc = 0;
+    for (int u = cl; ok && u < units; u += G, ++uc) {
+      const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
+      const int ob = kk & 1;
+      const int up = uc & 1;
+      int qpos[8];
+      bool rvalid[8];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int row = 8 * g + n;
+        rvalid[n] = row < R;
+        qpos[n] = x.L - a.Tq + (rvalid[n] ? row / a.H : 0);
+      }
+      const int qpos_min = x.L - a.Tq;
+      const bool all_rows = R >= kRp;
+      const int32_t* pt_row = a.pt + (int64_t)x.b * a.max_pages;
+      bool bad = false;   // a page this thread's tokens need is outside the pools
+      float m_ref[8], lt[8];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        m_ref[n] = -INFINITY;
+        lt[n] = 0.f;
+      }
+      for (int i = 0; ok && i < x.ntiles; ++i, ++gi) {
+        const int sb = gi & 1;
+        const int t0 = x.j0 + i * kTok;
+        const int ntok = min(kTok, x.j1 - t0);
+        if (tok < ntok) {
+          const int gpg = __ldg(pt_row + (t0 + tok) / a.P);
+          bad |= gpg < 0 || (int64_t)gpg >= a.num_pages;
+        }
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t own[8];
+        tmem_ld8(tmem + lane_off + kColS + (uint32_t)(sb * kRp + 8 * g), own);
+        tmem_ld_wait();
+        // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
+        if (gi >= 1) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+          st_async_v4(x_remote + (uint32_t)(((2 * g + v) * kTok + tok) * 16),
+                      make_uint4(own[4 * v], own[4 * v + 1], own[4 * v + 2], own[4 * v + 3]), xfull_remote);
+        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), gi & 1, abort_flag));
+        if (!ok) break;
+        float s[8];
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const float4 pv = reinterpret_cast<const float4*>(sX)[(2 * g + v) * kTok + tok];
+          const float o0 = __uint_as_float(own[4 * v]), o1 = __uint_as_float(own[4 * v + 1]);
+          const float o2 = __uint_as_float(own[4 * v + 2]), o3 = __uint_as_float(own[4 * v + 3]);
+          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+          s[4 * v + 0] = h ? pv.x + o0 : o0 + pv.x;
+          s[4 * v + 1] = h ? pv.y + o1 : o1 + pv.y;
+          s[4 * v + 2] = h ? pv.z + o2 : o2 + pv.z;
+          s[4 * v + 3] = h ? pv.w + o3 : o3 + pv.w;
+        }
+        mbar_arrive(smem_u32(&bar_x_read));
+        // causal / tail / padding-row mask, base-2 scaling
+        const bool full_vis = all_rows && ntok == kTok && (int64_t)(t0 + kTok - 1) * a.c + x.r <= qpos_min;
+        const int64_t kpos = (int64_t)(t0 + tok) * a.c + x.r;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const bool vis = full_vis || (rvalid[n] && tok < ntok && kpos <= qpos[n]);
+          s[n] = vis ? s[n] * qscale : -INFINITY;
+        }
+        // Lazy reference max: a row moves it only when this tile's max exceeds it
+        // by more than 8 (every weight 2^(s - m_ref) stays <= 256); rows that move
+        // it after O holds data rescale their O^T columns and partial sums.  Whether
+        // any row of the warpgroup moves is one barrier-OR; only then is the tile's
+        // exact per-row max formed (warp reduction, then across the 4 warps).
+        bool over = false;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) over |= s[n] > m_ref[n] + 8.f;
+        if (named_bar_or(1 + g, 128, over)) {
+          float wm[8];
+#pragma unroll
+          for (int n = 0; n < 8; ++n) wm[n] = warp_max_f32(s[n]);
+          if (lane == 0) {
+            float4* dst = reinterpret_cast<float4*>(red_s[sb][g][quarter]);
+            dst[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
+            dst[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
+          }
+          named_bar_sync(1 + g, 128);
+          float tmax[8];
+#pragma unroll
+          for (int n = 0; n < 8; ++n) tmax[n] = -INFINITY;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 m0 = reinterpret_cast<const float4*>(red_s[sb][g][q])[0];
+            const float4 m1 = reinterpret_cast<const float4*>(red_s[sb][g][q])[1];
+            tmax[0] = fmaxf(tmax[0], m0.x); tmax[1] = fmaxf(tmax[1], m0.y);
+            tmax[2] = fmaxf(tmax[2], m0.z); tmax[3] = fmaxf(tmax[3], m0.w);
+            tmax[4] = fmaxf(tmax[4], m1.x); tmax[5] = fmaxf(tmax[5], m1.y);
+            tmax[6] = fmaxf(tmax[6], m1.z); tmax[7] = fmaxf(tmax[7], m1.w);
+          }
+          bool any_rescale = false;
+          float alpha[8];
+#pragma unroll
+          for (int n = 0; n < 8; ++n) {
+            const bool mv = tmax[n] > m_ref[n] + 8.f;
+            const bool rs = mv && m_ref[n] != -INFINITY;
+            alpha[n] = rs ? ex2_approx(m_ref[n] - tmax[n]) : 1.f;
+            any_rescale |= rs;
+            if (mv) m_ref[n] = tmax[n];
+          }
+          if (any_rescale) {   // the same decision in every thread of the warpgroup
+            ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll
+              for (int part = 0; part < 2; ++part) {   // hi rows, then lo rows
+                const uint32_t col =
+                    tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + part * 16 + 8 * g);
+                uint32_t v[8];
+                tmem_ld8(col, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int n = 0; n < 8; ++n) v[n] = __float_as_uint(__uint_as_float(v[n]) * alpha[n]);
+                tmem_st8(col, v);
+              }
+            }
+            tmem_st_wait();
+#pragma unroll
+            for (int n = 0; n < 8; ++n) lt[n] *= alpha[n];
+          }
+        }
+        // P^T as bf16 hi (rows 0-15) + lo (rows 16-31); one bf16 rounding of the
+        // weights alone would cost ~1e-3 relative error in O
+        if (gi >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+        uint8_t* pbase = sP + sb * kPBuf + (tok >> 6) * kPChunk;
+        const int t64 = tok & 63;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const float mr = m_ref[n] == -INFINITY ? 0.f : m_ref[n];   // every s is -inf then
+          const float pw = ex2_approx(s[n] - mr);
+          lt[n] += pw;
+          const uint16_t hb = bf16_bits(pw);
+          const float hf = __uint_as_float((uint32_t)hb << 16);
+          const uint16_t lb = bf16_bits(pw - hf);
+          const int row = 8 * g + n;
+          *reinterpret_cast<uint16_t*>(pbase + sw128_off(row, t64)) = hb;
+          *reinterpret_cast<uint16_t*>(pbase + sw128_off(kRp + row, t64)) = lb;
+        }
+        if (ntok < kTok) {
+          // rows past the unit's last token hold stale data: zero this CTA's V rows
+          uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStage);
+          const int tail = kTok - ntok;
+          for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
+            const int cch = e / (tail * 8), rem = e % (tail * 8);
+            v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[sb]));
+      }
+      if (!ok) break;
+      // ---- unit epilogue: O^T / l, partial or final output ----
+      if (x.ntiles > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // a unit that needed a bad page is written as empty (its partial, for a split item)
+      // (tagged with the unit's ordinal: a slot is rewritten only two units later,
+      // after every thread has passed the next unit's barrier)
+      if (bad) ubad_s[up] = uc + 1;
+      named_bar_sync(3, kSoftmaxThreads);
+      const bool unit_bad = ubad_s[up] == uc + 1;
+      // row sums over the 128 token lanes: warp butterfly, then the 4 warps in order
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        float v = lt[n];
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+        lt[n] = v;
+      }
+      if (lane == 0) {
+        float4* dst = reinterpret_cast<float4*>(lsum_s[up][g][quarter]);
+        dst[0] = make_float4(lt[0], lt[1], lt[2], lt[3]);
+        dst[1] = make_float4(lt[4], lt[5], lt[6], lt[7]);
+      }
+      named_bar_sync(1 + g, 128);
+      float inv[8], ltot[8];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        ltot[n] = ((lsum_s[up][g][0][n] + lsum_s[up][g][1][n]) + lsum_s[up][g][2][n]) + lsum_s[up][g][3][n];
+        inv[n] = ltot[n] > 0.f ? 1.f / ltot[n] : 0.f;
+      }
+      const bool direct = x.nch == 1;
+      const bool empty_out = direct && unit_bad;
+      const int64_t orow0 = direct ? ((int64_t)x.sr * a.B + x.b) * R : (int64_t)u * R;
+      float* obase = direct ? a.o_part : p.ws_o;
+#pragma unroll
+      for (int mb = 0; mb < 2; ++mb) {
+        uint32_t hv[8], lv[8];
+        if (x.ntiles > 0) {
+          const uint32_t col = tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + 8 * g);
+          tmem_ld8(col, hv);
+          tmem_ld8(col + 16, lv);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const int row = 8 * g + n;
+          if (row >= R) continue;
+          const float val =
+              (x.ntiles > 0 && !empty_out) ? (__uint_as_float(hv[n]) + __uint_as_float(lv[n])) * inv[n] : 0.f;
+          obase[(orow0 + row) * kDL + h * 256 + mb * 128 + tok] = val;
+        }
+      }
+      if (h == 0 && quarter == 0 && lane == 0) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const int row = 8 * g + n;
+          if (row >= R) continue;
+          const float lse2 = (ltot[n] > 0.f && !empty_out) ? m_ref[n] + log2f(ltot[n]) : -INFINITY;
+          if (direct) a.lse_part[orow0 + row] = a.base2 ? lse2 : lse2 * kLn2;
+          else p.ws_lse[orow0 + row] = lse2;
+        }
+      }
+      if (x.ntiles > 0) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_o_free[ob]));
+        ++kk;
+      }
+      // a split item's units are merged by the combine kernel; it also reads this flag
+      if (!direct && h == 0 && stid == 0) p.ws_bad[u] = unit_bad ? 1 : 0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // the peer may still be writing into this CTA's exchange buffer or barriers
+  cluster_arrive();
+  cluster_wait();
+  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+}
+
+// Merge of the units of each (request, shard) cut into several: one block per
+// (item, query row), 128 threads x 4 value dims.  The exact LSE merge of split
+// partials (base 2): lse = log2 sum_k 2^lse_k, o = sum_k 2^(lse_k - lse) o_k; an
+// item any unit of which needed a bad page is written as empty.
+__global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
+                                                         const float* __restrict__ ws_o,
+                                                         const float* __restrict__ ws_lse,
+                                                         const int32_t* __restrict__ ws_bad) {
+  const int item = blockIdx.x, row = blockIdx.y, t = threadIdx.x;
+  const int first = pre[item], nch = pre[item + 1] - first;
+  if (nch <= 1) return;
+  const int64_t R = a.R;
+  bool bad = false;
+  float m = -INFINITY;
+  for (int k = 0; k < nch; ++k) {
+    bad |= ws_bad[first + k] != 0;
+    m = fmaxf(m, ws_lse[(int64_t)(first + k) * R + row]);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse2 = -INFINITY;
+  if (!bad && m != -INFINITY) {
+    float sum = 0.f;
+    for (int k = 0; k < nch; ++k) sum += exp2f(ws_lse[(int64_t)(first + k) * R + row] - m);
+    lse2 = m + log2f(sum);
+    const float4* src = reinterpret_cast<const float4*>(ws_o + ((int64_t)first * R + row) * kDL) + t;
+    const int64_t step = R * (kDL / 4);
+    int k = 0;
+    for (; k + 4 <= nch; k += 4) {
+      float w[4];
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[j] = exp2f(ws_lse[(int64_t)(first + k + j) * R + row] - lse2);
+        v[j] = __ldcs(src + (k + j) * step);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc.x = fmaf(w[j], v[j].x, acc.x);
+        acc.y = fmaf(w[j], v[j].y, acc.y);
+        acc.z = fmaf(w[j], v[j].z, acc.z);
+        acc.w = fmaf(w[j], v[j].w, acc.w);
+      }
+    }
+    for (; k < nch; ++k) {
+      const float w = exp2f(ws_lse[(int64_t)(first + k) * R + row] - lse2);
+      const float4 v = __ldcs(src + k * step);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  }
+  const int b = item / a.shard_count, sr = item % a.shard_count;
+  const int64_t orow = ((int64_t)sr * a.B + b) * R + row;
+  reinterpret_cast<float4*>(a.o_part + orow * kDL)[t] = acc;
+  if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
+}
+
+struct FhPlan {
+  int32_t clusters, max_units;
+  size_t pre_off, bad_off, lse_off, o_off, bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
+  FhPlan p{};
+  p.clusters = std::max(1, sm_count / 2);
+  const int64_t items = (int64_t)a.B * a.shard_count;
+  const int64_t tiles_max = std::max<int64_t>(1, ((int64_t)a.max_pages * a.P + kTok - 1) / kTok);
+  p.max_units = (int32_t)std::min<int64_t>((int64_t)p.clusters * kUnitsPerCluster + items, items * tiles_max);
+  p.pre_off = 0;
+  p.bad_off = align256((size_t)(items + 1) * 4);
+  p.lse_off = p.bad_off + align256((size_t)p.max_units * 4);
+  p.o_off = p.lse_off + align256((size_t)p.max_units * a.R * 4);
+  p.bytes = p.o_off + (size_t)p.max_units * a.R * kDL * 4;
+  return p;
+}
+
+}  // namespace
+
+bool fh_supported(const DecodeArgs& a, int sm_count) {
+  if (a.fp8 || a.R > kRp || sm_count < 2) return false;
+  if (a.shard_count > kMaxFhShards) return false;
+  if (!(a.P % kTok == 0 || (kTok % a.P == 0 && a.P % 8 == 0))) return false;
+  if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
+  if ((int64_t)a.B * a.R < kRp || (int64_t)a.B * a.R > INT32_MAX) return false;   // Q box of 16 rows
+  if (a.pool_rows > INT32_MAX) return false;
+  return true;
+}
+
+size_t fh_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_fh(a, sm_count).bytes; }
+
+int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
+  const FhPlan plan = plan_fh(a, sm_count);
+  if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
+  FhParams* fp = new (std::nothrow) FhParams();
+  if (!fp) return DCPMLA_ERR_CAPACITY;
+  FhParams& p = *fp;
+  p.a = a;
+  p.box_rows = std::min(a.P, kTok);
+  p.max_units = plan.max_units;
+  int rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
+  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
+    rc = tma_encode_bf16_2d(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)kDK, (uint64_t)a.pool_rows, 64,
+                            (uint32_t)p.box_rows);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
+  p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
+  p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
+  p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
+  if (rc == DCPMLA_OK &&
+      cudaFuncSetAttribute(decode_fh_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+          cudaSuccess)
+    rc = DCPMLA_ERR_CUDA;
+  if (rc == DCPMLA_OK) {
+    decode_fh_bf16_kernel<<<2 * plan.clusters, kThreads, kSmemBytes, st>>>(p);
+    rc = launch_status();
+  }
+  if (rc == DCPMLA_OK) {
+    const dim3 grid((unsigned)(a.B * a.shard_count), (unsigned)a.R);
+    fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, p.ws_o, p.ws_lse, p.ws_bad);
+    rc = launch_status();
+  }
+  delete fp;
+  return rc;
+}
+
+}  // namespace dcpmla

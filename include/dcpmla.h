@@ -215,6 +215,20 @@ int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, in
                                  int32_t shard_count, int32_t kv_dtype, int32_t max_pages,
                                  size_t* out);
 
+/* Which decode kernels dcpmla_decode runs for the same arguments as
+ * dcpmla_decode_workspace_size, on the current device (host only, no launch):
+ *   *path = DCPMLA_PATH_TC_FEWHEAD: tensor cores with the KV tokens as the MMA's
+ *           M dimension (at most 16 query rows H*Tq, bf16 KV);
+ *           DCPMLA_PATH_TC_ROWS: tensor cores on 128-row query tiles;
+ *           DCPMLA_PATH_CUDA_CORE: CUDA-core kernel (other shapes);
+ *   *kernel_launches = kernels one dcpmla_decode call enqueues (memsets excluded).
+ * Either output pointer may be NULL. */
+#define DCPMLA_PATH_TC_FEWHEAD 1
+#define DCPMLA_PATH_TC_ROWS 2
+#define DCPMLA_PATH_CUDA_CORE 3
+int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, int32_t shard_count,
+                       int32_t kv_dtype, int32_t max_pages, int32_t* path, int32_t* kernel_launches);
+
 /* ------------------------------------------------------------------------
  * Allocation-free decode.  The pages have no counterpart to this call: it is
  * a library convenience.

@@ -49,6 +49,18 @@ SMALL = {
                               seed=15, L=1500),
     "h128_c1_short": W.Workload("h128c1", B=3, H=128, Tq=1, c=1, P=64, kv_dtype="bf16",
                                 lse_base="e", seed=16, lengths_mix=(1, 100, 200, 1, 70)),
+    # token-major tensor-core path (<= 16 query rows): causal query pairs with odd c,
+    # padding rows (R = 8), empty shards with 8-token pages, 128-token pages, and
+    # (request, shard) ranges cut into multi-tile units that are merged in the kernel
+    "fh_tq2_c3": W.Workload("fhq", B=3, H=8, Tq=2, c=3, P=16, kv_dtype="bf16", lse_base="2",
+                            seed=17, L=1000),
+    "fh_r8_p64": W.Workload("fhr", B=2, H=4, Tq=2, c=2, P=64, kv_dtype="bf16", lse_base="e",
+                            seed=18, L=900),
+    "fh_short_p8": W.Workload("fhs", B=6, H=16, Tq=1, c=8, P=8, kv_dtype="bf16", lse_base="e",
+                              seed=19, lengths_mix=(2, 1, 7, 9, 300)),
+    "fh_p128": W.Workload("fhp", B=2, H=16, Tq=1, c=2, P=128, kv_dtype="bf16", lse_base="2",
+                          seed=20, L=3001),
+    "fh_chunked": W.scaled(W.WORKLOADS["long"], B=2, L=300000),
 }
 
 SENTINEL = 0xA5
@@ -175,9 +187,18 @@ def test_slot_map_bit_exact_and_error_bits():
     assert o4.tolist()[:3] == [-1, -1, -1] and o4.tolist()[3] >= 0
 
 
+BAD_INPUT_CASES = {
+    "dsv3_s": SMALL["dsv3_s"],                                       # 128-row tiles
+    "long_split": W.scaled(W.WORKLOADS["long"], B=3, L=40000),      # token-major, merged units
+    "fh_tq2_c3": SMALL["fh_tq2_c3"],                                 # token-major, one unit each
+}
+
+
 @needs_cuda
-def test_decode_flags_bad_page_and_short_length_without_faulting():
-    w = SMALL["dsv3_s"]
+@pytest.mark.parametrize("name", list(BAD_INPUT_CASES))
+def test_decode_flags_bad_page_and_short_length_without_faulting(name):
+    """A page id outside the pools and a length below Tq are flagged; their work is empty."""
+    w = BAD_INPUT_CASES[name]
     dw = Hn.build(w)
     st = dw.step
     st.run()                                         # append the step's new tokens first
@@ -187,7 +208,7 @@ def test_decode_flags_bad_page_and_short_length_without_faulting():
     st.seq_lens[2] = 0                               # request 2 shorter than its query block
     dw.cache.err.zero_()
     B.dcpmla_decode(st.q, dw.cache.pools, None, B.KV_BF16, st.page_table, st.seq_lens, w.P, w.c, 0,
-                    w.c, w.sm_scale, B.LSE_2, st.o_part, st.lse_part, st.workspace, dw.cache.err)
+                    w.c, w.sm_scale, st.lse_base, st.o_part, st.lse_part, st.workspace, dw.cache.err)
     torch.cuda.synchronize()
     e = dw.cache.check_errors()
     assert e & B.DERR_PAGE and e & B.DERR_LENGTH
@@ -216,3 +237,19 @@ def test_input_generator_is_device_independent(name):
     qc = W.q_tensor(w, "cpu", requests=[0, w.B - 1])
     qg = W.q_tensor(w, "cuda", requests=[0, w.B - 1])
     assert np.array_equal(bits(qc), bits(qg))
+
+
+@needs_cuda
+def test_decode_path_per_workload():
+    """Few-row bf16 shapes take the token-major tensor-core kernel (decode + split merge),
+    128-head shapes the 128-row tensor-core kernel, 16 shards per launch the CUDA cores."""
+    want = {"tiny": B.PATH_TC_FEWHEAD, "long": B.PATH_TC_FEWHEAD, "bimodal": B.PATH_TC_FEWHEAD,
+            "dsv3": B.PATH_TC_ROWS, "fp8": B.PATH_TC_ROWS}
+    for name, path in want.items():
+        w = W.WORKLOADS[name]
+        kv = B.KV_BF16 if w.kv_dtype == "bf16" else B.KV_E4M3
+        got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, kv, max(w.pages_per_request()))
+        assert got == (path, 2 if path == B.PATH_TC_FEWHEAD else 1), name
+    w = SMALL["c16_short"]
+    got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
+    assert got == (B.PATH_CUDA_CORE, 1)

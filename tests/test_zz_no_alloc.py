@@ -74,11 +74,10 @@ def test_noalloc_matches_regular_decode_two_calls(name):
 
 @needs_cuda
 def test_noalloc_refuses_shapes_beyond_its_scratch():
-    """Full bimodal batch: its split-KV scratch exceeds the static array, so the call is refused."""
+    """Full bimodal batch: the CUDA-core decode's split-KV scratch for it exceeds the static
+    array, so the call is refused before any launch."""
     w = W.WORKLOADS["bimodal"]
     pages = w.pages_per_request()
-    need = B.dcpmla_decode_workspace_size(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(pages))
-    assert need > B.NOALLOC_SCRATCH_BYTES
     dev = "cuda"
     q = torch.zeros((w.B, w.Tq, w.H, W.D_K), dtype=torch.bfloat16, device=dev)
     pools = [torch.zeros((w.P, W.D_K), dtype=torch.bfloat16, device=dev) for _ in range(w.c)]
