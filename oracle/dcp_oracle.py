@@ -24,6 +24,23 @@ Sources, by page and section:
              effective block size is the physical block times the DCP size.
   [GLM-FN]   vLLM GLM-5.3 serving post, footnote arithmetic: absorbed MLA scores
              use the 576-d key (512 latent + 64 rope), values the 512-d latent.
+  [SG-PD]    SGLang DCP docs, "DCP x PD disaggregation": dense prefill pages are not
+             copied straight into striped decode storage; a DCP-1 prefill feeds DCP
+             decode through a token relayout whose plan carries the exact token
+             count, so a partial final page leaks no stale rows; physical page size
+             and KV dtype match on both sides.
+  [SG-EXT]   same page, "Communication backends", closing paragraph: extend gathers
+             the cached prefix shards and restores token order (work that grows
+             with the prefix).
+  [GLM-AG]   vLLM GLM-5.3 serving post, "DCP: split the KV cache too": the prefill
+             engine gathers the shards into a temporary full-context copy.
+  [SG-HIC]   SGLang DCP docs, "DCP x HiCache L2": the controller addresses P*c slots
+             per widened page while each buffer stores its P local rows; before a
+             transfer both index lists keep the positions this rank owns and map
+             i to floor(i / c).
+  [VW-ILV]   vLLM DCP study page (llm-wiki), configuration example: the DCP KV
+             interleave size (default 1 token) hands out tokens to ranks in runs of
+             that many; larger runs trade balance for less sorting.
 
 Readings where the pages are silent (each listed in the design notes):
   * the query of draft token t (of Tq) sits at global position L - Tq + t and sees
@@ -396,3 +413,152 @@ def decode_request_dense(q_b: np.ndarray, k_dense: np.ndarray, L: int, sm_scale:
     Tq, H, _ = q_b.shape
     return attend(q_b.reshape(Tq * H, D_K), k_dense[:L], np.arange(L), query_positions(L, Tq, H),
                   sm_scale, base)
+
+
+# ---------------------------------------------------------------------------
+# Interleaved striping, relayout, un-stripe gather, HiCache index filter,
+# per-token E4M3 quantisation
+# ---------------------------------------------------------------------------
+def owner_i(v, c: int, I: int = 1):
+    """Rank that stores virtual slot v when tokens go to ranks in runs of I ([VW-ILV]).
+
+    I = 1 is owner(v) = v mod c ([SG-VKV]).  Runs of I consecutive slots share a
+    rank and the runs go round-robin over the c ranks.
+    """
+    return (np.asarray(v) // I) % c
+
+
+def physical_i(v, c: int, I: int = 1):
+    """Compacted slot of virtual slot v in its owner's pool with runs of I.
+
+    Each round of I*c slots gives every rank I consecutive local slots, so the
+    local slot is (round) * I + (offset inside the run); I = 1 is floor(v / c).
+    """
+    v = np.asarray(v)
+    return (v // (I * c)) * I + v % I
+
+
+def striped_slots(vpt_row: np.ndarray, positions, c: int, P: int, I: int = 1):
+    """(owner, physical slot) of global positions of one request, from its virtual
+    page table row (virtual page = P*c positions; I must divide P so that a virtual
+    page is whole rounds and its rank-local part is one physical page)."""
+    if P % I:
+        raise ValueError("the interleave size must divide the physical page size")
+    p = np.asarray(positions, dtype=np.int64)
+    vp = P * c
+    v = np.asarray(vpt_row, dtype=np.int64)[p // vp] * vp + p % vp
+    return owner_i(v, c, I), physical_i(v, c, I)
+
+
+def shard_positions(L: int, r: int, c: int, I: int = 1) -> np.ndarray:
+    """Global positions < L that rank r owns, in order (shard-local token j is the
+    j-th of them).  I = 1 gives r, r + c, r + 2c, ..."""
+    p = np.arange(L, dtype=np.int64)
+    return p[(p // I) % c == r]
+
+
+def dense_slots(dense_pt_row: np.ndarray, positions, P: int) -> np.ndarray:
+    """Slot of each position in a DCP-1 (unstriped) paged cache: page p // P, offset p % P."""
+    p = np.asarray(positions, dtype=np.int64)
+    return np.asarray(dense_pt_row, dtype=np.int64)[p // P] * P + p % P
+
+
+def relayout_dense_to_striped(dense_rows: np.ndarray, dense_scales: Optional[np.ndarray],
+                              dense_pt: np.ndarray, lens: Sequence[int], vpt: np.ndarray,
+                              pools: List[np.ndarray], scale_pools: Optional[List[np.ndarray]],
+                              c: int, P: int, I: int = 1) -> None:
+    """DCP-1 prefill cache -> striped decode pools, token by token ([SG-PD]).
+
+    For request b and every position p < lens[b] (the exact token count: rows past
+    it in a partial final dense page are not copied), the stored row at the dense
+    slot of p is copied bit for bit to pools[owner(p)][physical(p)]; per-token
+    scales travel with their rows.  pools / scale_pools are updated in place.
+    """
+    for b, L in enumerate(lens):
+        if L <= 0:
+            continue
+        p = np.arange(L, dtype=np.int64)
+        src = dense_slots(dense_pt[b], p, P)
+        own, dst = striped_slots(vpt[b], p, c, P, I)
+        for r in range(c):
+            sel = own == r
+            pools[r][dst[sel]] = dense_rows[src[sel]]
+            if scale_pools is not None:
+                scale_pools[r][dst[sel]] = dense_scales[src[sel]]
+
+
+def gather_unstriped(pools: List[np.ndarray], scale_pools: Optional[List[np.ndarray]],
+                     vpt: np.ndarray, lens: Sequence[int], out: np.ndarray,
+                     out_scales: Optional[np.ndarray], c: int, P: int, I: int = 1) -> None:
+    """Striped pools -> one contiguous full-context copy per request, in token order
+    ([SG-EXT], [GLM-AG]): out[b, p] = pools[owner(p)][physical(p)] for p < lens[b];
+    rows at p >= lens[b] are left as they are."""
+    for b, L in enumerate(lens):
+        if L <= 0:
+            continue
+        p = np.arange(L, dtype=np.int64)
+        own, src = striped_slots(vpt[b], p, c, P, I)
+        for r in range(c):
+            sel = own == r
+            out[b, p[sel]] = pools[r][src[sel]]
+            if out_scales is not None:
+                out_scales[b, p[sel]] = scale_pools[r][src[sel]]
+
+
+def hicache_filter(idx, c: int, rank: int, I: int = 1) -> np.ndarray:
+    """Widened-page slot indices -> this rank's local slots ([SG-HIC]).
+
+    Keeps the indices the rank owns, in their order, and maps each to its local
+    slot (floor(i / c) for I = 1).
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    keep = owner_i(idx, c, I) == rank
+    return physical_i(idx[keep], c, I)
+
+
+def _e4m3_magnitudes() -> np.ndarray:
+    """Every finite non-negative E4M3FN value, by code 0x00..0x7E (increasing)."""
+    return e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+
+
+def round_to_e4m3(y: np.ndarray) -> np.ndarray:
+    """Codes of the E4M3FN values nearest to y (|y| <= 448), ties to the even code.
+
+    Written from the definition: among the 127 finite magnitudes pick the closest;
+    at an exact midpoint take the code whose lowest mantissa bit is 0.  The sign
+    bit is y's, so a negative value that rounds to zero is stored as -0 (0x80), as
+    IEEE rounding gives it.
+    """
+    y = np.asarray(y, dtype=np.float64)
+    mags = _e4m3_magnitudes()
+    a = np.abs(y)
+    if np.any(a > 448.0):
+        raise ValueError("value outside the E4M3 range")
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, 126)   # first magnitude >= a
+    lo = np.clip(hi - 1, 0, 126)
+    dlo, dhi = a - mags[lo], mags[hi] - a
+    pick = np.where(dhi < dlo, hi, lo)
+    tie = (dhi == dlo) & (hi != lo)
+    pick = np.where(tie, np.where(hi % 2 == 0, hi, lo), pick)
+    sign = np.where(np.signbit(y), 0x80, 0x00)
+    return (pick | sign).astype(np.uint8)
+
+
+def quantize_e4m3_rows(rows_bf16_bits: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-token E4M3 quantisation of new KV rows (576 bf16 values each).
+
+    In float32, as both sides compute it: amax = max |x| over the row,
+    scale = amax / 448, codes = E4M3(clamp(x / scale, -448, 448)) rounded to
+    nearest-even; a row of zeros gets scale 0 and all-zero codes.  (The pages fix
+    an FP8 KV cache with a per-token scale; this recipe is the reading used.)
+    """
+    x = (np.asarray(rows_bf16_bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    amax = np.abs(x).max(axis=1).astype(np.float32)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    live = scale > 0
+    if np.any(live):
+        y = (x[live] / scale[live, None]).astype(np.float32)
+        y = np.clip(y, np.float32(-448.0), np.float32(448.0))
+        codes[live] = round_to_e4m3(y)
+    return codes, scale

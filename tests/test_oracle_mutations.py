@@ -77,3 +77,54 @@ def test_e4m3_without_subnormals_is_caught(monkeypatch):
         return np.where(((u >> 3) & 0xF) == 0, 0.0, v)
     _plant(monkeypatch, "e4m3_to_f64", no_sub)
     assert _fails(pins.test_e4m3_decode_matches_torch_for_all_codes)
+
+
+# ---- relayout, gather, interleave, HiCache filter, E4M3 quantisation ----
+import test_oracle_next as nxt  # noqa: E402
+
+
+def test_interleave_ignored_in_physical_slot_is_caught(monkeypatch):
+    _plant(monkeypatch, "physical_i", lambda v, c, I=1: np.asarray(v) // c)
+    assert _fails(nxt.test_interleaved_widened_page_is_one_physical_page_per_rank, 2, 64, 16)
+
+
+def test_relayout_of_whole_pages_is_caught(monkeypatch):
+    real = OD.relayout_dense_to_striped
+
+    def whole_pages(dense_rows, dense_scales, dense_pt, lens, vpt, pools, scale_pools, c, P, I=1):
+        lens = [-(-L // P) * P for L in lens]                # stale rows of the last page leak
+        return real(dense_rows, dense_scales, dense_pt, lens, vpt, pools, scale_pools, c, P, I)
+    _plant(monkeypatch, "relayout_dense_to_striped", whole_pages)
+    assert _fails(nxt.test_relayout_copies_the_exact_token_count, 17)
+
+
+def test_gather_in_shard_order_is_caught(monkeypatch):
+    def shard_major(pools, scale_pools, vpt, lens, out, out_scales, c, P, I=1):
+        for b, L in enumerate(lens):
+            own, src = OD.striped_slots(vpt[b], np.arange(L), c, P, I)
+            order = np.argsort(own, kind="stable")               # shard 0's tokens first
+            for k, i in enumerate(order):
+                out[b, k] = pools[own[i]][src[i]]
+    _plant(monkeypatch, "gather_unstriped", shard_major)
+    assert _fails(nxt.test_gather_restores_token_order_of_the_worked_example)
+
+
+def test_hicache_filter_with_remainder_instead_of_floor_is_caught(monkeypatch):
+    def rem(idx, c, rank, I=1):
+        idx = np.asarray(idx, dtype=np.int64)
+        return idx[OD.owner_i(idx, c, I) == rank] % c
+    _plant(monkeypatch, "hicache_filter", rem)
+    assert _fails(nxt.test_hicache_filter_keeps_owned_slots_and_maps_to_floor_i_over_c)
+
+
+def test_e4m3_ties_away_from_zero_is_caught(monkeypatch):
+    def away(y):
+        y = np.asarray(y, dtype=np.float64)
+        mags = OD._e4m3_magnitudes()
+        a = np.abs(y)
+        hi = np.clip(np.searchsorted(mags, a, side="left"), 0, 126)
+        lo = np.clip(hi - 1, 0, 126)
+        pick = np.where(mags[hi] - a <= a - mags[lo], hi, lo)   # ties go up
+        return (pick | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+    _plant(monkeypatch, "round_to_e4m3", away)
+    assert _fails(nxt.test_round_to_e4m3_matches_exhaustive_search_including_ties)
