@@ -199,11 +199,15 @@ class RequestTokenMap:
         return out
 
 
-def map_positions(rmap: RequestTokenMap, b: int, positions) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
-    """Position -> (virtual slot, owner rank, physical slot) for request b ([SG-VKV])."""
+def map_positions(rmap: RequestTokenMap, b: int, positions,
+                  I: int = 1) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Position -> (virtual slot, owner rank, physical slot) for request b ([SG-VKV]);
+    with an interleave size I > 1 the owner and slot follow owner_i / physical_i ([VW-ILV])."""
     v = rmap.vslot(b, positions)
     c = rmap.alloc.c
-    return v, owner(v, c), physical(v, c)
+    if I == 1:
+        return v, owner(v, c), physical(v, c)
+    return v, owner_i(v, c, I), physical_i(v, c, I)
 
 
 # ---------------------------------------------------------------------------
@@ -252,7 +256,7 @@ class ShardPools:
 
 
 def append_tokens(pools: ShardPools, rmap: RequestTokenMap, b: int, positions,
-                  rows: np.ndarray, row_scales: Optional[np.ndarray] = None) -> None:
+                  rows: np.ndarray, row_scales: Optional[np.ndarray] = None, I: int = 1) -> None:
     """Compacting write: each new token goes only to the rank that owns its slot, at physical(v).
 
     Rows are written page by page (a page of one rank at a time); within the
@@ -260,7 +264,7 @@ def append_tokens(pools: ShardPools, rmap: RequestTokenMap, b: int, positions,
     """
     positions = np.asarray(positions, dtype=np.int64)
     rows = np.asarray(rows)
-    v, r, s = map_positions(rmap, b, positions)
+    v, r, s = map_positions(rmap, b, positions, I)
     P = pools.P
     for rank in np.unique(r):
         idx = np.nonzero(r == rank)[0]
@@ -277,12 +281,14 @@ def append_tokens(pools: ShardPools, rmap: RequestTokenMap, b: int, positions,
             pools.written[int(rank)].update(s[sel].tolist())
 
 
-def shard_view(rmap: RequestTokenMap, b: int, L: int, r: int) -> Tuple[np.ndarray, np.ndarray]:
+def shard_view(rmap: RequestTokenMap, b: int, L: int, r: int,
+               I: int = 1) -> Tuple[np.ndarray, np.ndarray]:
     """Rank r's part of request b's first L positions: (global positions, physical slots), in position order."""
     p = np.arange(L, dtype=np.int64)
     v = rmap.vslot(b, p) if L > 0 else np.zeros(0, dtype=np.int64)
-    keep = owner(v, rmap.alloc.c) == r
-    return p[keep], physical(v[keep], rmap.alloc.c)
+    c = rmap.alloc.c
+    keep = (owner(v, c) if I == 1 else owner_i(v, c, I)) == r
+    return p[keep], (physical(v[keep], c) if I == 1 else physical_i(v[keep], c, I))
 
 
 # ---------------------------------------------------------------------------
@@ -383,7 +389,7 @@ def query_positions(L: int, Tq: int, H: int) -> np.ndarray:
 # ---------------------------------------------------------------------------
 def decode_request_striped(q_b: np.ndarray, pools: ShardPools, rmap: RequestTokenMap, b: int,
                            L: int, sm_scale: float, base: str,
-                           shards: Optional[Sequence[int]] = None):
+                           shards: Optional[Sequence[int]] = None, I: int = 1):
     """Per-shard partials and their merge for request b.
 
     q_b: (Tq, H, 576) float64.  For each rank r, attention runs over the
@@ -400,7 +406,7 @@ def decode_request_striped(q_b: np.ndarray, pools: ShardPools, rmap: RequestToke
     o_parts = np.zeros((len(shards), R, D_LATENT))
     lse_parts = np.full((len(shards), R), -np.inf)
     for i, r in enumerate(shards):
-        pos, slots = shard_view(rmap, b, L, r)
+        pos, slots = shard_view(rmap, b, L, r, I)
         rows, scs = pools.read(r, slots)
         k = dequant(rows, scs, pools.kv_dtype)
         o_parts[i], lse_parts[i] = attend(qrows, k, pos, qpos, sm_scale, base)

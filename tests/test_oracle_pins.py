@@ -265,7 +265,7 @@ def test_attend_empty_and_fully_masked_rows():
 # ---------------------------------------------------------------------------
 # Merge: exactness against brute force, c = 1 identity, base equivalence
 # ---------------------------------------------------------------------------
-def _random_case(c, P, L, Tq, H, seed, kv_dtype="bf16"):
+def _random_case(c, P, L, Tq, H, seed, kv_dtype="bf16", I=1):
     rng = np.random.default_rng(seed)
     pages = -(-L // (P * c)) + 1
     alloc = O.SharedVirtualAllocator(c, pages * P, P, rng.permutation(pages).tolist())
@@ -281,7 +281,7 @@ def _random_case(c, P, L, Tq, H, seed, kv_dtype="bf16"):
         scales = np.abs(x).max(axis=1) / 448.0
         rows = torch.from_numpy(x / scales[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         k_dense = O.e4m3_to_f64(rows) * scales.astype(np.float64)[:, None]
-    O.append_tokens(pools, rmap, 0, pos, rows, scales)
+    O.append_tokens(pools, rmap, 0, pos, rows, scales, I=I)
     q = O.bf16_to_f64(torch.from_numpy(rng.standard_normal((Tq, H, O.D_K)).astype(np.float32))
                       .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
     return q, pools, rmap, k_dense
@@ -302,6 +302,24 @@ def test_striped_merge_equals_brute_force(c, L, Tq, base):
     assert np.allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
     if L < c:   # some ranks hold nothing: their lse is -inf
         assert np.all(np.isneginf(lse_parts[L:]))
+
+
+@pytest.mark.parametrize("c,I,P", [(2, 16, 16), (4, 4, 8), (8, 2, 4), (3, 8, 16), (8, 16, 64)])
+@pytest.mark.parametrize("L,Tq", [(1, 1), (37, 1), (130, 4), (700, 2)])
+def test_interleaved_striped_merge_equals_brute_force(c, I, P, L, Tq):
+    """vLLM DCP study page, interleave size: handing tokens to ranks in runs of I changes
+    which rank holds a token, not the merged result (full attention, any c and I)."""
+    if L < Tq:
+        pytest.skip("context shorter than the query block")
+    q, pools, rmap, k_dense = _random_case(c, P, L, Tq, 3, seed=c * 100 + I * 7 + L, I=I)
+    _, lse_parts, o, lse = O.decode_request_striped(q, pools, rmap, 0, L, 0.125, "2", I=I)
+    o_ref, lse_ref = O.decode_request_dense(q, k_dense, L, 0.125, "2")
+    assert np.allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+    # a rank's tokens are the positions owned under runs of I
+    for r in range(c):
+        pos, _ = O.shard_view(rmap, 0, L, r, I)
+        assert np.array_equal(pos, O.shard_positions(L, r, c, I))
 
 
 def test_fp8_striped_equals_brute_force_on_dequantised_values():
