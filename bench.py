@@ -28,6 +28,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import dcp_workloads as W  # noqa: E402
@@ -474,6 +475,137 @@ def run_e2e(args, w, dw, stream, acc, ws):
                     "-> pinned host outputs, eager launches"}
 
 
+# ---------------------------------------------------------------------------
+# The layout calls around the decode (one call per step, large synthetic input)
+# ---------------------------------------------------------------------------
+def _event_time(fn, k, stream):
+    """Mean ms of fn() over k calls on `stream`, CUDA events on that stream."""
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / k
+
+
+def run_op(args, w: W.Workload):
+    """Relayout, gather, E4M3 quantising append or HiCache filter: HBM GB/s moved."""
+    from __graft_entry__ import build
+    build()
+    from decode_context_mla_gb300 import binding as B
+    dev = "cuda"
+    stream = torch.cuda.Stream()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    peaks = measured_peaks()
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    lens = w.seq_lens()
+    P, c, I = w.P, w.c, w.interleave
+    sample = ""
+    if args.op in ("relayout", "gather"):
+        dpages = [(L + P - 1) // P for L in lens]
+        vpages = [(L + P * c - 1) // (P * c) for L in lens]
+        dpt = torch.full((w.B, max(dpages)), -1, dtype=torch.int32)
+        vpt = torch.full((w.B, max(vpages)), -1, dtype=torch.int32)
+        dperm = torch.randperm(sum(dpages), generator=torch.Generator().manual_seed(1)).to(torch.int32)
+        vperm = torch.randperm(sum(vpages), generator=torch.Generator().manual_seed(2)).to(torch.int32)
+        k0 = k1 = 0
+        for b in range(w.B):
+            dpt[b, :dpages[b]] = dperm[k0:k0 + dpages[b]]
+            vpt[b, :vpages[b]] = vperm[k1:k1 + vpages[b]]
+            k0 += dpages[b]
+            k1 += vpages[b]
+        dense = torch.randint(-30000, 30000, (sum(dpages) * P, W.D_K), dtype=torch.int16, device=dev,
+                              generator=g).view(torch.bfloat16)
+        pools = [torch.empty((sum(vpages) * P, W.D_K), dtype=torch.bfloat16, device=dev) for _ in range(c)]
+        dpt_d, vpt_d = dpt.to(dev), vpt.to(dev)
+        lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+        B.dcpmla_relayout_dense_to_striped(dense, None, dpt_d, pools, None, B.KV_BF16, vpt_d, lens_d, P, c,
+                                           err, stream, interleave=I)
+        if args.op == "relayout":
+            fn = lambda: B.dcpmla_relayout_dense_to_striped(dense, None, dpt_d, pools, None, B.KV_BF16, vpt_d,
+                                                            lens_d, P, c, err, stream, interleave=I)
+        else:
+            out = torch.empty((w.B, max(lens), W.D_K), dtype=torch.bfloat16, device=dev)
+            fn = lambda: B.dcpmla_gather_unstriped(pools, None, B.KV_BF16, vpt_d, lens_d, P, c, out, None, err,
+                                                   stream, interleave=I)
+        moved = 2 * sum(lens) * W.D_K * 2
+        units, unit = sum(lens), "tokens"
+        sample = "oracle relayout of 4096 tokens of request 0"
+        def cpu_leg():
+            import oracle as O
+            n = 4096
+            rows = np.zeros((n, W.D_K), np.uint16)
+            dpt_h = np.arange((n + P - 1) // P)[None, :]
+            vpt_h = np.arange((n + P * c - 1) // (P * c))[None, :]
+            pools_h = [np.zeros(((n // c) + 2 * P, W.D_K), np.uint16) for _ in range(c)]
+            t0 = time.perf_counter()
+            O.relayout_dense_to_striped(rows, None, dpt_h, [n], vpt_h, pools_h, None, c, P, I)
+            return n * W.D_K * 2 * 2 / (time.perf_counter() - t0) / 1e9
+    elif args.op == "append_e4m3":
+        n = 1 << 20
+        pages = (n + P - 1) // P + 1
+        pools = [torch.empty((pages * P, W.D_K), dtype=torch.uint8, device=dev) for _ in range(c)]
+        spools = [torch.empty(pages * P, dtype=torch.float32, device=dev) for _ in range(c)]
+        rows = torch.randn((n, W.D_K), generator=g, device=dev).to(torch.bfloat16)
+        own = (torch.arange(n, device=dev) % c).to(torch.int32)
+        phys = (torch.arange(n, device=dev) // c).to(torch.int64)
+        fn = lambda: B.dcpmla_kv_append_e4m3(pools, spools, own, phys, rows[:, :512], rows[:, 512:], err, stream)
+        moved = n * (W.D_K * 2 + 4 + 8 + W.D_K + 4)
+        units, unit = n, "rows"
+        sample = "oracle quantisation of 2048 rows"
+        def cpu_leg():
+            import oracle as O
+            r = np.random.default_rng(0).integers(0, 1 << 15, (2048, W.D_K)).astype(np.uint16)
+            t0 = time.perf_counter()
+            O.quantize_e4m3_rows(r)
+            return 2048 * (W.D_K * 2 + W.D_K + 4) / (time.perf_counter() - t0) / 1e9
+    elif args.op == "hicache":
+        n = 1 << 24
+        idx = torch.randint(0, 1 << 40, (n,), dtype=torch.int64, device=dev, generator=g)
+        out = torch.empty(n, dtype=torch.int64, device=dev)
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        ws = torch.empty(max(16, B.dcpmla_hicache_filter_workspace_size(n)), dtype=torch.uint8, device=dev)
+        fn = lambda: B.dcpmla_hicache_filter(idx, c, 0, out, cnt, ws, err, stream, interleave=I)
+        moved = 2 * n * 8 + (n // c) * 8       # two passes over the list, the kept slots written
+        units, unit = n, "indices"
+        sample = "oracle filter of 1M indices"
+        def cpu_leg():
+            import oracle as O
+            x = np.random.default_rng(0).integers(0, 1 << 40, 1 << 20)
+            t0 = time.perf_counter()
+            O.hicache_filter(x, c, 0, I)
+            return (1 << 20) * 8 * (1 + 1 / c) / (time.perf_counter() - t0) / 1e9
+    else:
+        raise ValueError(args.op)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            fn()
+    torch.cuda.synchronize()
+    ms = _event_time(fn, args.steps, stream)
+    if int(err.item()):
+        raise RuntimeError(f"device error bits {int(err.item())}")
+    gbs = moved / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        cpu = {"value": round(cpu_leg(), 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample}
+    line = {"metric": f"{args.op}: HBM GB/s moved", "value": round(gbs, 2), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.op != "hicache" else "int64", "data": "synthetic",
+            "config": {"workload": f"{args.op} on {w.name}" if args.op in ("relayout", "gather") else args.op,
+                       "units_per_step": units, "unit": unit, "c": c, "P": P, "interleave": I},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "algorithmic_bytes": moved},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps * (3 if args.op == "hicache" else 1)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -483,6 +615,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--op", default="step", choices=["step", "relayout", "gather", "append_e4m3", "hicache"],
+                    help="what to time: the decode step (default) or one of the layout calls")
+    ap.add_argument("--interleave", type=int, default=0, help="override the interleave size")
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload with this many requests (small profiling captures)")
     args = ap.parse_args()
@@ -491,6 +626,11 @@ def main():
     w = W.WORKLOADS[args.config]
     if args.batch:
         w = W.scaled(w, B=args.batch, name=f"{w.name}_b{args.batch}")
+    if args.interleave:
+        w = W.scaled(w, interleave=args.interleave, name=f"{w.name}_i{args.interleave}")
+    if args.op != "step":
+        run_op(args, w)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

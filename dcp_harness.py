@@ -43,7 +43,7 @@ def build(w: W.Workload, device="cuda", chunk_tokens: int = 1 << 18,
     order = W.free_list_order(w.seed, num_pages)
     cache = StripedKVCache(w.c, w.P, num_pages, kv_code(w), max_requests=w.B,
                            max_pages_per_request=max(pages), initial_order=order, device=device,
-                           fill_byte=fill_byte)
+                           fill_byte=fill_byte, interleave=w.interleave)
     for b, L in enumerate(lens):
         cache.extend(b, L)
     step = DecodeStep(cache, range(w.B), w.Tq, w.H, w.sm_scale, base_code(w), append=append)

@@ -98,6 +98,7 @@ class Workload:
     lengths_mix: Optional[tuple] = None   # (n_long, long_lo, long_hi, short_lo, short_hi)
     sm_scale: float = 1.0 / math.sqrt(192.0)
     description: str = ""
+    interleave: int = 1       # tokens go to shards in runs of this many positions
 
     @property
     def rows_per_request(self) -> int:

@@ -32,17 +32,25 @@ SIGNATURES = {
     "dcpmla_reqmap_release": (C.c_int, [vp, i32]),
     "dcpmla_reqmap_length": (C.c_int, [vp, i32, P_i64]),
     "dcpmla_reqmap_page_table": (C.c_int, [vp, vp, i32, i32, i32, vp, vp]),
-    "dcpmla_map_positions": (C.c_int, [vp, i32, i32, i32, vp, vp, i64, vp, vp, vp]),
-    "dcpmla_slot_map": (C.c_int, [vp, i32, i32, i64, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp]),
+    "dcpmla_map_positions": (C.c_int, [vp, i32, i32, i32, i32, vp, vp, i64, vp, vp, vp]),
+    "dcpmla_slot_map": (C.c_int, [vp, i32, i32, i64, i32, i32, i32, vp, vp, i64, vp, vp, vp, vp,
+                                  vp]),
     "dcpmla_kv_append": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp, i64, vp, i64, vp, i64, vp,
                                    vp]),
     "dcpmla_decode": (C.c_int, [vp, vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, i32, i32,
-                                i32, f32, i32, vp, vp, vp, sz, vp, vp]),
+                                i32, i32, f32, i32, vp, vp, vp, sz, vp, vp]),
     "dcpmla_decode_noalloc": (C.c_int, [vp, vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32,
                                         i32, i32, i32, f32, i32, vp, vp, vp, vp]),
     "dcpmla_decode_workspace_size": (C.c_int, [i32, i32, i32, i32, i32, i32, i32, i32, P_sz]),
     "dcpmla_decode_path": (C.c_int, [i32, i32, i32, i32, i32, i32, i32, i32, P_i32, P_i32]),
     "dcpmla_lse_merge": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp, vp]),
+    "dcpmla_relayout_dense_to_striped": (C.c_int, [vp, vp, i64, vp, i32, vp, vp, i32, i64, vp, i32,
+                                                   vp, i32, i32, i32, i32, vp, vp]),
+    "dcpmla_gather_unstriped": (C.c_int, [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, vp, vp,
+                                          i64, vp, vp]),
+    "dcpmla_kv_append_e4m3": (C.c_int, [vp, vp, i64, i32, vp, vp, vp, i64, vp, i64, i64, vp, vp]),
+    "dcpmla_hicache_filter_workspace_size": (C.c_int, [i64, P_sz]),
+    "dcpmla_hicache_filter": (C.c_int, [vp, i64, i32, i32, i32, vp, vp, vp, sz, vp, vp]),
 }
 
 _lib = None

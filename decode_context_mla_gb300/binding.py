@@ -152,7 +152,7 @@ def dcpmla_reqmap_page_table(h, reqs: Sequence[int], max_pages: int, pad: int = 
 
 
 def dcpmla_map_positions(page_table: torch.Tensor, c: int, P: int, req: torch.Tensor,
-                         pos: torch.Tensor):
+                         pos: torch.Tensor, interleave: int = 1):
     """Host arrays in, (vslot int64, owner int32, phys int64) out."""
     assert page_table.dtype == torch.int32 and page_table.dim() == 2 and not page_table.is_cuda
     req = req.to(torch.int32).contiguous()
@@ -162,7 +162,7 @@ def dcpmla_map_positions(page_table: torch.Tensor, c: int, P: int, req: torch.Te
     o = torch.empty(n, dtype=torch.int32)
     s = torch.empty(n, dtype=torch.int64)
     pt = page_table.contiguous()
-    _check(lib().dcpmla_map_positions(C.c_void_p(pt.data_ptr()), pt.shape[1], c, P,
+    _check(lib().dcpmla_map_positions(C.c_void_p(pt.data_ptr()), pt.shape[1], c, interleave, P,
                                       C.c_void_p(req.data_ptr()), C.c_void_p(pos.data_ptr()), n,
                                       C.c_void_p(v.data_ptr()), C.c_void_p(o.data_ptr()),
                                       C.c_void_p(s.data_ptr())), "dcpmla_map_positions")
@@ -174,11 +174,12 @@ def dcpmla_map_positions(page_table: torch.Tensor, c: int, P: int, req: torch.Te
 # ---------------------------------------------------------------------------
 def dcpmla_slot_map(page_table: torch.Tensor, num_pages: int, c: int, P: int, req: torch.Tensor,
                     pos: torch.Tensor, vslot: Optional[torch.Tensor], owner: Optional[torch.Tensor],
-                    phys: Optional[torch.Tensor], err: Optional[torch.Tensor], stream=None) -> None:
+                    phys: Optional[torch.Tensor], err: Optional[torch.Tensor], stream=None,
+                    interleave: int = 1) -> None:
     n = pos.numel()
     _check(lib().dcpmla_slot_map(
         _dev(page_table, "page_table", torch.int32), page_table.shape[0], page_table.shape[1],
-        num_pages, c, P, _dev(req, "req", torch.int32), _dev(pos, "pos", torch.int64), n,
+        num_pages, c, interleave, P, _dev(req, "req", torch.int32), _dev(pos, "pos", torch.int64), n,
         _dev(vslot, "vslot", torch.int64, True), _dev(owner, "owner", torch.int32, True),
         _dev(phys, "phys", torch.int64, True), _dev(err, "err", torch.int32, True),
         _stream(stream)), "dcpmla_slot_map")
@@ -230,7 +231,7 @@ def dcpmla_decode(q: torch.Tensor, pools: Sequence[torch.Tensor],
                   page_table: torch.Tensor, seq_lens: torch.Tensor, P: int, c: int,
                   shard_begin: int, shard_count: int, sm_scale: float, lse_base: int,
                   o_part: torch.Tensor, lse_part: torch.Tensor, workspace: Optional[torch.Tensor],
-                  err: Optional[torch.Tensor], stream=None) -> None:
+                  err: Optional[torch.Tensor], stream=None, interleave: int = 1) -> None:
     """q: bf16 [B, Tq, H, 576]; pools: c tensors [pool_rows, 576]; page_table int32 [B, max_pages]."""
     B, Tq, H, _ = q.shape
     if len(pools) != c:
@@ -242,8 +243,8 @@ def dcpmla_decode(q: torch.Tensor, pools: Sequence[torch.Tensor],
     _check(lib().dcpmla_decode(
         _dev(q, "q", torch.bfloat16), parr, sarr, kv_dtype, pools[0].shape[0],
         _dev(page_table, "page_table", torch.int32), page_table.shape[1],
-        _dev(seq_lens, "seq_lens", torch.int32), B, Tq, H, P, c, shard_begin, shard_count,
-        float(sm_scale), lse_base, _dev(o_part, "o_part", torch.float32),
+        _dev(seq_lens, "seq_lens", torch.int32), B, Tq, H, P, c, interleave, shard_begin,
+        shard_count, float(sm_scale), lse_base, _dev(o_part, "o_part", torch.float32),
         _dev(lse_part, "lse_part", torch.float32), ws, ws_bytes,
         _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_decode")
 
@@ -279,3 +280,73 @@ def dcpmla_lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, c: int, rows:
         _dev(o_part, "o_part", torch.float32), _dev(lse_part, "lse_part", torch.float32), c, rows,
         lse_base, _dev(o, "o", torch.float32), _dev(lse, "lse", torch.float32, True),
         _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_lse_merge")
+
+
+# ---------------------------------------------------------------------------
+# Relayout, un-stripe gather, E4M3 quantising append, HiCache index filter
+# ---------------------------------------------------------------------------
+def dcpmla_relayout_dense_to_striped(dense: torch.Tensor, dense_scales: Optional[torch.Tensor],
+                                     dense_page_table: torch.Tensor, pools: Sequence[torch.Tensor],
+                                     scale_pools: Optional[Sequence[torch.Tensor]], kv_dtype: int,
+                                     page_table: torch.Tensor, seq_lens: torch.Tensor, P: int, c: int,
+                                     err: Optional[torch.Tensor], stream=None,
+                                     interleave: int = 1) -> None:
+    """dense: [dense_rows, 576] (bf16 or uint8 E4M3 codes); tables int32 [B, *]; pools: c tensors."""
+    B_ = page_table.shape[0]
+    parr = _ptr_array(pools, "pools")
+    sarr = None if scale_pools is None else _ptr_array(scale_pools, "scale_pools", torch.float32)
+    _check(lib().dcpmla_relayout_dense_to_striped(
+        _dev(dense, "dense"), _dev(dense_scales, "dense_scales", torch.float32, True), dense.shape[0],
+        _dev(dense_page_table, "dense_page_table", torch.int32), dense_page_table.shape[1], parr, sarr,
+        kv_dtype, pools[0].shape[0], _dev(page_table, "page_table", torch.int32), page_table.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), B_, P, c, interleave,
+        _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_relayout_dense_to_striped")
+
+
+def dcpmla_gather_unstriped(pools: Sequence[torch.Tensor], scale_pools: Optional[Sequence[torch.Tensor]],
+                            kv_dtype: int, page_table: torch.Tensor, seq_lens: torch.Tensor, P: int,
+                            c: int, out: torch.Tensor, out_scales: Optional[torch.Tensor],
+                            err: Optional[torch.Tensor], stream=None, interleave: int = 1) -> None:
+    """out: [B, capacity, 576] (kv dtype); out_scales: fp32 [B, capacity] for E4M3."""
+    parr = _ptr_array(pools, "pools")
+    sarr = None if scale_pools is None else _ptr_array(scale_pools, "scale_pools", torch.float32)
+    _check(lib().dcpmla_gather_unstriped(
+        parr, sarr, kv_dtype, pools[0].shape[0], _dev(page_table, "page_table", torch.int32),
+        page_table.shape[1], _dev(seq_lens, "seq_lens", torch.int32), page_table.shape[0], P, c,
+        interleave, _dev(out, "out"), _dev(out_scales, "out_scales", torch.float32, True), out.shape[1],
+        _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_gather_unstriped")
+
+
+def dcpmla_kv_append_e4m3(pools: Sequence[torch.Tensor], scale_pools: Sequence[torch.Tensor],
+                          owner: torch.Tensor, phys: torch.Tensor, ckv: torch.Tensor,
+                          krope: torch.Tensor, err: Optional[torch.Tensor], stream=None) -> None:
+    """ckv: bf16 [n, >=512], krope: bf16 [n, >=64] (rows may be strided)."""
+    n = owner.numel()
+    if ckv.dtype != torch.bfloat16 or krope.dtype != torch.bfloat16 or not ckv.is_cuda:
+        raise ValueError("ckv / krope must be bf16 CUDA tensors")
+    if ckv.stride(1) != 1 or krope.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    _check(lib().dcpmla_kv_append_e4m3(
+        _ptr_array(pools, "pools", torch.uint8), _ptr_array(scale_pools, "scale_pools", torch.float32),
+        pools[0].shape[0], len(pools), _dev(owner, "owner", torch.int32), _dev(phys, "phys", torch.int64),
+        C.c_void_p(ckv.data_ptr()), ckv.stride(0), C.c_void_p(krope.data_ptr()), krope.stride(0), n,
+        _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_kv_append_e4m3")
+
+
+def dcpmla_hicache_filter_workspace_size(n: int) -> int:
+    out = C.c_size_t()
+    _check(lib().dcpmla_hicache_filter_workspace_size(n, C.byref(out)), "dcpmla_hicache_filter_workspace_size")
+    return out.value
+
+
+def dcpmla_hicache_filter(idx: torch.Tensor, c: int, rank: int, out: torch.Tensor, count: torch.Tensor,
+                          workspace: Optional[torch.Tensor], err: Optional[torch.Tensor], stream=None,
+                          interleave: int = 1) -> None:
+    """idx: int64 [n] widened-page slots; out: int64 [n]; count: int64 [1] (device)."""
+    n = idx.numel()
+    ws = None if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().dcpmla_hicache_filter(
+        _dev(idx, "idx", torch.int64), n, c, interleave, rank, _dev(out, "out", torch.int64),
+        _dev(count, "count", torch.int64), ws, ws_bytes, _dev(err, "err", torch.int32, True),
+        _stream(stream)), "dcpmla_hicache_filter")

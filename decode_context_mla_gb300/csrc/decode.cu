@@ -15,11 +15,12 @@ namespace {
 int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* scale_pools,
               int32_t kv_dtype, int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
               const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
-              int32_t shard_begin, int32_t shard_count, float sm_scale, int32_t lse_base,
-              float* d_o_part, float* d_lse_part, int32_t* d_err, bool check_ptrs) {
+              int32_t interleave, int32_t shard_begin, int32_t shard_count, float sm_scale,
+              int32_t lse_base, float* d_o_part, float* d_lse_part, int32_t* d_err, bool check_ptrs) {
   if (B < 0 || Tq < 1 || H < 1 || P < 1 || c < 1 || c > DCPMLA_MAX_SHARDS || max_pages < 1 ||
       pool_rows < 0 || shard_begin < 0 || shard_count < 1 || shard_begin + shard_count > c)
     return DCPMLA_ERR_INVALID;
+  if (interleave < 1 || P % interleave) return DCPMLA_ERR_INVALID;
   if (lse_base != DCPMLA_LSE_E && lse_base != DCPMLA_LSE_2) return DCPMLA_ERR_INVALID;
   if (kv_dtype != DCPMLA_KV_BF16 && kv_dtype != DCPMLA_KV_E4M3) return DCPMLA_ERR_UNSUPPORTED;
   if (Tq > 16 || (int64_t)Tq * H > 1024) return DCPMLA_ERR_UNSUPPORTED;
@@ -32,7 +33,7 @@ int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* 
   a.pt = d_page_table;
   a.max_pages = max_pages;
   a.seq_lens = d_seq_lens;
-  a.B = B; a.Tq = Tq; a.H = H; a.R = Tq * H; a.P = P; a.c = c;
+  a.B = B; a.Tq = Tq; a.H = H; a.R = Tq * H; a.P = P; a.c = c; a.I = interleave;
   a.shard_begin = shard_begin;
   a.shard_count = shard_count;
   a.sm_scale = sm_scale;
@@ -74,7 +75,7 @@ int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, in
   if (!out) return DCPMLA_ERR_INVALID;
   DecodeArgs a;
   const int st = fill_args(a, nullptr, nullptr, nullptr, kv_dtype, 0, nullptr, max_pages, nullptr,
-                           B, Tq, H, P, c, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
+                           B, Tq, H, P, c, 1, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
                            nullptr, false);
   if (st != DCPMLA_OK) return st;
   const int sm = device_sm_count();
@@ -87,7 +88,7 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
                        int32_t kv_dtype, int32_t max_pages, int32_t* path, int32_t* kernel_launches) {
   DecodeArgs a;
   const int st = fill_args(a, nullptr, nullptr, nullptr, kv_dtype, 0, nullptr, max_pages, nullptr,
-                           B, Tq, H, P, c, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
+                           B, Tq, H, P, c, 1, 0, shard_count, 1.f, DCPMLA_LSE_E, nullptr, nullptr,
                            nullptr, false);
   if (st != DCPMLA_OK) return st;
   const int sm = device_sm_count();
@@ -107,13 +108,13 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
 int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools, int32_t kv_dtype,
                   int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
                   const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P,
-                  int32_t c, int32_t shard_begin, int32_t shard_count, float sm_scale,
-                  int32_t lse_base, float* d_o_part, float* d_lse_part, void* d_workspace,
-                  size_t ws_bytes, int32_t* d_err, void* stream) {
+                  int32_t c, int32_t interleave, int32_t shard_begin, int32_t shard_count,
+                  float sm_scale, int32_t lse_base, float* d_o_part, float* d_lse_part,
+                  void* d_workspace, size_t ws_bytes, int32_t* d_err, void* stream) {
   DecodeArgs a;
   int st = fill_args(a, d_q, pools, scale_pools, kv_dtype, pool_rows, d_page_table, max_pages,
-                     d_seq_lens, B, Tq, H, P, c, shard_begin, shard_count, sm_scale, lse_base,
-                     d_o_part, d_lse_part, d_err, true);
+                     d_seq_lens, B, Tq, H, P, c, interleave, shard_begin, shard_count, sm_scale,
+                     lse_base, d_o_part, d_lse_part, d_err, true);
   if (st != DCPMLA_OK) return st;
   if (B == 0) return DCPMLA_OK;
   const int sm = device_sm_count();
@@ -167,7 +168,7 @@ extern "C" int dcpmla_decode_noalloc(const void* d_q, void* const* pools,
                                      int32_t* d_err, void* stream) {
   DecodeArgs a;
   int st = fill_args(a, d_q, pools, scale_pools, kv_dtype, pool_rows, d_page_table, max_pages,
-                     d_seq_lens, B, Tq, H, P, c, shard_begin, shard_count, sm_scale, lse_base,
+                     d_seq_lens, B, Tq, H, P, c, 1, shard_begin, shard_count, sm_scale, lse_base,
                      d_o_part, d_lse_part, d_err, true);
   if (st != DCPMLA_OK) return st;
   if (B == 0) return DCPMLA_OK;

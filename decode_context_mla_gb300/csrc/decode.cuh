@@ -17,6 +17,7 @@ struct DecodeArgs {
   int32_t max_pages;
   const int32_t* seq_lens;  // [B], global lengths
   int32_t B, Tq, H, R, P, c, shard_begin, shard_count;
+  int32_t I;                // interleave size: tokens go to shards in runs of I
   float sm_scale;
   bool base2;
   float* o_part;            // [shard_count, B, R, 512]

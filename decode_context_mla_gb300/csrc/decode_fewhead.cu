@@ -104,7 +104,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Tokens of request b on shard r (0 for a length the launch rejects).
 __device__ __forceinline__ int shard_tokens(const DecodeArgs& a, int L, int r) {
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) return 0;
-  return L > r ? (L - r + a.c - 1) / a.c : 0;
+  return shard_len(L, r, a.c, a.I);
 }
 
 struct Unit {
@@ -162,7 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int* sPre = reinterpret_cast<int*>(smem + kOffPre);
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ uint64_t bar_q_full[2], bar_q_free[2];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_p_free[2], bar_o_free[2];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_p_free[2], bar_o_free[2], bar_o_full[2];
   __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
   __shared__ uint64_t bar_o, bar_drain;
   __shared__ __align__(16) float red_s[2][2][4][8];     // [tile parity][warpgroup][quarter][row]
@@ -191,6 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);
       mbar_init(smem_u32(&bar_p_free[s]), 1);
       mbar_init(smem_u32(&bar_o_free[s]), kSoftmaxThreads);
+      mbar_init(smem_u32(&bar_o_full[s]), 1);
     }
     mbar_init(smem_u32(&bar_x_full), 1);
     mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
@@ -375,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (uq < units && (ntq = get_unit(a, sPre, nitems, chunk_tiles, uq).ntiles) == 0) uq += G;
       int gq = 0, gp = 0;                 // next tile to QK / to PV
       int pv_ob[2], pv_kk[2];
-      bool pv_first[2];
+      bool pv_first[2], pv_last[2];
       long long t_idle = clock64();
       while (gp < total) {
         bool progressed = false;
@@ -399,6 +400,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(&bar_kv_empty[sb]));
             mma_commit(smem_u32(&bar_p_free[sb]));
             mma_commit(smem_u32(&bar_o));
+            // the unit's O^T is complete: one phase of its buffer's barrier per unit
+            if (pv_last[sb]) mma_commit(smem_u32(&bar_o_full[ob]));
             ++gp;
             progressed = true;
           }
@@ -422,6 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pv_ob[sb] = kkq & 1;
             pv_kk[sb] = kkq;
             pv_first[sb] = iq == 0;
+            pv_last[sb] = iq == ntq - 1;
             if (++iq == ntq) {               // last tile of the unit: its Q buffer may be refilled
               mma_commit(smem_u32(&bar_q_free[qb]));
               iq = 0;
@@ -535,8 +539,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(smem_u32(&bar_x_read));
         // causal / tail / padding-row mask, base-2 scaling
-        const bool full_vis = all_rows && ntok == kTok && (int64_t)(t0 + kTok - 1) * a.c + x.r <= qpos_min;
-        const int64_t kpos = (int64_t)(t0 + tok) * a.c + x.r;
+        const bool full_vis = all_rows && ntok == kTok && shard_pos(t0 + kTok - 1, x.r, a.c, a.I) <= qpos_min;
+        const int64_t kpos = shard_pos(t0 + tok, x.r, a.c, a.I);
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
           const bool vis = full_vis || (rvalid[n] && tok < ntok && kpos <= qpos[n]);
@@ -641,7 +645,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- unit epilogue: O^T / l, partial or final output ----
       if (x.ntiles > 0) {
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
+        // Not bar_o: when the last tile's softmax ends, the PV two tiles back may
+        // still be running, and a parity wait on bar_o would then match an older
+        // phase.  bar_o_full[ob] completes once per unit on this buffer.
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full[ob]), (kk >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
       }

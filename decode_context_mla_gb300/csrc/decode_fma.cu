@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fma_kernel(const FmaParams
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
     if (tid == 0) bad_s = DCPMLA_DERR_LENGTH;
   } else {
-    const int n = L > r ? (L - r + a.c - 1) / a.c : 0;   // tokens of b on shard r
+    const int n = shard_len(L, r, a.c, a.I);   // tokens of b on shard r
     j0 = min(split * fp.chunk, n);
     j1 = min(n, j0 + fp.chunk);
     // Every split checks all of the request's pages, so a bad entry empties the
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fma_kernel(const FmaParams
         s = fmaf(qb.z, k[6], s); s = fmaf(qb.w, k[7], s);
       }
       const int j = ts + lane;
-      const bool vis = (lane < ntok) && (j * a.c + r <= qpos);
+      const bool vis = (lane < ntok) && (shard_pos(j, r, a.c, a.I) <= qpos);
       float kscale = 1.f;
       if (kFp8 && lane < ntok) kscale = scl_s[buf * kTile + lane];
       s = vis ? s * kscale : -INFINITY;

@@ -130,7 +130,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
   __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
-  __shared__ uint64_t bar_q_full, bar_o, bar_drain, bar_l;
+  __shared__ uint64_t bar_q_full, bar_o, bar_o_full, bar_drain, bar_l;
   __shared__ float xmax_s[2][2][kRows];
   __shared__ float l_s[2][kRows];
   __shared__ float kscale_s[kFp8 ? kStages : 1][kTileTok];
@@ -167,6 +167,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_o_full), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_s = 0;
     bad_s = 0;
@@ -181,7 +182,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
     if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
   } else {
-    const int n = L > r ? (L - r + a.c - 1) / a.c : 0;
+    const int n = shard_len(L, r, a.c, a.I);
     j0 = min(split * p.chunk, n);
     j1 = min(n, j0 + p.chunk);
     npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
@@ -321,6 +322,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
             mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, 1u);
           mma_commit(smem_u32(&bar_kv_empty[st]));
           mma_commit(smem_u32(&bar_o));
+          if (pi == ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // O complete
         }
       }
       // drain: every MMA issued above completes before TMEM is released
@@ -477,12 +479,12 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
         for (int k = 0; k < 32; ++k) x[k] *= ks[k];
       }
       // causal / tail mask on raw scores (only tiles that need it)
-      const bool full_vis = ntok == kTileTok && (t0 + kTileTok - 1) * a.c + r <= qpos_min;
+      const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
       if (!full_vis) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const int kk = 32 * g + k;
-          const bool vis = kk < ntok && (t0 + kk) * a.c + r <= qpos;
+          const bool vis = kk < ntok && shard_pos(t0 + kk, r, a.c, a.I) <= qpos;
           x[k] = vis ? x[k] : -INFINITY;
         }
       }
@@ -568,7 +570,9 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     }
     // ---- epilogue ----
     if (ok && ntiles > 0)
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (ntiles - 1) & 1, abort_flag));
+      // Not bar_o: when the last tile's softmax ends, PV(ntiles - 2) may still be
+      // running, and a parity wait on bar_o would then match an older phase.
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
     l_s[g][row] = l;
     mbar_arrive(smem_u32(&bar_l));
     const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));

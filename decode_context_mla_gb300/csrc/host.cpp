@@ -215,10 +215,12 @@ int dcpmla_reqmap_page_table(const dcpmla_reqmap* m, const int32_t* reqs, int32_
   return DCPMLA_OK;
 }
 
-int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c, int32_t P,
-                         const int32_t* req, const int64_t* pos, int64_t n, int64_t* vslot,
+int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c, int32_t interleave,
+                         int32_t P, const int32_t* req, const int64_t* pos, int64_t n, int64_t* vslot,
                          int32_t* owner, int64_t* phys) {
   if (n < 0 || c < 1 || P < 1 || max_pages < 1) return DCPMLA_ERR_INVALID;
+  if (interleave < 1 || P % interleave) return DCPMLA_ERR_INVALID;
+  const int64_t I = interleave;
   if (n > 0 && (!page_table || !req || !pos)) return DCPMLA_ERR_INVALID;
   const int64_t vp = (int64_t)P * c;
   for (int64_t i = 0; i < n; ++i) {
@@ -229,8 +231,8 @@ int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c
     if (g < 0) return DCPMLA_ERR_INVALID;
     const int64_t v = (int64_t)g * vp + pos[i] % vp;
     if (vslot) vslot[i] = v;
-    if (owner) owner[i] = (int32_t)(v % c);
-    if (phys) phys[i] = v / c;
+    if (owner) owner[i] = (int32_t)((v / I) % c);
+    if (phys) phys[i] = (v / (I * c)) * I + v % I;
   }
   return DCPMLA_OK;
 }

@@ -32,7 +32,7 @@ int device_sm_count() {
 // Slot map: (request, position) -> (virtual slot, owner, physical slot)
 // ---------------------------------------------------------------------------
 __global__ void slot_map_kernel(const int32_t* __restrict__ pt, int32_t n_requests,
-                                int32_t max_pages, int64_t num_pages, int32_t c, int32_t P,
+                                int32_t max_pages, int64_t num_pages, int32_t c, int32_t I, int32_t P,
                                 const int32_t* __restrict__ req, const int64_t* __restrict__ pos,
                                 int64_t n, int64_t* vslot, int32_t* owner, int64_t* phys,
                                 int32_t* err) {
@@ -54,8 +54,9 @@ __global__ void slot_map_kernel(const int32_t* __restrict__ pt, int32_t n_reques
   }
   if (bad) set_err(err, bad);
   if (vslot) vslot[i] = v;
-  if (owner) owner[i] = bad ? -1 : (int32_t)(v % c);
-  if (phys) phys[i] = bad ? -1 : v / c;
+  // runs of I consecutive slots per rank; I = 1 is owner = v mod c, phys = floor(v / c)
+  if (owner) owner[i] = bad ? -1 : (int32_t)((v / I) % c);
+  if (phys) phys[i] = bad ? -1 : (v / ((int64_t)I * c)) * I + v % I;
 }
 
 // ---------------------------------------------------------------------------
@@ -140,20 +141,21 @@ using namespace dcpmla;
 extern "C" {
 
 int dcpmla_slot_map(const int32_t* d_page_table, int32_t n_requests, int32_t max_pages,
-                    int64_t num_pages, int32_t c, int32_t P, const int32_t* d_req,
+                    int64_t num_pages, int32_t c, int32_t interleave, int32_t P, const int32_t* d_req,
                     const int64_t* d_pos, int64_t n, int64_t* d_vslot, int32_t* d_owner,
                     int64_t* d_phys, int32_t* d_err, void* stream) {
   if (n < 0 || c < 1 || c > DCPMLA_MAX_SHARDS || P < 1 || max_pages < 1 || n_requests < 0 ||
       num_pages < 0)
     return DCPMLA_ERR_INVALID;
+  if (interleave < 1 || P % interleave) return DCPMLA_ERR_INVALID;
   if (n == 0) return DCPMLA_OK;
   if (!d_page_table || !d_req || !d_pos) return DCPMLA_ERR_INVALID;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
   if (blocks > INT32_MAX) return DCPMLA_ERR_UNSUPPORTED;
   slot_map_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
-      d_page_table, n_requests, max_pages, num_pages, c, P, d_req, d_pos, n, d_vslot, d_owner,
-      d_phys, d_err);
+      d_page_table, n_requests, max_pages, num_pages, c, interleave, P, d_req, d_pos, n, d_vslot,
+      d_owner, d_phys, d_err);
   return launch_status();
 }
 

@@ -1,0 +1,411 @@
+// Layout moves around the striped cache, and the quantising append.
+//
+//   relayout  SGLang "Decode Context Parallelism" docs, DCP x PD disaggregation:
+//             a DCP-1 prefill cache (dense pages) is copied token by token into
+//             the striped decode pools; the plan carries the exact token count, so
+//             rows of a partial final page are not copied.
+//   gather    same page, Communication backends (extend gathers the cached prefix
+//             shards and restores token order); vLLM GLM-5.3 serving post, DCP
+//             section (a temporary full-context copy): striped pools -> one
+//             contiguous copy per request in token order.
+//   HiCache   same page, DCP x HiCache L2: an index list in widened-page slot
+//             space keeps the slots this rank owns, mapped to local slots.
+//   E4M3 append  per-token amax / 448 scale, codes rounded to nearest-even,
+//             written to the owner pool with the scale.
+//
+// All are HBM- or latency-bound; none uses the tensor cores.
+#include <algorithm>
+
+#include "decode.cuh"
+
+using namespace dcpmla;
+
+namespace {
+
+constexpr int kTokPerIter = 32;   // tokens a block copies per loop iteration
+
+// Where position p of request b lives in the striped pools (owner, physical slot),
+// or owner -1 when the page-table entry is outside the pools.
+struct Slot {
+  int32_t owner;
+  int64_t phys;
+};
+__device__ __forceinline__ Slot striped_slot(const int32_t* vpt_row, int64_t p, int32_t c, int32_t I, int32_t P,
+                                             int64_t num_pages) {
+  const int64_t vp = (int64_t)P * c;
+  const int32_t g = __ldg(vpt_row + p / vp);
+  Slot s;
+  if (g < 0 || (int64_t)g >= num_pages) {
+    s.owner = -1;
+    s.phys = -1;
+    return s;
+  }
+  const int64_t v = (int64_t)g * vp + p % vp;
+  s.owner = (int32_t)((v / I) % c);
+  s.phys = (v / ((int64_t)I * c)) * I + v % I;
+  return s;
+}
+
+__device__ __forceinline__ int64_t dense_slot(const int32_t* dpt_row, int64_t p, int32_t P, int64_t dense_pages) {
+  const int32_t g = __ldg(dpt_row + p / P);
+  if (g < 0 || (int64_t)g >= dense_pages) return -1;
+  return (int64_t)g * P + p % P;
+}
+
+// dir = 0: dense -> striped (relayout); dir = 1: striped -> contiguous (gather).
+template <int kDir>
+__global__ void __launch_bounds__(256) move_rows_kernel(
+    const uint8_t* __restrict__ dense, const float* __restrict__ dense_scales, int64_t dense_rows,
+    const int32_t* __restrict__ dense_pt, int32_t dense_max_pages, ShardPtrs pools, int64_t pool_rows,
+    const int32_t* __restrict__ pt, int32_t max_pages, const int32_t* __restrict__ lens, int32_t P, int32_t c,
+    int32_t I, int32_t row_bytes, bool fp8, uint8_t* __restrict__ out, float* __restrict__ out_scales,
+    int64_t out_cap, int32_t* err) {
+  const int b = blockIdx.y;
+  const int64_t L = __ldg(lens + b);
+  const int64_t limit = kDir == 0 ? min((int64_t)dense_max_pages * P, (int64_t)max_pages * P * c)
+                                  : min(out_cap, (int64_t)max_pages * P * c);
+  if (L < 0 || L > limit) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_err(err, DCPMLA_DERR_LENGTH);
+    return;
+  }
+  const int chunks = row_bytes / 16;
+  const int32_t* vpt_row = pt + (int64_t)b * max_pages;
+  const int32_t* dpt_row = kDir == 0 ? dense_pt + (int64_t)b * dense_max_pages : nullptr;
+  const int64_t num_pages = pool_rows / P, dense_pages = dense_rows / P;
+  for (int64_t t0 = (int64_t)blockIdx.x * kTokPerIter; t0 < L; t0 += (int64_t)gridDim.x * kTokPerIter) {
+    for (int e = threadIdx.x; e < kTokPerIter * chunks; e += blockDim.x) {
+      const int64_t p = t0 + e / chunks;
+      const int ch = e % chunks;
+      if (p >= L) continue;
+      const Slot s = striped_slot(vpt_row, p, c, I, P, num_pages);
+      if (s.owner < 0) {
+        if (ch == 0) set_err(err, DCPMLA_DERR_PAGE);
+        continue;
+      }
+      uint8_t* pool = static_cast<uint8_t*>(pools.pool[s.owner]);
+      if (kDir == 0) {
+        const int64_t d = dense_slot(dpt_row, p, P, dense_pages);
+        if (d < 0) {
+          if (ch == 0) set_err(err, DCPMLA_DERR_PAGE);
+          continue;
+        }
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(dense + d * row_bytes) + ch);
+        reinterpret_cast<uint4*>(pool + s.phys * row_bytes)[ch] = v;
+        if (fp8 && ch == 0) pools.scale[s.owner][s.phys] = __ldcs(dense_scales + d);
+      } else {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(pool + s.phys * row_bytes) + ch);
+        reinterpret_cast<uint4*>(out + ((int64_t)b * out_cap + p) * row_bytes)[ch] = v;
+        if (fp8 && ch == 0) out_scales[(int64_t)b * out_cap + p] = __ldcs(pools.scale[s.owner] + s.phys);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// E4M3 quantising append: one warp per new token row (576 bf16 values).
+// Lane l holds latent values [16l, 16l + 16); lanes 0-3 also rope values
+// [16l, 16l + 16).  In float32: amax = max |x|, scale = amax / 448 (IEEE
+// division), code = E4M3(clamp(x / scale, +-448)) rounded to nearest-even; a row of
+// zeros stores scale 0 and zero codes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(256) append_e4m3_kernel(
+    ShardPtrs dst, int64_t pool_rows, int32_t c, const int32_t* __restrict__ owner,
+    const int64_t* __restrict__ phys, const uint8_t* __restrict__ ckv, int64_t ckv_stride_b,
+    const uint8_t* __restrict__ krope, int64_t krope_stride_b, int64_t n, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= n) return;
+  const int32_t r = __ldg(owner + row);
+  const int64_t s = __ldg(phys + row);
+  if (r < 0 || r >= c || s < 0 || s >= pool_rows) {   // uniform across the warp
+    if (lane == 0) set_err(err, DCPMLA_DERR_SLOT);
+    return;
+  }
+  float lat[16], rope[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(ckv + row * ckv_stride_b) + 2 * lane;
+    float a[8], b[8];
+    unpack_bf16x8(__ldg(src), a);
+    unpack_bf16x8(__ldg(src + 1), b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      lat[i] = a[i];
+      lat[8 + i] = b[i];
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(lat[i]));
+  if (lane < 4) {
+    const uint4* src = reinterpret_cast<const uint4*>(krope + row * krope_stride_b) + 2 * lane;
+    float a[8], b[8];
+    unpack_bf16x8(__ldg(src), a);
+    unpack_bf16x8(__ldg(src + 1), b);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      rope[i] = a[i];
+      rope[8 + i] = b[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(rope[i]));
+  }
+  // non-negative floats order like their bit patterns
+  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+  const float scale = __fdiv_rn(amax, 448.f);
+  uint8_t* prow = static_cast<uint8_t*>(dst.pool[r]) + s * kDK;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = 4 * k;
+    if (scale > 0.f) {
+      float y[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[m] = fminf(fmaxf(__fdiv_rn(lat[i + m], scale), -448.f), 448.f);
+      w[k] = (uint32_t)e4m3x2(y[0], y[1]) | ((uint32_t)e4m3x2(y[2], y[3]) << 16);
+    } else {
+      w[k] = 0u;
+    }
+  }
+  reinterpret_cast<uint4*>(prow)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+  if (lane < 4) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = 4 * k;
+      if (scale > 0.f) {
+        float y[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = fminf(fmaxf(__fdiv_rn(rope[i + m], scale), -448.f), 448.f);
+        w[k] = (uint32_t)e4m3x2(y[0], y[1]) | ((uint32_t)e4m3x2(y[2], y[3]) << 16);
+      } else {
+        w[k] = 0u;
+      }
+    }
+    reinterpret_cast<uint4*>(prow + kDL)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (lane == 0) dst.scale[r][s] = scale;
+}
+
+// ---------------------------------------------------------------------------
+// HiCache index filter: order-preserving compaction in three launches.
+// ---------------------------------------------------------------------------
+constexpr int kFilterBlock = 1024;   // indices per block (256 threads x 4)
+
+__device__ __forceinline__ bool owned(int64_t i, int32_t c, int32_t I, int32_t rank) {
+  return i >= 0 && (int32_t)((i / I) % c) == rank;
+}
+
+__global__ void __launch_bounds__(256) filter_count_kernel(const int64_t* __restrict__ idx, int64_t n, int32_t c,
+                                                           int32_t I, int32_t rank, uint32_t* counts,
+                                                           int32_t* err) {
+  __shared__ uint32_t warp_n[8];
+  const int64_t base = (int64_t)blockIdx.x * kFilterBlock;
+  uint32_t k = 0;
+  bool neg = false;
+  for (int e = threadIdx.x; e < kFilterBlock; e += 256) {
+    const int64_t i = base + e;
+    if (i >= n) break;
+    const int64_t v = __ldg(idx + i);
+    neg |= v < 0;
+    k += owned(v, c, I, rank) ? 1u : 0u;
+  }
+  if (neg) set_err(err, DCPMLA_DERR_POSITION);
+  k = __reduce_add_sync(0xffffffffu, k);
+  if ((threadIdx.x & 31) == 0) warp_n[threadIdx.x >> 5] = k;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < 8; ++w) t += warp_n[w];
+    counts[blockIdx.x] = t;
+  }
+}
+
+// Exclusive scan of the block counts in place (one block); the total goes to *count.
+__global__ void __launch_bounds__(1024) filter_scan_kernel(uint32_t* counts, int64_t nblocks, int64_t* count) {
+  __shared__ uint32_t part[1024];
+  const int t = threadIdx.x;
+  const int64_t per = (nblocks + 1023) / 1024;
+  const int64_t b0 = min(nblocks, (int64_t)t * per), b1 = min(nblocks, b0 + per);
+  uint32_t s = 0;
+  for (int64_t b = b0; b < b1; ++b) s += counts[b];
+  part[t] = s;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {   // inclusive Hillis-Steele scan of the parts
+    const uint32_t v = t >= d ? part[t - d] : 0u;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  uint32_t run = part[t] - s;
+  for (int64_t b = b0; b < b1; ++b) {
+    const uint32_t v = counts[b];
+    counts[b] = run;
+    run += v;
+  }
+  if (t == 1023) *count = (int64_t)part[1023];
+}
+
+__global__ void __launch_bounds__(256) filter_scatter_kernel(const int64_t* __restrict__ idx, int64_t n, int32_t c,
+                                                             int32_t I, int32_t rank,
+                                                             const uint32_t* __restrict__ offsets,
+                                                             int64_t* __restrict__ out) {
+  __shared__ uint32_t warp_n[8];
+  const int64_t base = (int64_t)blockIdx.x * kFilterBlock;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // each warp takes 128 consecutive indices (4 rounds of 32), in order
+  int64_t v[4];
+  bool keep[4];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t i = base + warp * 128 + k * 32 + lane;
+    v[k] = i < n ? __ldg(idx + i) : -1;
+    keep[k] = i < n && owned(v[k], c, I, rank);
+    mine += __popc(__ballot_sync(0xffffffffu, keep[k]));
+  }
+  if (lane == 0) warp_n[warp] = mine;
+  __syncthreads();
+  uint32_t pos = offsets[blockIdx.x];
+  for (int w = 0; w < warp; ++w) pos += warp_n[w];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep[k]);
+    if (keep[k]) {
+      const int64_t x = v[k];
+      out[pos + __popc(bal & ((1u << lane) - 1u))] = (x / ((int64_t)I * c)) * I + x % I;
+    }
+    pos += __popc(bal);
+  }
+}
+
+int check_pools(void* const* pools, float* const* scale_pools, int32_t c, bool fp8, ShardPtrs& sp) {
+  sp = ShardPtrs{};
+  for (int r = 0; r < c; ++r) {
+    if (!pools[r] || !aligned16(pools[r])) return DCPMLA_ERR_INVALID;
+    sp.pool[r] = pools[r];
+    if (fp8) {
+      if (!scale_pools || !scale_pools[r]) return DCPMLA_ERR_INVALID;
+      sp.scale[r] = scale_pools[r];
+    }
+  }
+  return DCPMLA_OK;
+}
+
+int move_grid_x(int32_t max_pages, int32_t P, int32_t c) {
+  const int64_t tokens = (int64_t)max_pages * P * c;
+  const int64_t blocks = (tokens + kTokPerIter - 1) / kTokPerIter;
+  return (int)std::min<int64_t>(std::max<int64_t>(blocks, 1), 128);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dcpmla_relayout_dense_to_striped(const void* d_dense, const float* d_dense_scales, int64_t dense_rows,
+                                     const int32_t* d_dense_page_table, int32_t dense_max_pages,
+                                     void* const* pools, float* const* scale_pools, int32_t kv_dtype,
+                                     int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+                                     const int32_t* d_seq_lens, int32_t B, int32_t P, int32_t c,
+                                     int32_t interleave, int32_t* d_err, void* stream) {
+  if (B < 0 || P < 1 || c < 1 || c > DCPMLA_MAX_SHARDS || max_pages < 1 || dense_max_pages < 1 ||
+      pool_rows < 0 || dense_rows < 0 || interleave < 1 || P % interleave)
+    return DCPMLA_ERR_INVALID;
+  if (kv_dtype != DCPMLA_KV_BF16 && kv_dtype != DCPMLA_KV_E4M3) return DCPMLA_ERR_UNSUPPORTED;
+  if (B == 0) return DCPMLA_OK;
+  const bool fp8 = kv_dtype == DCPMLA_KV_E4M3;
+  if (!d_dense || !aligned16(d_dense) || !pools || !d_dense_page_table || !d_page_table || !d_seq_lens)
+    return DCPMLA_ERR_INVALID;
+  if (fp8 && !d_dense_scales) return DCPMLA_ERR_INVALID;
+  ShardPtrs sp;
+  const int rc = check_pools(pools, scale_pools, c, fp8, sp);
+  if (rc != DCPMLA_OK) return rc;
+  if (B > 65535) return DCPMLA_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)move_grid_x(max_pages, P, c), (unsigned)B);
+  move_rows_kernel<0><<<grid, 256, 0, (cudaStream_t)stream>>>(
+      static_cast<const uint8_t*>(d_dense), d_dense_scales, dense_rows, d_dense_page_table, dense_max_pages, sp,
+      pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave, fp8 ? kDK : 2 * kDK, fp8, nullptr,
+      nullptr, 0, d_err);
+  return launch_status();
+}
+
+int dcpmla_gather_unstriped(void* const* pools, float* const* scale_pools, int32_t kv_dtype, int64_t pool_rows,
+                            const int32_t* d_page_table, int32_t max_pages, const int32_t* d_seq_lens, int32_t B,
+                            int32_t P, int32_t c, int32_t interleave, void* d_out, float* d_out_scales,
+                            int64_t out_capacity, int32_t* d_err, void* stream) {
+  if (B < 0 || P < 1 || c < 1 || c > DCPMLA_MAX_SHARDS || max_pages < 1 || pool_rows < 0 || out_capacity < 0 ||
+      interleave < 1 || P % interleave)
+    return DCPMLA_ERR_INVALID;
+  if (kv_dtype != DCPMLA_KV_BF16 && kv_dtype != DCPMLA_KV_E4M3) return DCPMLA_ERR_UNSUPPORTED;
+  if (B == 0) return DCPMLA_OK;
+  const bool fp8 = kv_dtype == DCPMLA_KV_E4M3;
+  if (!d_out || !aligned16(d_out) || !pools || !d_page_table || !d_seq_lens) return DCPMLA_ERR_INVALID;
+  if (fp8 && !d_out_scales) return DCPMLA_ERR_INVALID;
+  ShardPtrs sp;
+  const int rc = check_pools(pools, scale_pools, c, fp8, sp);
+  if (rc != DCPMLA_OK) return rc;
+  if (B > 65535) return DCPMLA_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)move_grid_x(max_pages, P, c), (unsigned)B);
+  move_rows_kernel<1><<<grid, 256, 0, (cudaStream_t)stream>>>(
+      nullptr, nullptr, 0, nullptr, 1, sp, pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave,
+      fp8 ? kDK : 2 * kDK, fp8, static_cast<uint8_t*>(d_out), d_out_scales, out_capacity, d_err);
+  return launch_status();
+}
+
+int dcpmla_kv_append_e4m3(void* const* pools, float* const* scale_pools, int64_t pool_rows, int32_t c,
+                          const int32_t* d_owner, const int64_t* d_phys, const void* d_ckv, int64_t ckv_stride,
+                          const void* d_krope, int64_t krope_stride, int64_t n, int32_t* d_err, void* stream) {
+  if (c < 1 || c > DCPMLA_MAX_SHARDS || n < 0 || pool_rows < 0) return DCPMLA_ERR_INVALID;
+  if (n == 0) return DCPMLA_OK;
+  if (!pools || !scale_pools || !d_owner || !d_phys || !d_ckv || !d_krope) return DCPMLA_ERR_INVALID;
+  if (!aligned16(d_ckv) || !aligned16(d_krope) || ckv_stride < kDL || krope_stride < kDR ||
+      (ckv_stride * 2) % 16 || (krope_stride * 2) % 16)
+    return DCPMLA_ERR_INVALID;
+  ShardPtrs sp;
+  const int rc = check_pools(pools, scale_pools, c, true, sp);
+  if (rc != DCPMLA_OK) return rc;
+  const int64_t blocks = (n * 32 + 255) / 256;
+  if (blocks > INT32_MAX) return DCPMLA_ERR_UNSUPPORTED;
+  append_e4m3_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+      sp, pool_rows, c, d_owner, d_phys, static_cast<const uint8_t*>(d_ckv), ckv_stride * 2,
+      static_cast<const uint8_t*>(d_krope), krope_stride * 2, n, d_err);
+  return launch_status();
+}
+
+int dcpmla_hicache_filter_workspace_size(int64_t n, size_t* out) {
+  if (n < 0 || !out) return DCPMLA_ERR_INVALID;
+  *out = (size_t)((n + kFilterBlock - 1) / kFilterBlock) * 4;
+  return DCPMLA_OK;
+}
+
+int dcpmla_hicache_filter(const int64_t* d_idx, int64_t n, int32_t c, int32_t interleave, int32_t rank,
+                          int64_t* d_out, int64_t* d_count, void* d_workspace, size_t ws_bytes, int32_t* d_err,
+                          void* stream) {
+  if (n < 0 || c < 1 || interleave < 1 || rank < 0 || rank >= c || !d_count) return DCPMLA_ERR_INVALID;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (n == 0) return cudaMemsetAsync(d_count, 0, sizeof(int64_t), st) == cudaSuccess ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+  if (!d_idx || !d_out) return DCPMLA_ERR_INVALID;
+  const int64_t nb = (n + kFilterBlock - 1) / kFilterBlock;
+  if ((size_t)nb * 4 > ws_bytes || !d_workspace) return DCPMLA_ERR_CAPACITY;
+  if (nb > INT32_MAX || n > (int64_t)UINT32_MAX) return DCPMLA_ERR_UNSUPPORTED;
+  uint32_t* counts = static_cast<uint32_t*>(d_workspace);
+  filter_count_kernel<<<(unsigned)nb, 256, 0, st>>>(d_idx, n, c, interleave, rank, counts, d_err);
+  filter_scan_kernel<<<1, 1024, 0, st>>>(counts, nb, d_count);
+  filter_scatter_kernel<<<(unsigned)nb, 256, 0, st>>>(d_idx, n, c, interleave, rank, counts, d_out);
+  return launch_status();
+}
+
+}  // extern "C"

@@ -21,8 +21,9 @@ class StripedKVCache:
 
     def __init__(self, c: int, P: int, num_pages: int, kv_dtype: int, max_requests: int,
                  max_pages_per_request: int, initial_order: Optional[torch.Tensor] = None,
-                 device="cuda", fill_byte: Optional[int] = None):
+                 device="cuda", fill_byte: Optional[int] = None, interleave: int = 1):
         self.c, self.P, self.num_pages, self.kv_dtype = c, P, num_pages, kv_dtype
+        self.interleave = interleave
         self.max_pages = max_pages_per_request
         self.alloc = B.dcpmla_alloc_create(c, num_pages * P, P, initial_order)
         self.reqmap = B.dcpmla_reqmap_create(self.alloc, max_requests, max_pages_per_request)
@@ -62,7 +63,7 @@ class StripedKVCache:
                stream=None) -> None:
         """Slot map then compacting write of len(pos_d) new rows (device tensors)."""
         B.dcpmla_slot_map(page_table_d, self.num_pages, self.c, self.P, req_d, pos_d, vslot_d,
-                          owner_d, phys_d, self.err, stream)
+                          owner_d, phys_d, self.err, stream, interleave=self.interleave)
         B.dcpmla_kv_append(self.pools, self.scales, self.kv_dtype, owner_d, phys_d, ckv, krope,
                            row_scales, self.err, stream)
 
@@ -141,7 +142,7 @@ class DecodeStep:
         c = self.cache
         B.dcpmla_decode(self.q, c.pools, c.scales, c.kv_dtype, self.page_table, self.seq_lens, c.P,
                         c.c, 0, c.c, self.sm_scale, self.lse_base, self.o_part, self.lse_part,
-                        self.workspace, c.err, stream)
+                        self.workspace, c.err, stream, interleave=c.interleave)
 
     def run_merge(self, stream=None) -> None:
         """Exact LSE merge of the c partials into o, lse."""

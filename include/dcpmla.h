@@ -128,17 +128,27 @@ int dcpmla_reqmap_page_table(const dcpmla_reqmap* m, const int32_t* reqs, int32_
                              int32_t max_pages, int32_t pad, int32_t* out_table,
                              int32_t* out_seq_lens);
 
+/* Interleave size (vLLM DCP study page, configuration example: the DCP KV
+ * interleave size, default 1 token): tokens go to ranks in runs of
+ * `interleave` consecutive virtual slots, round-robin over the c ranks:
+ *   owner(v) = floor(v / I) mod c,   physical(v) = floor(v / (I*c)) * I + v mod I,
+ * which for I = 1 is the SGLang layout owner = v mod c, physical = floor(v / c).
+ * I must divide P, so that a widened page of P*c slots is still one physical
+ * page of P slots on every rank (page id g on every pool); a call with I < 1 or
+ * P mod I != 0 returns DCPMLA_ERR_INVALID.  Shard r's local token j is then
+ * global position floor(j / I) * I * c + r * I + j mod I. */
+
 /* Host position map (same arithmetic as dcpmla_slot_map, on host arrays).
  * For i < n: request req[i] (a row of page_table [*, max_pages]), position
- * pos[i] -> vslot[i], owner[i] = vslot mod c, phys[i] = floor(vslot / c).
+ * pos[i] -> vslot[i], owner[i] and phys[i] as above (I = interleave).
  * ERR_INVALID if a position's page entry is negative or beyond max_pages. */
-int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c, int32_t P,
-                         const int32_t* req, const int64_t* pos, int64_t n,
-                         int64_t* vslot, int32_t* owner, int64_t* phys);
+int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c,
+                         int32_t interleave, int32_t P, const int32_t* req, const int64_t* pos,
+                         int64_t n, int64_t* vslot, int32_t* owner, int64_t* phys);
 
 /* ------------------------------------------------------------------------
  * Device slot map (SGLang DCP docs, Virtual KV layout: owner(v) = v mod c,
- * physical(v) = floor(v / c)).
+ * physical(v) = floor(v / c); with interleave I as stated above).
  * d_page_table: device int32 [n_requests, max_pages]; d_req, d_pos: device
  * arrays of n request indices / positions.  Writes d_vslot (int64), d_owner
  * (int32) and d_phys (int64), each of n entries; any output pointer may be
@@ -147,7 +157,7 @@ int dcpmla_map_positions(const int32_t* page_table, int32_t max_pages, int32_t c
  * DCPMLA_DERR_PAGE and writes owner = -1, vslot = phys = -1 for that entry.
  * ------------------------------------------------------------------------ */
 int dcpmla_slot_map(const int32_t* d_page_table, int32_t n_requests, int32_t max_pages,
-                    int64_t num_pages, int32_t c, int32_t P, const int32_t* d_req,
+                    int64_t num_pages, int32_t c, int32_t interleave, int32_t P, const int32_t* d_req,
                     const int64_t* d_pos, int64_t n, int64_t* d_vslot, int32_t* d_owner,
                     int64_t* d_phys, int32_t* d_err, void* stream);
 
@@ -180,8 +190,9 @@ int dcpmla_kv_append(void* const* pools, float* const* scale_pools, int32_t kv_d
  *
  * For every request b, query token t < Tq, head h and shard r in
  * [shard_begin, shard_begin + shard_count):
- *   shard-local token j of request b is global position p = j*c + r, stored in
- *   pool r at physical slot page_table[b][j / P]*P + j % P; it is visible to
+ *   shard-local token j of request b is global position p = j*c + r (with
+ *   interleave I: floor(j/I)*I*c + r*I + j mod I), stored in pool r at
+ *   physical slot page_table[b][j / P]*P + j % P; it is visible to
  *   query t iff p <= L_b - Tq + t (causality over global positions);
  *   s_j   = sm_scale * (q[b,t,h,:] . key_j)  over all 576 dims
  *           (E4M3: key_j = code_j * scale_j);
@@ -204,9 +215,10 @@ int dcpmla_kv_append(void* const* pools, float* const* scale_pools, int32_t kv_d
 int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools,
                   int32_t kv_dtype, int64_t pool_rows, const int32_t* d_page_table,
                   int32_t max_pages, const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H,
-                  int32_t P, int32_t c, int32_t shard_begin, int32_t shard_count, float sm_scale,
-                  int32_t lse_base, float* d_o_part, float* d_lse_part, void* d_workspace,
-                  size_t ws_bytes, int32_t* d_err, void* stream);
+                  int32_t P, int32_t c, int32_t interleave, int32_t shard_begin,
+                  int32_t shard_count, float sm_scale, int32_t lse_base, float* d_o_part,
+                  float* d_lse_part, void* d_workspace, size_t ws_bytes, int32_t* d_err,
+                  void* stream);
 
 /* Bytes of device workspace dcpmla_decode needs for the same B, Tq, H, P, c,
  * shard_count, kv_dtype and max_pages (every L_b is at most max_pages*P*c).
@@ -230,6 +242,87 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
                        int32_t kv_dtype, int32_t max_pages, int32_t* path, int32_t* kernel_launches);
 
 /* ------------------------------------------------------------------------
+ * Token relayout, DCP-1 prefill cache -> striped decode pools (SGLang DCP
+ * docs, DCP x PD disaggregation: dense prefill pages are not copied straight
+ * into striped storage; a DCP-1 prefill feeds DCP decode through a token
+ * relayout whose plan carries the exact token count, so a partial final page
+ * leaks no stale rows; page size and KV dtype match on both sides).
+ *
+ * For request b < B and each position p < d_seq_lens[b], the stored row at
+ * dense slot d_dense_page_table[b][p / P] * P + p % P of d_dense is copied
+ * byte for byte to pools[owner(p)] at physical(p), with owner and physical from
+ * d_page_table (virtual pages of P*c) and the interleave size (as in
+ * dcpmla_slot_map); for E4M3 the fp32 scale d_dense_scales[dense slot] goes to
+ * scale_pools[owner][physical].  Nothing else is written.
+ * d_dense: [dense_rows, 576] rows of kv_dtype (1152 B bf16, 576 B E4M3),
+ *   16-byte aligned; d_dense_page_table: int32 [B, dense_max_pages];
+ * pools / scale_pools: HOST arrays of c device pointers, as in
+ *   dcpmla_kv_append; d_page_table: int32 [B, max_pages]; d_seq_lens: int32 [B].
+ * Device errors: a length above dense_max_pages*P or max_pages*P*c sets
+ * DCPMLA_DERR_LENGTH and skips the request; a page id outside either pool sets
+ * DCPMLA_DERR_PAGE and skips that token.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+int dcpmla_relayout_dense_to_striped(const void* d_dense, const float* d_dense_scales, int64_t dense_rows,
+                                     const int32_t* d_dense_page_table, int32_t dense_max_pages,
+                                     void* const* pools, float* const* scale_pools, int32_t kv_dtype,
+                                     int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+                                     const int32_t* d_seq_lens, int32_t B, int32_t P, int32_t c,
+                                     int32_t interleave, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Un-stripe gather, striped pools -> one contiguous copy per request in token
+ * order (SGLang DCP docs, Communication backends: extend gathers the cached
+ * prefix shards and restores token order; vLLM GLM-5.3 serving post, DCP
+ * section: a temporary full-context copy of the shards).
+ *
+ * d_out[b][p] (rows of kv_dtype, [B, out_capacity, 576], 16-byte aligned) =
+ * pools[owner(p)][physical(p)] for p < d_seq_lens[b]; for E4M3 also
+ * d_out_scales[b][p] ([B, out_capacity] fp32).  Rows at p >= d_seq_lens[b] are
+ * not written.  Errors as for the relayout (a length above out_capacity or
+ * max_pages*P*c sets DCPMLA_DERR_LENGTH).
+ * ------------------------------------------------------------------------ */
+int dcpmla_gather_unstriped(void* const* pools, float* const* scale_pools, int32_t kv_dtype, int64_t pool_rows,
+                            const int32_t* d_page_table, int32_t max_pages, const int32_t* d_seq_lens, int32_t B,
+                            int32_t P, int32_t c, int32_t interleave, void* d_out, float* d_out_scales,
+                            int64_t out_capacity, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * E4M3 quantising append: like dcpmla_kv_append into E4M3 pools, but from bf16
+ * rows, computing each token's scale (the FP8 cache with one fp32 scale per
+ * token that the FP8 workload stores).  In float32: amax = max |x| over the 576
+ * values, scale = amax / 448 (IEEE division), code = E4M3FN(clamp(x / scale,
+ * -448, 448)) rounded to nearest-even (IEEE signed zero); a row of zeros gets
+ * scale 0 and zero codes.  Codes go to pools[owner][phys], the scale to
+ * scale_pools[owner][phys].
+ * d_ckv: bf16 [n, ckv_stride] (first 512 used), d_krope: bf16 [n, krope_stride]
+ * (first 64 used), both 16-byte aligned with strides in elements that keep
+ * rows 16-byte aligned; d_owner / d_phys as from dcpmla_slot_map.  An entry
+ * with owner outside [0, c) or phys outside [0, pool_rows) sets
+ * DCPMLA_DERR_SLOT and is skipped.
+ * ------------------------------------------------------------------------ */
+int dcpmla_kv_append_e4m3(void* const* pools, float* const* scale_pools, int64_t pool_rows, int32_t c,
+                          const int32_t* d_owner, const int64_t* d_phys, const void* d_ckv, int64_t ckv_stride,
+                          const void* d_krope, int64_t krope_stride, int64_t n, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
+ * HiCache index filter (SGLang DCP docs, DCP x HiCache L2: the controller
+ * addresses P*c slots per widened page while each buffer stores its P local
+ * rows; before a host<->device transfer both index lists keep the positions
+ * this rank owns and map i to floor(i / c)).
+ *
+ * d_idx: int64 [n] slots in widened-page space.  Writes, in input order, the
+ * local slot of every entry that `rank` owns (owner / physical with the
+ * interleave size, floor(i / c) for interleave 1) to d_out (int64, room for n)
+ * and their number to *d_count (device int64).  A negative index sets
+ * DCPMLA_DERR_POSITION and is dropped.  d_workspace: at least
+ * dcpmla_hicache_filter_workspace_size(n) bytes (ERR_CAPACITY otherwise).
+ * ------------------------------------------------------------------------ */
+int dcpmla_hicache_filter_workspace_size(int64_t n, size_t* out);
+int dcpmla_hicache_filter(const int64_t* d_idx, int64_t n, int32_t c, int32_t interleave, int32_t rank,
+                          int64_t* d_out, int64_t* d_count, void* d_workspace, size_t ws_bytes, int32_t* d_err,
+                          void* stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free decode.  The pages have no counterpart to this call: it is
  * a library convenience.
  *
@@ -238,7 +331,8 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
  * in its enqueue path, a process whose memory is already fully reserved by a
  * caching allocator, or a latency-critical loop in which cudaMalloc/cudaFree
  * would synchronise the device.  This call takes the same arguments as
- * dcpmla_decode minus the workspace and computes the same result with the
+ * dcpmla_decode minus the workspace and the interleave size (it serves the
+ * plain striping, interleave 1) and computes the same result with the
  * CUDA-core decode kernel; its split-KV scratch is a static device array of
  * DCPMLA_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until
  * the process exits.  It calls no cudaMalloc, cudaFree or other allocating

@@ -49,7 +49,8 @@ class OracleWorkload:
             p1 = min(L, p0 + chunk)
             rows, scales = W.kv_rows(self.w, b, p0, p1, gen_device)
             sc = None if scales is None else scales.cpu().numpy()
-            O.append_tokens(self.pools, self.rmap, b, np.arange(p0, p1), bits(rows), sc)
+            O.append_tokens(self.pools, self.rmap, b, np.arange(p0, p1), bits(rows), sc,
+                            I=self.w.interleave)
         self.loaded.add(b)
 
     def q(self, b: int, gen_device="cpu") -> np.ndarray:
@@ -59,7 +60,8 @@ class OracleWorkload:
         """(o_parts (c,R,512), lse_parts (c,R), o (R,512), lse (R,)) for request b."""
         self.load(b, gen_device)
         return O.decode_request_striped(self.q(b, gen_device), self.pools, self.rmap, b,
-                                        self.lens[b], self.w.sm_scale, self.w.lse_base)
+                                        self.lens[b], self.w.sm_scale, self.w.lse_base,
+                                        I=self.w.interleave)
 
     def decode_many(self, reqs: Iterable[int], gen_device="cpu") -> Dict[int, tuple]:
         return {b: self.decode(b, gen_device) for b in reqs}

@@ -75,8 +75,9 @@ def test_page_tables_bit_exact_against_oracle(name):
     B.dcpmla_alloc_destroy(h)
 
 
-@pytest.mark.parametrize("c,P", [(1, 16), (3, 5), (4, 16), (8, 64), (2, 16), (16, 1)])
-def test_host_position_map_bit_exact(c, P):
+@pytest.mark.parametrize("c,P,I", [(1, 16, 1), (3, 5, 1), (4, 16, 1), (8, 64, 1), (2, 16, 1), (16, 1, 1),
+                                   (2, 64, 16), (4, 16, 4), (8, 16, 2), (3, 8, 8)])
+def test_host_position_map_bit_exact(c, P, I):
     rng = np.random.default_rng(c * 100 + P)
     lens = rng.integers(1, 3000, size=5).tolist()
     pages = [-(-L // (P * c)) for L in lens]
@@ -91,10 +92,11 @@ def test_host_position_map_bit_exact(c, P):
     pt, _ = B.dcpmla_reqmap_page_table(m, list(range(len(lens))), max(pages))
     req = np.concatenate([np.full(L, b) for b, L in enumerate(lens)])
     pos = np.concatenate([np.arange(L) for L in lens])
-    v, own, phys = B.dcpmla_map_positions(pt, c, P, torch.from_numpy(req), torch.from_numpy(pos))
+    v, own, phys = B.dcpmla_map_positions(pt, c, P, torch.from_numpy(req), torch.from_numpy(pos),
+                                          interleave=I)
     for b in range(len(lens)):
         sel = req == b
-        wv, wo, wp = O.map_positions(rmap, b, pos[sel])
+        wv, wo, wp = O.map_positions(rmap, b, pos[sel], I)
         assert np.array_equal(v.numpy()[sel], wv)
         assert np.array_equal(own.numpy()[sel], wo)
         assert np.array_equal(phys.numpy()[sel], wp)
@@ -161,8 +163,10 @@ def test_device_calls_reject_bad_arguments_before_launch():
     assert lib.dcpmla_lse_merge(None, None, 0, 4, 0, None, None, None, None) == -1
     assert lib.dcpmla_lse_merge(None, None, 2, 4, 3, None, None, None, None) == -1
     assert lib.dcpmla_lse_merge(None, None, 2, 4, 0, None, None, None, None) == -1
-    assert lib.dcpmla_slot_map(None, 1, 4, 4, 0, 16, None, None, 5, None, None, None, None,
+    assert lib.dcpmla_slot_map(None, 1, 4, 4, 0, 1, 16, None, None, 5, None, None, None, None,
                                None) == -1
+    assert lib.dcpmla_slot_map(None, 1, 4, 4, 2, 3, 16, None, None, 5, None, None, None, None,
+                               None) == -1                    # interleave must divide P
     assert lib.dcpmla_kv_append(None, None, 5, 10, 2, None, None, None, 576, None, 576, None, 1,
                                 None, None) == -2
     # a zero-sized call is a no-op

@@ -61,6 +61,14 @@ SMALL = {
     "fh_p128": W.Workload("fhp", B=2, H=16, Tq=1, c=2, P=128, kv_dtype="bf16", lse_base="2",
                           seed=20, L=3001),
     "fh_chunked": W.scaled(W.WORKLOADS["long"], B=2, L=300000),
+    # interleave size I > 1 (tokens to shards in runs of I) on each decode kernel
+    "ilv16_long": W.scaled(W.WORKLOADS["long"], B=2, L=40000, interleave=16),
+    "ilv2_c3_tq2": W.Workload("il2", B=3, H=8, Tq=2, c=3, P=16, kv_dtype="bf16", lse_base="2",
+                              seed=22, L=777, interleave=2),
+    "ilv4_dsv3": W.scaled(W.WORKLOADS["dsv3"], B=2, L=3000, interleave=4),
+    "ilv8_fp8": W.scaled(W.WORKLOADS["fp8"], B=1, L=2000, interleave=8),
+    "ilv2_c16": W.Workload("il16", B=4, H=16, Tq=1, c=16, P=4, kv_dtype="bf16", lse_base="e",
+                           seed=23, lengths_mix=(2, 100, 300, 1, 40), interleave=2),
 }
 
 SENTINEL = 0xA5
