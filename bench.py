@@ -563,7 +563,8 @@ def run_op(args, w: W.Workload):
             return 2048 * (W.D_K * 2 + W.D_K + 4) / (time.perf_counter() - t0) / 1e9
     elif args.op == "hicache":
         n = 1 << 24
-        idx = torch.randint(0, 1 << 40, (n,), dtype=torch.int64, device=dev, generator=g)
+        # slots of the widened-page space of a 2^31-slot virtual capacity
+        idx = torch.randint(0, 1 << 31, (n,), dtype=torch.int64, device=dev, generator=g)
         out = torch.empty(n, dtype=torch.int64, device=dev)
         cnt = torch.zeros(1, dtype=torch.int64, device=dev)
         ws = torch.empty(max(16, B.dcpmla_hicache_filter_workspace_size(n)), dtype=torch.uint8, device=dev)

@@ -22,8 +22,6 @@ using namespace dcpmla;
 
 namespace {
 
-constexpr int kTokPerIter = 32;   // tokens a block copies per loop iteration
-
 // Where position p of request b lives in the striped pools (owner, physical slot),
 // or owner -1 when the page-table entry is outside the pools.
 struct Slot {
@@ -53,14 +51,22 @@ __device__ __forceinline__ int64_t dense_slot(const int32_t* dpt_row, int64_t p,
 }
 
 // dir = 0: dense -> striped (relayout); dir = 1: striped -> contiguous (gather).
-template <int kDir>
+// Each warp moves kWarpTok tokens per iteration: lanes 0..kWarpTok-1 look up one
+// token's source and destination rows, the addresses are broadcast with shuffles,
+// and every lane issues all of its 16-byte loads before any store.
+constexpr int kWarpTok = 4;
+
+template <int kDir, int kChunks>
 __global__ void __launch_bounds__(256) move_rows_kernel(
     const uint8_t* __restrict__ dense, const float* __restrict__ dense_scales, int64_t dense_rows,
     const int32_t* __restrict__ dense_pt, int32_t dense_max_pages, ShardPtrs pools, int64_t pool_rows,
     const int32_t* __restrict__ pt, int32_t max_pages, const int32_t* __restrict__ lens, int32_t P, int32_t c,
-    int32_t I, int32_t row_bytes, bool fp8, uint8_t* __restrict__ out, float* __restrict__ out_scales,
-    int64_t out_cap, int32_t* err) {
+    int32_t I, bool fp8, uint8_t* __restrict__ out, float* __restrict__ out_scales, int64_t out_cap,
+    int32_t* err) {
+  constexpr int kRowBytes = kChunks * 16;
+  constexpr int kPer = (kWarpTok * kChunks + 31) / 32;   // chunks per lane per iteration
   const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31;
   const int64_t L = __ldg(lens + b);
   const int64_t limit = kDir == 0 ? min((int64_t)dense_max_pages * P, (int64_t)max_pages * P * c)
                                   : min(out_cap, (int64_t)max_pages * P * c);
@@ -68,36 +74,58 @@ __global__ void __launch_bounds__(256) move_rows_kernel(
     if (threadIdx.x == 0 && blockIdx.x == 0) set_err(err, DCPMLA_DERR_LENGTH);
     return;
   }
-  const int chunks = row_bytes / 16;
   const int32_t* vpt_row = pt + (int64_t)b * max_pages;
   const int32_t* dpt_row = kDir == 0 ? dense_pt + (int64_t)b * dense_max_pages : nullptr;
   const int64_t num_pages = pool_rows / P, dense_pages = dense_rows / P;
-  for (int64_t t0 = (int64_t)blockIdx.x * kTokPerIter; t0 < L; t0 += (int64_t)gridDim.x * kTokPerIter) {
-    for (int e = threadIdx.x; e < kTokPerIter * chunks; e += blockDim.x) {
-      const int64_t p = t0 + e / chunks;
-      const int ch = e % chunks;
-      if (p >= L) continue;
-      const Slot s = striped_slot(vpt_row, p, c, I, P, num_pages);
-      if (s.owner < 0) {
-        if (ch == 0) set_err(err, DCPMLA_DERR_PAGE);
-        continue;
-      }
-      uint8_t* pool = static_cast<uint8_t*>(pools.pool[s.owner]);
-      if (kDir == 0) {
-        const int64_t d = dense_slot(dpt_row, p, P, dense_pages);
-        if (d < 0) {
-          if (ch == 0) set_err(err, DCPMLA_DERR_PAGE);
-          continue;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kWarpTok; t0 < L;
+       t0 += warps * kWarpTok) {
+    // lane k < kWarpTok resolves token t0 + k: source and destination row pointers
+    const uint8_t* src = nullptr;
+    uint8_t* dst = nullptr;
+    const float* ssrc = nullptr;
+    float* sdst = nullptr;
+    if (lane < kWarpTok && t0 + lane < L) {
+      const int64_t p = t0 + lane;
+      const Slot sl = striped_slot(vpt_row, p, c, I, P, num_pages);
+      int64_t d = 0;
+      if (kDir == 0) d = dense_slot(dpt_row, p, P, dense_pages);
+      if (sl.owner < 0 || d < 0) {
+        set_err(err, DCPMLA_DERR_PAGE);
+      } else if (kDir == 0) {
+        src = dense + d * kRowBytes;
+        dst = static_cast<uint8_t*>(pools.pool[sl.owner]) + sl.phys * kRowBytes;
+        if (fp8) {
+          ssrc = dense_scales + d;
+          sdst = pools.scale[sl.owner] + sl.phys;
         }
-        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(dense + d * row_bytes) + ch);
-        reinterpret_cast<uint4*>(pool + s.phys * row_bytes)[ch] = v;
-        if (fp8 && ch == 0) pools.scale[s.owner][s.phys] = __ldcs(dense_scales + d);
       } else {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(pool + s.phys * row_bytes) + ch);
-        reinterpret_cast<uint4*>(out + ((int64_t)b * out_cap + p) * row_bytes)[ch] = v;
-        if (fp8 && ch == 0) out_scales[(int64_t)b * out_cap + p] = __ldcs(pools.scale[s.owner] + s.phys);
+        src = static_cast<const uint8_t*>(pools.pool[sl.owner]) + sl.phys * kRowBytes;
+        dst = out + ((int64_t)b * out_cap + p) * kRowBytes;
+        if (fp8) {
+          ssrc = pools.scale[sl.owner] + sl.phys;
+          sdst = out_scales + (int64_t)b * out_cap + p;
+        }
       }
     }
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = k * 32 + lane;                      // (token, chunk) pair of this lane
+      const int tk = e / kChunks, ch = e % kChunks;
+      const uint8_t* s = reinterpret_cast<const uint8_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), tk < kWarpTok ? tk : 0));
+      v[k] = (e < kWarpTok * kChunks && s) ? __ldcs(reinterpret_cast<const uint4*>(s) + ch) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int e = k * 32 + lane;
+      const int tk = e / kChunks, ch = e % kChunks;
+      uint8_t* d = reinterpret_cast<uint8_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), tk < kWarpTok ? tk : 0));
+      if (e < kWarpTok * kChunks && d) reinterpret_cast<uint4*>(d)[ch] = v[k];
+    }
+    if (fp8 && lane < kWarpTok && ssrc) *sdst = __ldcs(ssrc);
   }
 }
 
@@ -205,8 +233,24 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kFilterBlock = 1024;   // indices per block (256 threads x 4)
 
+// owner and local slot of widened-page slot i (i >= 0); 32-bit division when i fits
+__device__ __forceinline__ void owner_local(int64_t i, int32_t c, int32_t I, int32_t& own, int64_t& loc) {
+  if ((uint64_t)i <= 0xFFFFFFFFull) {
+    const uint32_t u = (uint32_t)i, q = I == 1 ? u : u / (uint32_t)I, w = q / (uint32_t)c;
+    own = (int32_t)(q - w * (uint32_t)c);
+    loc = (int64_t)w * I + (u - q * (uint32_t)I);
+  } else {
+    const int64_t q = i / I, w = q / c;
+    own = (int32_t)(q - w * c);
+    loc = w * I + (i - q * I);
+  }
+}
 __device__ __forceinline__ bool owned(int64_t i, int32_t c, int32_t I, int32_t rank) {
-  return i >= 0 && (int32_t)((i / I) % c) == rank;
+  if (i < 0) return false;
+  int32_t o;
+  int64_t l;
+  owner_local(i, c, I, o, l);
+  return o == rank;
 }
 
 __global__ void __launch_bounds__(256) filter_count_kernel(const int64_t* __restrict__ idx, int64_t n, int32_t c,
@@ -285,8 +329,10 @@ __global__ void __launch_bounds__(256) filter_scatter_kernel(const int64_t* __re
   for (int k = 0; k < 4; ++k) {
     const uint32_t bal = __ballot_sync(0xffffffffu, keep[k]);
     if (keep[k]) {
-      const int64_t x = v[k];
-      out[pos + __popc(bal & ((1u << lane) - 1u))] = (x / ((int64_t)I * c)) * I + x % I;
+      int32_t o;
+      int64_t l;
+      owner_local(v[k], c, I, o, l);
+      out[pos + __popc(bal & ((1u << lane) - 1u))] = l;
     }
     pos += __popc(bal);
   }
@@ -305,10 +351,13 @@ int check_pools(void* const* pools, float* const* scale_pools, int32_t c, bool f
   return DCPMLA_OK;
 }
 
-int move_grid_x(int32_t max_pages, int32_t P, int32_t c) {
+// Blocks per request: enough warps for the longest request, at most one wave of
+// 8-warp blocks over the SMs for all requests together.
+int move_grid_x(int32_t max_pages, int32_t P, int32_t c, int32_t B) {
   const int64_t tokens = (int64_t)max_pages * P * c;
-  const int64_t blocks = (tokens + kTokPerIter - 1) / kTokPerIter;
-  return (int)std::min<int64_t>(std::max<int64_t>(blocks, 1), 128);
+  const int64_t blocks = (tokens + 8 * kWarpTok - 1) / (8 * kWarpTok);
+  const int64_t wave = std::max<int64_t>(1, (int64_t)device_sm_count() * 8 / std::max(B, 1));
+  return (int)std::min<int64_t>(std::max<int64_t>(blocks, 1), std::max<int64_t>(wave, 1));
 }
 
 }  // namespace
@@ -334,11 +383,15 @@ int dcpmla_relayout_dense_to_striped(const void* d_dense, const float* d_dense_s
   const int rc = check_pools(pools, scale_pools, c, fp8, sp);
   if (rc != DCPMLA_OK) return rc;
   if (B > 65535) return DCPMLA_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)move_grid_x(max_pages, P, c), (unsigned)B);
-  move_rows_kernel<0><<<grid, 256, 0, (cudaStream_t)stream>>>(
-      static_cast<const uint8_t*>(d_dense), d_dense_scales, dense_rows, d_dense_page_table, dense_max_pages, sp,
-      pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave, fp8 ? kDK : 2 * kDK, fp8, nullptr,
-      nullptr, 0, d_err);
+  const dim3 grid((unsigned)move_grid_x(max_pages, P, c, B), (unsigned)B);
+  if (fp8)
+    move_rows_kernel<0, kDK / 16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(d_dense), d_dense_scales, dense_rows, d_dense_page_table, dense_max_pages, sp,
+        pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave, true, nullptr, nullptr, 0, d_err);
+  else
+    move_rows_kernel<0, 2 * kDK / 16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(d_dense), nullptr, dense_rows, d_dense_page_table, dense_max_pages, sp,
+        pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave, false, nullptr, nullptr, 0, d_err);
   return launch_status();
 }
 
@@ -358,10 +411,15 @@ int dcpmla_gather_unstriped(void* const* pools, float* const* scale_pools, int32
   const int rc = check_pools(pools, scale_pools, c, fp8, sp);
   if (rc != DCPMLA_OK) return rc;
   if (B > 65535) return DCPMLA_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)move_grid_x(max_pages, P, c), (unsigned)B);
-  move_rows_kernel<1><<<grid, 256, 0, (cudaStream_t)stream>>>(
-      nullptr, nullptr, 0, nullptr, 1, sp, pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave,
-      fp8 ? kDK : 2 * kDK, fp8, static_cast<uint8_t*>(d_out), d_out_scales, out_capacity, d_err);
+  const dim3 grid((unsigned)move_grid_x(max_pages, P, c, B), (unsigned)B);
+  if (fp8)
+    move_rows_kernel<1, kDK / 16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        nullptr, nullptr, 0, nullptr, 1, sp, pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave,
+        true, static_cast<uint8_t*>(d_out), d_out_scales, out_capacity, d_err);
+  else
+    move_rows_kernel<1, 2 * kDK / 16><<<grid, 256, 0, (cudaStream_t)stream>>>(
+        nullptr, nullptr, 0, nullptr, 1, sp, pool_rows, d_page_table, max_pages, d_seq_lens, P, c, interleave,
+        false, static_cast<uint8_t*>(d_out), nullptr, out_capacity, d_err);
   return launch_status();
 }
 
