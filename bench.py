@@ -307,7 +307,7 @@ def run_ours(args, w: W.Workload):
     build()
     import dcp_harness as Hn
 
-    dw = Hn.build(w)
+    dw = Hn.build(w, fused=args.fused)
     step = dw.step
     lens = dw.lens
     acc = accounting(w, lens, step.page_table.shape[1])
@@ -420,14 +420,18 @@ def run_ours(args, w: W.Workload):
                          f"{w.name} workload, {t:.1f} s of CPU work"}
 
     # slot map + append (when the step appends), the decode's kernels, the merge
-    launches_per_step = (2 if step.do_append else 0) + dec_launches + 1
+    # (fused: the decode's own merge kernel replaces the split merge and the LSE merge)
+    launches_per_step = (2 if step.do_append else 0) + (dec_launches if not args.fused else
+                                                         (2 if path == 1 else 1 if path == 2 else 2))
+    if not args.fused:
+        launches_per_step += 1
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
-            "config": config_obj(w),
+            "config": dict(config_obj(w), step="decode + merge fused" if args.fused else "decode, then merge"),
             "attended_tokens_per_s": round(sum(lens) * w.Tq * ws / (ms_step * 1e-3), 1),
             "decode_tokens_per_s": round(w.B * w.Tq * ws / (ms_step * 1e-3), 1),
             "step_hbm_frac": round(acc["step_bytes"] / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -619,6 +623,8 @@ def main():
     ap.add_argument("--op", default="step", choices=["step", "relayout", "gather", "append_e4m3", "hicache"],
                     help="what to time: the decode step (default) or one of the layout calls")
     ap.add_argument("--interleave", type=int, default=0, help="override the interleave size")
+    ap.add_argument("--fused", action="store_true",
+                    help="decode and merge in one call (dcpmla_decode_merged) instead of decode + merge")
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload with this many requests (small profiling captures)")
     args = ap.parse_args()

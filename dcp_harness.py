@@ -36,7 +36,7 @@ class DeviceWorkload:
 
 
 def build(w: W.Workload, device="cuda", chunk_tokens: int = 1 << 18,
-          fill_byte: Optional[int] = None, append: bool = True) -> DeviceWorkload:
+          fill_byte: Optional[int] = None, append: bool = True, fused: bool = False) -> DeviceWorkload:
     lens = w.seq_lens()
     pages = w.pages_per_request()
     num_pages = sum(pages)
@@ -46,7 +46,7 @@ def build(w: W.Workload, device="cuda", chunk_tokens: int = 1 << 18,
                            fill_byte=fill_byte, interleave=w.interleave)
     for b, L in enumerate(lens):
         cache.extend(b, L)
-    step = DecodeStep(cache, range(w.B), w.Tq, w.H, w.sm_scale, base_code(w), append=append)
+    step = DecodeStep(cache, range(w.B), w.Tq, w.H, w.sm_scale, base_code(w), append=append, fused=fused)
 
     # Earlier tokens (positions 0 .. L-Tq-1) go in through the same append path.
     n_pre = 0

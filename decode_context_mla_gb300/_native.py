@@ -43,6 +43,9 @@ SIGNATURES = {
                                         i32, i32, i32, f32, i32, vp, vp, vp, vp]),
     "dcpmla_decode_workspace_size": (C.c_int, [i32, i32, i32, i32, i32, i32, i32, i32, P_sz]),
     "dcpmla_decode_path": (C.c_int, [i32, i32, i32, i32, i32, i32, i32, i32, P_i32, P_i32]),
+    "dcpmla_decode_merged_workspace_size": (C.c_int, [i32, i32, i32, i32, i32, i32, i32, P_sz]),
+    "dcpmla_decode_merged": (C.c_int, [vp, vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, i32, i32,
+                                       f32, i32, vp, vp, vp, sz, vp, vp]),
     "dcpmla_lse_merge": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp, vp]),
     "dcpmla_relayout_dense_to_striped": (C.c_int, [vp, vp, i64, vp, i32, vp, vp, i32, i64, vp, i32,
                                                    vp, i32, i32, i32, i32, vp, vp]),

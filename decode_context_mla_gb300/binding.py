@@ -350,3 +350,35 @@ def dcpmla_hicache_filter(idx: torch.Tensor, c: int, rank: int, out: torch.Tenso
         _dev(idx, "idx", torch.int64), n, c, interleave, rank, _dev(out, "out", torch.int64),
         _dev(count, "count", torch.int64), ws, ws_bytes, _dev(err, "err", torch.int32, True),
         _stream(stream)), "dcpmla_hicache_filter")
+
+
+# ---------------------------------------------------------------------------
+# Fused decode + merge
+# ---------------------------------------------------------------------------
+def dcpmla_decode_merged_workspace_size(B: int, Tq: int, H: int, P: int, c: int, kv_dtype: int,
+                                        max_pages: int) -> int:
+    out = C.c_size_t()
+    _check(lib().dcpmla_decode_merged_workspace_size(B, Tq, H, P, c, kv_dtype, max_pages, C.byref(out)),
+           "dcpmla_decode_merged_workspace_size")
+    return out.value
+
+
+def dcpmla_decode_merged(q: torch.Tensor, pools: Sequence[torch.Tensor],
+                         scale_pools: Optional[Sequence[torch.Tensor]], kv_dtype: int,
+                         page_table: torch.Tensor, seq_lens: torch.Tensor, P: int, c: int, sm_scale: float,
+                         lse_base: int, o: torch.Tensor, lse: torch.Tensor, workspace: Optional[torch.Tensor],
+                         err: Optional[torch.Tensor], stream=None, interleave: int = 1) -> None:
+    """All c shards decoded and merged: o fp32 [B, Tq, H, 512], lse fp32 [B, Tq, H]."""
+    B_, Tq, H, _ = q.shape
+    if len(pools) != c:
+        raise ValueError("need one pool per shard")
+    parr = _ptr_array(pools, "pools")
+    sarr = None if scale_pools is None else _ptr_array(scale_pools, "scale_pools", torch.float32)
+    ws = None if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().dcpmla_decode_merged(
+        _dev(q, "q", torch.bfloat16), parr, sarr, kv_dtype, pools[0].shape[0],
+        _dev(page_table, "page_table", torch.int32), page_table.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), B_, Tq, H, P, c, interleave, float(sm_scale), lse_base,
+        _dev(o, "o", torch.float32), _dev(lse, "lse", torch.float32), ws, ws_bytes,
+        _dev(err, "err", torch.int32, True), _stream(stream)), "dcpmla_decode_merged")

@@ -33,15 +33,19 @@ int device_sm_count();
 // Tokens go to shards in runs of `I` consecutive positions, round-robin (vLLM DCP
 // study page, configuration example: the KV interleave size; I = 1 is the SGLang
 // layout owner = v mod c).  Global position of shard r's local token j:
-__host__ __device__ __forceinline__ int64_t shard_pos(int64_t j, int32_t r, int32_t c, int32_t I) {
-  return (j / I) * I * c + (int64_t)r * I + j % I;
+// (j is a shard-local index, < 2^31; I = 1, the common layout, needs no division)
+__host__ __device__ __forceinline__ int64_t shard_pos(int32_t j, int32_t r, int32_t c, int32_t I) {
+  if (I == 1) return (int64_t)j * c + r;
+  const int32_t q = j / I;
+  return (int64_t)q * I * c + (int64_t)r * I + (j - q * I);
 }
-// Number of the first L positions that shard r holds.
-__host__ __device__ __forceinline__ int32_t shard_len(int64_t L, int32_t r, int32_t c, int32_t I) {
-  const int64_t round = (int64_t)I * c, full = L / round;
-  int64_t extra = L - full * round - (int64_t)r * I;
+// Number of the first L positions that shard r holds (L < 2^31; 32-bit arithmetic,
+// which also keeps a 64-bit division helper out of the decode kernels).
+__host__ __device__ __forceinline__ int32_t shard_len(int32_t L, int32_t r, int32_t c, int32_t I) {
+  const int32_t round = I * c, full = L / round;
+  int32_t extra = L - full * round - r * I;
   extra = extra < 0 ? 0 : (extra > I ? I : extra);
-  return (int32_t)(full * I + extra);
+  return full * I + extra;
 }
 
 __device__ __forceinline__ void set_err(int32_t* err, int bits) {

@@ -124,6 +124,66 @@ int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools
   return launch_decode_fma(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
 }
 
+// Fused decode + merge of all c shards.  The tensor-core kernels merge in-kernel
+// (token-major: a merge kernel over every unit of the request; 128-row tiles: the
+// last CTA of a request's row tile); the CUDA-core path decodes into the
+// workspace and merges with the LSE-merge kernel.
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t merged_ws(const DecodeArgs& a, int sm, size_t* part_off) {
+  if (fh_supported(a, sm)) return fh_workspace_bytes(a, sm);
+  if (tc_supported(a)) return tc_workspace_bytes(a, sm, true);
+  const size_t f = align256(fma_workspace_bytes(a, sm));
+  if (part_off) *part_off = f;
+  const size_t rows = (size_t)a.shard_count * a.B * a.R;
+  return f + align256(rows * kDL * 4) + rows * 4;
+}
+}  // namespace
+
+int dcpmla_decode_merged_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+                                        int32_t kv_dtype, int32_t max_pages, size_t* out) {
+  if (!out) return DCPMLA_ERR_INVALID;
+  DecodeArgs a;
+  const int st = fill_args(a, nullptr, nullptr, nullptr, kv_dtype, 0, nullptr, max_pages, nullptr, B, Tq, H, P,
+                           c, 1, 0, c, 1.f, DCPMLA_LSE_E, nullptr, nullptr, nullptr, false);
+  if (st != DCPMLA_OK) return st;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  *out = merged_ws(a, sm, nullptr);
+  return DCPMLA_OK;
+}
+
+int dcpmla_decode_merged(const void* d_q, void* const* pools, float* const* scale_pools, int32_t kv_dtype,
+                         int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+                         const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+                         int32_t interleave, float sm_scale, int32_t lse_base, float* d_o, float* d_lse,
+                         void* d_workspace, size_t ws_bytes, int32_t* d_err, void* stream) {
+  DecodeArgs a;
+  int st = fill_args(a, d_q, pools, scale_pools, kv_dtype, pool_rows, d_page_table, max_pages, d_seq_lens, B,
+                     Tq, H, P, c, interleave, 0, c, sm_scale, lse_base, d_o, d_lse, d_err, true);
+  if (st != DCPMLA_OK) return st;
+  if (B == 0) return DCPMLA_OK;
+  const int sm = device_sm_count();
+  if (sm <= 0) return DCPMLA_ERR_CUDA;
+  size_t part_off = 0;
+  const size_t need = merged_ws(a, sm, &part_off);
+  if (ws_bytes < need || (need && !d_workspace)) return DCPMLA_ERR_CAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (fh_supported(a, sm)) return launch_decode_fh(a, d_workspace, ws_bytes, sm, s, true);
+  if (tc_supported(a)) return launch_decode_tc(a, d_workspace, ws_bytes, sm, s, true);
+  uint8_t* w = static_cast<uint8_t*>(d_workspace);
+  const size_t rows = (size_t)c * B * a.R;
+  float* o_part = reinterpret_cast<float*>(w + part_off);
+  float* lse_part = reinterpret_cast<float*>(w + part_off + align256(rows * kDL * 4));
+  DecodeArgs ap = a;
+  ap.o_part = o_part;
+  ap.lse_part = lse_part;
+  st = launch_decode_fma(ap, d_workspace, part_off, sm, s);
+  if (st != DCPMLA_OK) return st;
+  return dcpmla_lse_merge(o_part, lse_part, c, (int64_t)B * a.R, lse_base, d_o, d_lse, d_err, stream);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -32,12 +32,17 @@ int tma_encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t
 // Tensor-core path for few query rows (<= 16): KV tokens are the MMA's M dimension.
 bool fh_supported(const DecodeArgs& a, int sm_count);
 size_t fh_workspace_bytes(const DecodeArgs& a, int sm_count);
-int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st);
+// fused: write every unit to the workspace and merge all shards into o = a.o_part
+// [B, R, 512], lse = a.lse_part [B, R] (shard_count must be c).
+int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
+                     bool fused = false);
 
 // Tensor-core path (tcgen05 / TMEM / TMA): 128-row query tiles, bf16 or e4m3 KV.
 bool tc_supported(const DecodeArgs& a);
-size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count);
-int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st);
+size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused = false);
+// fused: as for launch_decode_fh (every shard and split merged into o, lse).
+int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
+                     bool fused = false);
 
 // Generic CUDA-core path (any head count, bf16 or e4m3).
 size_t fma_workspace_bytes(const DecodeArgs& a, int sm_count);

@@ -86,6 +86,7 @@ struct FhParams {
   float* ws_lse;                     // [max_units, R] (base 2)
   int32_t* ws_bad;                   // [max_units]: the unit needed a page outside the pools
   int32_t* ws_pre;                   // [B * shard_count + 1]: first unit of each (request, shard)
+  int32_t fused;                     // 1: every unit to the workspace, merged over shards into o, lse
 };
 
 template <bool kCluster>
@@ -678,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ltot[n] = ((lsum_s[up][g][0][n] + lsum_s[up][g][1][n]) + lsum_s[up][g][2][n]) + lsum_s[up][g][3][n];
         inv[n] = ltot[n] > 0.f ? 1.f / ltot[n] : 0.f;
       }
-      const bool direct = x.nch == 1;
+      const bool direct = !p.fused && x.nch == 1;
       const bool empty_out = direct && unit_bad;
       const int64_t orow0 = direct ? ((int64_t)x.sr * a.B + x.b) * R : (int64_t)u * R;
       float* obase = direct ? a.o_part : p.ws_o;
@@ -790,6 +791,78 @@ __global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, con
   if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
 }
 
+// Fused decode + merge: one block per (request, query row) merges the partials of
+// every unit of every shard of the request (SGLang DCP docs, MLA decode dataflow:
+// the exact LSE merge; the split partials of one shard merge the same way), in
+// base 2, into o [B, R, 512] and lse [B, R] (base converted at the end).  A shard
+// any unit of which needed a bad page is left out, as the unfused path writes it
+// as empty (lse = -inf).
+__global__ void __launch_bounds__(32) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
+                                                          const float* __restrict__ ws_o,
+                                                          const float* __restrict__ ws_lse,
+                                                          const int32_t* __restrict__ ws_bad) {
+  // block (b, row, quarter): 32 threads x 4 dims = a quarter of the 512 value dims
+  const int b = blockIdx.x, row = blockIdx.y, t = blockIdx.z * 32 + threadIdx.x;
+  const int64_t R = a.R;
+  float m = -INFINITY;
+  for (int sr = 0; sr < a.shard_count; ++sr) {
+    const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
+    bool bad = false;
+    for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
+    if (bad) continue;
+    for (int k = 0; k < nch; ++k) m = fmaxf(m, ws_lse[(int64_t)(first + k) * R + row]);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse2 = -INFINITY;
+  if (m != -INFINITY) {
+    float sum = 0.f;
+    for (int sr = 0; sr < a.shard_count; ++sr) {
+      const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
+      bool bad = false;
+      for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
+      if (bad) continue;
+      for (int k = 0; k < nch; ++k) sum += exp2f(ws_lse[(int64_t)(first + k) * R + row] - m);
+    }
+    lse2 = m + log2f(sum);
+    for (int sr = 0; sr < a.shard_count; ++sr) {
+      const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
+      bool bad = false;
+      for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
+      if (bad) continue;
+      const float4* src = reinterpret_cast<const float4*>(ws_o + ((int64_t)first * R + row) * kDL) + t;
+      const int64_t step = R * (kDL / 4);
+      int k = 0;
+      for (; k + 4 <= nch; k += 4) {       // four partials' loads in flight
+        float w[4];
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          w[j] = exp2f(ws_lse[(int64_t)(first + k + j) * R + row] - lse2);
+          v[j] = __ldcs(src + (k + j) * step);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc.x = fmaf(w[j], v[j].x, acc.x);
+          acc.y = fmaf(w[j], v[j].y, acc.y);
+          acc.z = fmaf(w[j], v[j].z, acc.z);
+          acc.w = fmaf(w[j], v[j].w, acc.w);
+        }
+      }
+      for (; k < nch; ++k) {
+        const float w = exp2f(ws_lse[(int64_t)(first + k) * R + row] - lse2);
+        const float4 v = __ldcs(src + k * step);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+  }
+  const int64_t orow = (int64_t)b * R + row;
+  reinterpret_cast<float4*>(a.o_part + orow * kDL)[t] = acc;
+  if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
+}
+
 struct FhPlan {
   int32_t clusters, max_units;
   size_t pre_off, bad_off, lse_off, o_off, bytes;
@@ -825,7 +898,7 @@ bool fh_supported(const DecodeArgs& a, int sm_count) {
 
 size_t fh_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_fh(a, sm_count).bytes; }
 
-int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
+int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st, bool fused) {
   const FhPlan plan = plan_fh(a, sm_count);
   if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
   FhParams* fp = new (std::nothrow) FhParams();
@@ -834,6 +907,7 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   p.a = a;
   p.box_rows = std::min(a.P, kTok);
   p.max_units = plan.max_units;
+  p.fused = fused ? 1 : 0;
   int rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
     rc = tma_encode_bf16_2d(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)kDK, (uint64_t)a.pool_rows, 64,
@@ -851,7 +925,11 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     decode_fh_bf16_kernel<<<2 * plan.clusters, kThreads, kSmemBytes, st>>>(p);
     rc = launch_status();
   }
-  if (rc == DCPMLA_OK) {
+  if (rc == DCPMLA_OK && fused) {
+    const dim3 grid((unsigned)a.B, (unsigned)a.R, 4);
+    fh_merge_all_kernel<<<grid, 32, 0, st>>>(a, p.ws_pre, p.ws_o, p.ws_lse, p.ws_bad);
+    rc = launch_status();
+  } else if (rc == DCPMLA_OK) {
     const dim3 grid((unsigned)(a.B * a.shard_count), (unsigned)a.R);
     fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, p.ws_o, p.ws_lse, p.ws_bad);
     rc = launch_status();

@@ -86,6 +86,7 @@ struct TcParams {
   float* ws_o;
   float* ws_lse;
   uint32_t* ws_cnt;
+  int32_t fused;                      // 1: merge all shards and splits of a row tile into o, lse
 };
 
 template <bool kCluster>
@@ -579,9 +580,11 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     ok = ok && l_ok;
     const float l_tot = l_s[0][row] + l_s[1][row];
     tc_fence_after();
-    const bool direct = p.num_splits == 1;
-    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL
-                         : p.ws_o + (((int64_t)split * a.B * a.shard_count + bz) * R + grow) * kDL) +
+    const bool direct = !p.fused && p.num_splits == 1;
+    // workspace slot of this (shard, split): split-major unfused, shard-major fused
+    const int64_t wrow = p.fused ? ((int64_t)(sr * p.num_splits + split) * a.B + b) * R + grow
+                                 : ((int64_t)split * a.B * a.shard_count + bz) * R + grow;
+    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL : p.ws_o + wrow * kDL) +
                  h * 256 + g * 128;
     const bool read_o = ok && ntiles > 0;                   // uniform across the warp
     const bool live = read_o && l_tot > 0.f;
@@ -605,7 +608,7 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
       if (direct)
         a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
       else
-        p.ws_lse[((int64_t)split * a.B * a.shard_count + bz) * R + grow] = lse2;
+        p.ws_lse[wrow] = lse2;
     }
   }
 
@@ -619,42 +622,98 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   cluster_arrive();
   cluster_wait();
   if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
-  if (p.num_splits == 1) return;
+  if (p.num_splits == 1 && !p.fused) return;
 
-  // ---- split combine: the last of the 2 * num_splits CTAs of (b, r, row tile) merges ----
+  // ---- combine: the last CTA of a group merges the group's partials (exact LSE merge,
+  // base 2).  Unfused: the 2 * num_splits CTAs of (b, r, row tile), into o_part.
+  // Fused: the 2 * shard_count * num_splits CTAs of (b, row tile), every shard and
+  // split of the request, straight into o = o_part [B, R, 512] and lse = lse_part.
   __threadfence();
   __syncthreads();
+  const int nparts = p.fused ? a.shard_count * p.num_splits : p.num_splits;
   if (tid == 0) {
-    const uint32_t prev = atomicAdd(p.ws_cnt + (int64_t)bz * p.row_tiles + rt, 1u);
-    last_s = prev == (uint32_t)(2 * p.num_splits - 1);
+    const int64_t ci = p.fused ? (int64_t)b * p.row_tiles + rt : (int64_t)bz * p.row_tiles + rt;
+    const uint32_t prev = atomicAdd(p.ws_cnt + ci, 1u);
+    last_s = prev == (uint32_t)(2 * nparts - 1);
   }
   __syncthreads();
   if (!last_s) return;
   __threadfence();
-  const int64_t sstride = (int64_t)a.B * a.shard_count * R;
+  // partial k of this group's row: k * kstride + base.  The stage buffers are idle
+  // now (MMAs drained, peer past the cluster barrier): each row's merge weights go
+  // there once, then the partial rows stream through in float4s.
+  const int64_t kstride = p.fused ? (int64_t)a.B * R : (int64_t)a.B * a.shard_count * R;
   const int rows_here = (int)min((long long)kRows, (long long)(R - (int64_t)rt * kRows));
+  const int64_t base0 = (p.fused ? (int64_t)b * R : (int64_t)bz * R) + (int64_t)rt * kRows;
+  float* wts = reinterpret_cast<float*>(sKV);            // [nparts][kRows]
+  float* lse_s = wts + (size_t)nparts * kRows;           // [kRows]
+  const bool fits = (size_t)(nparts + 1) * kRows * 4 <= (size_t)kStages * kStageBytes;
+  if (fits) {
+    for (int rr = tid; rr < rows_here; rr += kThreads) {
+      float m = -INFINITY;
+      for (int k = 0; k < nparts; ++k) m = fmaxf(m, __ldcg(p.ws_lse + k * kstride + base0 + rr));
+      float lse2 = -INFINITY;
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int k = 0; k < nparts; ++k) sum += exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - m);
+        lse2 = m + log2f(sum);
+      }
+      for (int k = 0; k < nparts; ++k)
+        wts[k * kRows + rr] =
+            lse2 == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - lse2);
+      lse_s[rr] = lse2;
+    }
+    __syncthreads();
+  }
   for (int e = tid; e < rows_here * (kDL / 4); e += kThreads) {
     const int rrow = e / (kDL / 4), d4 = e % (kDL / 4);
-    const int64_t base = (int64_t)bz * R + (int64_t)rt * kRows + rrow;
-    float m = -INFINITY;
-    for (int s = 0; s < p.num_splits; ++s) m = fmaxf(m, __ldcg(p.ws_lse + s * sstride + base));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t base = base0 + rrow;
     float lse2 = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int s = 0; s < p.num_splits; ++s) sum += exp2f(__ldcg(p.ws_lse + s * sstride + base) - m);
-      lse2 = m + log2f(sum);
-      for (int s = 0; s < p.num_splits; ++s) {
-        const float w = exp2f(__ldcg(p.ws_lse + s * sstride + base) - lse2);
-        if (w == 0.f) continue;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * sstride + base) * kDL) + d4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (fits) {
+      lse2 = lse_s[rrow];
+      const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * kDL) + d4;
+      const int64_t step = kstride * (kDL / 4);
+      int k = 0;
+      for (; k + 4 <= nparts; k += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + (k + j) * step);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float w = wts[(k + j) * kRows + rrow];
+          acc.x = fmaf(w, v[j].x, acc.x);
+          acc.y = fmaf(w, v[j].y, acc.y);
+          acc.z = fmaf(w, v[j].z, acc.z);
+          acc.w = fmaf(w, v[j].w, acc.w);
+        }
+      }
+      for (; k < nparts; ++k) {
+        const float4 v = __ldcg(src + k * step);
+        const float w = wts[k * kRows + rrow];
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
         acc.w = fmaf(w, v.w, acc.w);
       }
+    } else {
+      float m = -INFINITY;
+      for (int s = 0; s < nparts; ++s) m = fmaxf(m, __ldcg(p.ws_lse + s * kstride + base));
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int s = 0; s < nparts; ++s) sum += exp2f(__ldcg(p.ws_lse + s * kstride + base) - m);
+        lse2 = m + log2f(sum);
+        for (int s = 0; s < nparts; ++s) {
+          const float w = exp2f(__ldcg(p.ws_lse + s * kstride + base) - lse2);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * kstride + base) * kDL) + d4);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
     }
-    const int64_t orow = ((int64_t)sr * a.B + b) * R + (int64_t)rt * kRows + rrow;
+    const int64_t orow = p.fused ? base : ((int64_t)sr * a.B + b) * R + (int64_t)rt * kRows + rrow;
     reinterpret_cast<float4*>(a.o_part + orow * kDL)[d4] = acc;
     if (d4 == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
   }
@@ -735,7 +794,7 @@ struct TcPlan {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-TcPlan plan_tc(const DecodeArgs& a, int sm_count) {
+TcPlan plan_tc(const DecodeArgs& a, int sm_count, bool fused) {
   TcPlan p{};
   p.row_tiles = (a.R + kRows - 1) / kRows;
   const int64_t units = (int64_t)a.B * a.shard_count * p.row_tiles;   // clusters per split
@@ -762,7 +821,7 @@ TcPlan plan_tc(const DecodeArgs& a, int sm_count) {
   p.splits = (int32_t)((n_max + chunk - 1) / chunk);
   if (p.splits <= 1) {
     p.splits = 1;
-    return p;
+    if (!fused) return p;
   }
   const int64_t rows_all = (int64_t)a.B * a.shard_count * a.R;
   p.cnt_off = 0;
@@ -799,7 +858,9 @@ bool tc_supported(const DecodeArgs& a) {
   return true;
 }
 
-size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_tc(a, sm_count).bytes; }
+size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
+  return plan_tc(a, sm_count, fused).bytes;
+}
 
 template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
@@ -814,8 +875,9 @@ int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
   return launch_status();
 }
 
-int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
-  const TcPlan plan = plan_tc(a, sm_count);
+int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
+                     bool fused) {
+  const TcPlan plan = plan_tc(a, sm_count, fused);
   if (ws_bytes < plan.bytes || (plan.bytes && !ws)) return DCPMLA_ERR_CAPACITY;
   TcParams* tp = new (std::nothrow) TcParams();
   if (!tp) return DCPMLA_ERR_CAPACITY;
@@ -825,6 +887,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   p.num_splits = plan.splits;
   p.chunk = plan.chunk;
   p.row_tiles = plan.row_tiles;
+  p.fused = fused ? 1 : 0;
   int rc = DCPMLA_OK;
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
     const void* pool = a.kv.pool[a.shard_begin + i];
@@ -835,7 +898,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
     if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
       p.use3d = 0;   // fall back to one 2-D box per chunk
-  if (rc == DCPMLA_OK && plan.splits > 1) {
+  if (rc == DCPMLA_OK && (plan.splits > 1 || fused)) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
     p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);

@@ -89,7 +89,7 @@ class DecodeStep:
     """Preallocated buffers for one batch shape: append Tq new tokens per request, decode, merge."""
 
     def __init__(self, cache: StripedKVCache, reqs: Sequence[int], Tq: int, H: int,
-                 sm_scale: float, lse_base: int, append: bool = True):
+                 sm_scale: float, lse_base: int, append: bool = True, fused: bool = False):
         self.cache = cache
         self.reqs = list(reqs)
         self.Bn = len(self.reqs)
@@ -97,6 +97,7 @@ class DecodeStep:
         self.R = Tq * H
         self.sm_scale, self.lse_base = sm_scale, lse_base
         self.do_append = append
+        self.fused = fused            # decode + merge in one call (no per-shard partials)
         dev = cache.device
         c = cache.c
         pt, lens = cache.tables(self.reqs)
@@ -122,6 +123,9 @@ class DecodeStep:
         self.lse = torch.empty((self.Bn, Tq, H), dtype=torch.float32, device=dev)
         ws = B.dcpmla_decode_workspace_size(self.Bn, Tq, H, cache.P, c, c, cache.kv_dtype,
                                             self.page_table.shape[1])
+        if fused:
+            ws = B.dcpmla_decode_merged_workspace_size(self.Bn, Tq, H, cache.P, c, cache.kv_dtype,
+                                                       self.page_table.shape[1])
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
 
     def run(self, stream=None) -> None:
@@ -138,14 +142,21 @@ class DecodeStep:
                      self.new_scales, self.owner, self.phys, None, stream)
 
     def run_decode(self, stream=None) -> None:
-        """Shard-local decode of all c shards: o_part, lse_part."""
+        """Shard-local decode of all c shards: o_part, lse_part (fused: merged o, lse)."""
         c = self.cache
+        if self.fused:
+            B.dcpmla_decode_merged(self.q, c.pools, c.scales, c.kv_dtype, self.page_table, self.seq_lens,
+                                   c.P, c.c, self.sm_scale, self.lse_base, self.o, self.lse,
+                                   self.workspace, c.err, stream, interleave=c.interleave)
+            return
         B.dcpmla_decode(self.q, c.pools, c.scales, c.kv_dtype, self.page_table, self.seq_lens, c.P,
                         c.c, 0, c.c, self.sm_scale, self.lse_base, self.o_part, self.lse_part,
                         self.workspace, c.err, stream, interleave=c.interleave)
 
     def run_merge(self, stream=None) -> None:
-        """Exact LSE merge of the c partials into o, lse."""
+        """Exact LSE merge of the c partials into o, lse (nothing to do when fused)."""
+        if self.fused:
+            return
         c = self.cache
         B.dcpmla_lse_merge(self.o_part, self.lse_part, c.c, self.Bn * self.R, self.lse_base,
                            self.o, self.lse, c.err, stream)

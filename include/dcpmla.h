@@ -242,6 +242,28 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
                        int32_t kv_dtype, int32_t max_pages, int32_t* path, int32_t* kernel_launches);
 
 /* ------------------------------------------------------------------------
+ * Fused decode + merge (SGLang DCP docs, MLA decode dataflow: every shard's
+ * locally normalised (o_r, lse_r) goes into the exact LSE merge).  Decodes all
+ * c shards of every request as dcpmla_decode does and writes the merged result
+ * directly: d_o fp32 [B, Tq, H, 512] = sum_r b^(lse_r - lse) o_r and d_lse fp32
+ * [B, Tq, H] = log_b sum_r b^(lse_r), in lse_base; there is no per-shard output.
+ * The tensor-core paths merge inside the decode (the token-major path in one
+ * merge kernel over every partial of the request, the 128-row path in the last
+ * CTA of each request's row tile); the CUDA-core path decodes into the
+ * workspace and then runs the LSE merge.  A shard that needed a bad page id is
+ * left out of the merge (DCPMLA_DERR_PAGE is set), like its empty partial in
+ * the unfused path.  Arguments as in dcpmla_decode; d_workspace: at least
+ * dcpmla_decode_merged_workspace_size() bytes for the same shape.
+ * ------------------------------------------------------------------------ */
+int dcpmla_decode_merged_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+                                        int32_t kv_dtype, int32_t max_pages, size_t* out);
+int dcpmla_decode_merged(const void* d_q, void* const* pools, float* const* scale_pools, int32_t kv_dtype,
+                         int64_t pool_rows, const int32_t* d_page_table, int32_t max_pages,
+                         const int32_t* d_seq_lens, int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
+                         int32_t interleave, float sm_scale, int32_t lse_base, float* d_o, float* d_lse,
+                         void* d_workspace, size_t ws_bytes, int32_t* d_err, void* stream);
+
+/* ------------------------------------------------------------------------
  * Token relayout, DCP-1 prefill cache -> striped decode pools (SGLang DCP
  * docs, DCP x PD disaggregation: dense prefill pages are not copied straight
  * into striped storage; a DCP-1 prefill feeds DCP decode through a token

@@ -261,3 +261,48 @@ def test_decode_path_per_workload():
     w = SMALL["c16_short"]
     got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
     assert got == (B.PATH_CUDA_CORE, 1)
+
+
+
+FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
+               "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
+               "ilv2_c16"]
+
+
+@needs_cuda
+@pytest.mark.parametrize("name", FUSED_CASES)
+def test_fused_decode_merge_parity(name):
+    """dcpmla_decode_merged: the merged (o, lse) straight from the decode, on every kernel path."""
+    w = SMALL[name]
+    dw = Hn.build(w, fused=True)
+    dw.step.run()
+    torch.cuda.synchronize()
+    assert dw.cache.check_errors() == 0
+    ow = OracleWorkload(w)
+    tol = TOL[w.kv_dtype]
+    o = dw.step.o.cpu().numpy()
+    lse = dw.step.lse.cpu().numpy()
+    R = w.Tq * w.H
+    for b in range(w.B):
+        _, _, o_ref, l_ref = ow.decode(b)
+        assert row_rel_err(o[b].reshape(R, 512), o_ref) < tol, (name, b, "o")
+        assert lse_err(lse[b].reshape(R), l_ref) < tol, (name, b, "lse")
+
+
+@needs_cuda
+@pytest.mark.parametrize("name", ["dsv3_s", "fh_tq2_c3"])
+def test_fused_decode_merge_leaves_out_a_bad_request(name):
+    w = BAD_INPUT_CASES[name]
+    dw = Hn.build(w, fused=True)
+    st = dw.step
+    st.run()
+    torch.cuda.synchronize()
+    st.page_table[1, 0] = 10**8
+    dw.cache.err.zero_()
+    st.run_decode()
+    torch.cuda.synchronize()
+    assert dw.cache.check_errors() & B.DERR_PAGE
+    assert torch.all(torch.isneginf(st.lse[1])) and torch.all(st.o[1] == 0)
+    ow = OracleWorkload(w)
+    _, _, o_ref, _ = ow.decode(0)
+    assert row_rel_err(st.o[0].cpu().numpy().reshape(-1, 512), o_ref) < TOL["bf16"]
