@@ -59,6 +59,7 @@ constexpr int kRawStages = 2;
 constexpr int kQropeBytes = kRows * 128;             // 64 rope dims x 128 rows
 constexpr int kXBytes = kRows * kTileTok * 4;        // one fp32 partial score tile
 constexpr int kSoftmaxThreads = 256;
+constexpr int kWgThreads = 128;                     // one softmax warpgroup
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
 constexpr long long kWaitCycles = 2000000000LL;     // about one second
 
@@ -68,10 +69,13 @@ constexpr long long kWaitCycles = 2000000000LL;     // about one second
 // 3-deep ring of fp16 stages, and all MMAs run in fp16.
 template <bool kFp8>
 struct Cfg {
-  static constexpr int kStages = kFp8 ? 3 : 4;
+  static constexpr int kStages = 3;
+  // bf16: the two softmax warpgroups take alternate tiles, each with its own exchange
+  // buffer; E4M3 keeps both warpgroups on one tile (its converter stages need the room)
+  static constexpr int kXBufs = kFp8 ? 1 : 2;
   static constexpr int kThreads = kFp8 ? 384 : 320;   // <= 3 warps per SM sub-partition
   static constexpr int kConvThreads = 64;
-  static constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBytes +
+  static constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBufs * kXBytes +
                                        (kFp8 ? kRawStages * kRawStageBytes : 0);
 };
 
@@ -125,15 +129,17 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
   uint8_t* sKV = smem + kQropeBytes;                     // kStages x kStageBytes (16-bit values)
-  uint8_t* sX = sKV + kStages * kStageBytes;             // the peer's partial scores
-  uint8_t* sRaw = sX + kXBytes;                          // E4M3 only: raw stages
+  uint8_t* sX = sKV + kStages * kStageBytes;             // the peer's partial scores, per warpgroup
+  uint8_t* sRaw = sX + C::kXBufs * kXBytes;              // E4M3 only: raw stages
+  constexpr int kXB = C::kXBufs;
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
-  __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_mref[2], bar_max[2];
+  __shared__ uint64_t bar_x_full[2], bar_x_empty[2], bar_x_read[2];
   __shared__ uint64_t bar_q_full, bar_o, bar_o_full, bar_drain, bar_l;
-  __shared__ float xmax_s[2][2][kRows];
-  __shared__ float l_s[2][kRows];
+  __shared__ float mref_s[2][kRows];                       // a warpgroup's reference max after its tile
+  __shared__ float xmax_s[kFp8 ? 2 : 1][2][kFp8 ? kRows : 1];   // E4M3: the two halves' row maxima
+  __shared__ float l_s[2][kRows], m_s[2][kRows];
   __shared__ float kscale_s[kFp8 ? kStages : 1][kTileTok];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s, bad_s, last_s;
@@ -159,12 +165,14 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bar_s_full[s]), 1);
-      mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);
+      // bf16: one warpgroup per tile parity; E4M3: both warpgroups on every tile
+      mbar_init(smem_u32(&bar_p_full[s]), kFp8 ? kSoftmaxThreads : kWgThreads);
+      mbar_init(smem_u32(&bar_mref[s]), kWgThreads);
       mbar_init(smem_u32(&bar_max[s]), kSoftmaxThreads);
+      mbar_init(smem_u32(&bar_x_full[s]), 1);
+      mbar_init(smem_u32(&bar_x_empty[s]), 1);                 // the peer's relay thread
+      mbar_init(smem_u32(&bar_x_read[s]), kFp8 ? kSoftmaxThreads : kWgThreads);
     }
-    mbar_init(smem_u32(&bar_x_full), 1);
-    mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
-    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
     mbar_init(smem_u32(&bar_o), 1);
@@ -336,10 +344,10 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
       // relay: once all softmax threads have read the peer's partial for a tile,
       // tell the peer its next partial may overwrite our exchange buffer.  This
       // thread has no stores in flight, so its cluster-scope release is cheap.
-      const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
+      // tile i goes through exchange buffer i % kXB (bf16: its warpgroup's)
       for (int i = 0; i < ntiles; ++i) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
-        mbar_arrive_remote(xe_peer);
+        if (!wait_bar<false>(smem_u32(&bar_x_read[i % kXB]), (i / kXB) & 1, abort_flag)) break;
+        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[i % kXB]), peer));
       }
     }
   } else if (warp >= 10) {
@@ -387,7 +395,6 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int stid = g * kRows + row;                        // 0..255
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
     const bool real = grow < R;                              // rows past R pad the tile
@@ -395,8 +402,9 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     const int qpos_min = L - a.Tq;                           // earliest query of the request
     const float qscale = a.sm_scale * kLog2e;
     const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
-    const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
-    float m_ref = -INFINITY, l = 0.f;
+    // this warpgroup's partial sum l is relative to m_own (the reference max at its
+    // last tile); the current reference is the latest one any warpgroup published
+    float m_own = -INFINITY, l = 0.f;
     bool ok = true;
     if (ntiles > 0) {
       // this CTA's latent dims of the query row into TMEM as packed 16-bit pairs
@@ -434,140 +442,313 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_q_full));
     }
-    for (int i = 0; ok && i < ntiles; ++i) {
-      const int sb = i & 1, st = i % kStages;
-      const int t0 = j0 + i * kTileTok;
-      const int ntok = min(kTileTok, j1 - t0);
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t own[32];
-      tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
-      tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
-                *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
-      tmem_ld_wait();
-      // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
-      // float4), once the peer has read the previous one
-      if (i >= 1) {
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
-                    make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
-      if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
-      ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), i & 1, abort_flag));
-      if (!ok) break;
-      float x[32];
-      const float4* xin = reinterpret_cast<const float4*>(sX);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 pv = xin[(8 * g + c) * kRows + row];
-        const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
-        const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
-        // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
-        x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
-        x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
-        x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
-        x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
-      }
-      mbar_arrive(smem_u32(&bar_x_read));
-      const float* ks = kscale_s[kFp8 ? st : 0] + 32 * g;
-      if (kFp8) {
-        // E4M3: the key's per-token scale multiplies its score
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] *= ks[k];
-      }
-      // causal / tail mask on raw scores (only tiles that need it)
-      const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
-      if (!full_vis) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int kk = 32 * g + k;
-          const bool vis = kk < ntok && shard_pos(t0 + kk, r, a.c, a.I) <= qpos;
-          x[k] = vis ? x[k] : -INFINITY;
-        }
-      }
-      float tmax = fmaxf(x[0], x[1]);
-#pragma unroll
-      for (int k = 2; k < 32; ++k) tmax = fmaxf(tmax, x[k]);
-      // row max across the two warpgroups; this sync also orders every thread's
-      // S reads before any P write into the same TMEM columns
-      xmax_s[i & 1][g][row] = tmax;
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_max[i & 1]));
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
-      // Lazy reference max: move it only when this tile's max exceeds it by more
-      // than 8 (so every weight 2^(x - m_ref) stays <= 256).  Rows that move it
-      // after O holds data rescale O (each warpgroup its 128 columns).
-      const bool move = tmax > m_ref + 8.f;
-      const bool rescale_me = move && m_ref != -INFINITY;
-      if (__any_sync(0xffffffffu, rescale_me)) {
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+    if constexpr (kFp8) {
+      // both warpgroups on every tile, warpgroup g on tile columns [32g, 32g + 32)
+      const int stid = g * kRows + row;                      // 0..255
+      const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[0]), peer);
+      float m_ref = -INFINITY;
+      for (int i = 0; ok && i < ntiles; ++i) {
+        const int sb = i & 1, st = i % kStages;
+        const int t0 = j0 + i * kTileTok;
+        const int ntok = min(kTileTok, j1 - t0);
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
-        for (int q = 0; q < 8; ++q) {
-          uint32_t u[16];
-          const uint32_t oc = tmem + lane_off + kColO + g * 128 + q * 16;
-          tmem_ld16(oc, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-          tmem_st16(oc, u);
+        uint32_t own[32];
+        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
+        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
+                  *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
+        tmem_ld_wait();
+        // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
+        // float4), once the peer has read the previous one
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[0]), (i - 1) & 1, abort_flag));
+          if (!ok) break;
         }
-        l *= alpha;
-      }
-      if (move) m_ref = tmax;
-      const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
-      const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
-      float ps = 0.f;
-      if (kFp8) {
-        // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
-        uint32_t pp[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
-          const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
-          ps += p0 + p1;
-          pp[k >> 1] = pack_f16(p0 * ks[k], p1 * ks[k + 1]);
+  #pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
+                      make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
+        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[0]), kXBytes);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[0]), i & 1, abort_flag));
+        if (!ok) break;
+        float x[32];
+        const float4* xin = reinterpret_cast<const float4*>(sX);
+  #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 pv = xin[(8 * g + c) * kRows + row];
+          const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
+          const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
+          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+          x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
+          x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
+          x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
+          x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
         }
-        tmem_st16(pcol + 16 * g, pp);
-      } else {
-        // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
-        // rounding of the weights alone would cost ~1e-3 relative error in O.
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
-          const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
-          ps += p0 + p1;
-          const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-          const float2 hf = __bfloat1622float2(hh);
-          hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
-          lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+        mbar_arrive(smem_u32(&bar_x_read[0]));
+        const float* ks = kscale_s[st] + 32 * g;
+        if (kFp8) {
+          // E4M3: the key's per-token scale multiplies its score
+  #pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] *= ks[k];
         }
-        tmem_st16(pcol + 16 * g, hi);
-        tmem_st16(pcol + 32 + 16 * g, lo);
-        if (ntok < kTileTok) {
-          // rows past the split's last token hold stale data: zero this CTA's V rows
-          uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
-          const int tail = kTileTok - ntok;
-          for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
-            const int cch = e / (tail * 8), rem = e % (tail * 8);
-            v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+        // causal / tail mask on raw scores (only tiles that need it)
+        const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
+        if (!full_vis) {
+  #pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int kk = 32 * g + k;
+            const bool vis = kk < ntok && shard_pos(t0 + kk, r, a.c, a.I) <= qpos;
+            x[k] = vis ? x[k] : -INFINITY;
           }
-          fence_proxy_async();
         }
+        float tmax = fmaxf(x[0], x[1]);
+  #pragma unroll
+        for (int k = 2; k < 32; ++k) tmax = fmaxf(tmax, x[k]);
+        // row max across the two warpgroups; this sync also orders every thread's
+        // S reads before any P write into the same TMEM columns
+        xmax_s[i & 1][g][row] = tmax;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_max[i & 1]));
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
+        // Lazy reference max: move it only when this tile's max exceeds it by more
+        // than 8 (so every weight 2^(x - m_ref) stays <= 256).  Rows that move it
+        // after O holds data rescale O (each warpgroup its 128 columns).
+        const bool move = tmax > m_ref + 8.f;
+        const bool rescale_me = move && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale_me)) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+          for (int q = 0; q < 8; ++q) {
+            uint32_t u[16];
+            const uint32_t oc = tmem + lane_off + kColO + g * 128 + q * 16;
+            tmem_ld16(oc, u);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+            tmem_st16(oc, u);
+          }
+          l *= alpha;
+        }
+        if (move) m_ref = tmax;
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
+        const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
+        float ps = 0.f;
+        if (kFp8) {
+          // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
+          uint32_t pp[16];
+  #pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+            const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
+            ps += p0 + p1;
+            pp[k >> 1] = pack_f16(p0 * ks[k], p1 * ks[k + 1]);
+          }
+          tmem_st16(pcol + 16 * g, pp);
+        } else {
+          // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
+          // rounding of the weights alone would cost ~1e-3 relative error in O.
+          uint32_t hi[16], lo[16];
+  #pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+            const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
+            ps += p0 + p1;
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(hh);
+            hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+            lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+          }
+          tmem_st16(pcol + 16 * g, hi);
+          tmem_st16(pcol + 32 + 16 * g, lo);
+          if (ntok < kTileTok) {
+            // rows past the split's last token hold stale data: zero this CTA's V rows
+            uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
+            const int tail = kTileTok - ntok;
+            for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
+              const int cch = e / (tail * 8), rem = e % (tail * 8);
+              v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+          }
+        }
+        l += ps;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[sb]));
       }
-      l += ps;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p_full[sb]));
+      m_own = m_ref;                                           // the same in both warpgroups
+    } else {
+      // Tiles alternate between the warpgroups: warpgroup g takes tiles i with i % 2 == g,
+      // each thread one query row over all 64 columns, so two tiles' exchanges and
+      // softmax chains are in flight at once.  The lazy reference max is handed from
+      // tile to tile through shared memory.
+      const int wtid = row;                                    // thread within its warpgroup
+      for (int i = g; ok && i < ntiles; i += 2) {
+        const int st = i % kStages;
+        const int t0 = j0 + i * kTileTok;
+        const int ntok = min(kTileTok, j1 - t0);
+        const uint32_t scol = tmem + lane_off + kColS + g * kTileTok;
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[g]), (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        // send this CTA's partial into the peer's buffer g ([16 column groups][128 rows]
+        // of float4), once the peer has read what this warpgroup sent two tiles ago
+        if (i >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((i >> 1) - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+        const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
+  #pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t own[32];
+          tmem_ld16(scol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
+          tmem_ld16(scol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
+          tmem_ld_wait();
+  #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_async_v4(x_remote + g * kXBytes + ((8 * half + c) * kRows + row) * 16,
+                        make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
+        }
+        if (wtid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        float x[64];
+        const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
+  #pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t own[32];   // this CTA's partial again (still in TMEM: P(i) is not written yet)
+          tmem_ld16(scol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
+          tmem_ld16(scol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
+          tmem_ld_wait();
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 pv = xin[(8 * half + c) * kRows + row];
+            const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
+            const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
+            // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+            float* xx = x + 32 * half + 4 * c;
+            xx[0] = h ? pv.x + o0 : o0 + pv.x;
+            xx[1] = h ? pv.y + o1 : o1 + pv.y;
+            xx[2] = h ? pv.z + o2 : o2 + pv.z;
+            xx[3] = h ? pv.w + o3 : o3 + pv.w;
+          }
+        }
+        mbar_arrive(smem_u32(&bar_x_read[g]));
+        const float* ks = kscale_s[kFp8 ? st : 0];
+        if (kFp8) {
+          // E4M3: the key's per-token scale multiplies its score
+  #pragma unroll
+          for (int k = 0; k < 64; ++k) x[k] *= ks[k];
+        }
+        // causal / tail mask on raw scores (only tiles that need it)
+        const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
+        if (!full_vis) {
+  #pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const bool vis = k < ntok && shard_pos(t0 + k, r, a.c, a.I) <= qpos;
+            x[k] = vis ? x[k] : -INFINITY;
+          }
+        }
+        float tmax = fmaxf(x[0], x[1]);
+  #pragma unroll
+        for (int k = 2; k < 64; ++k) tmax = fmaxf(tmax, x[k]);
+        tmax *= qscale;
+        // the reference max as the previous tile (the other warpgroup's) left it
+        float m_ref = -INFINITY;
+        if (i >= 1) {
+          const int pg = g ^ 1;
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[pg]), ((i - 1) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          m_ref = mref_s[pg][row];
+        }
+        // Lazy reference max: move it only when this tile's max exceeds it by more
+        // than 8 (so every weight 2^(x - m_ref) stays <= 256).  A row that moves it
+        // after O holds data rescales its O columns (all 256 of this CTA).
+        const bool move = tmax > m_ref + 8.f;
+        const bool rescale_me = move && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale_me)) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+          for (int q = 0; q < 16; ++q) {
+            uint32_t u[16];
+            const uint32_t oc = tmem + lane_off + kColO + q * 16;
+            tmem_ld16(oc, u);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+            tmem_st16(oc, u);
+          }
+          tmem_st_wait();
+        }
+        if (move) m_ref = tmax;
+        mref_s[g][row] = m_ref;
+        mbar_arrive(smem_u32(&bar_mref[g]));
+        // this warpgroup's partial sum follows the reference
+        if (m_own != m_ref) {
+          l = m_own == -INFINITY ? 0.f : l * ex2_approx(m_own - m_ref);
+          m_own = m_ref;
+        }
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
+        float ps = 0.f;
+        if (kFp8) {
+          // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
+  #pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pp[16];
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const int kk = 32 * half + k;
+              const float p0 = ex2_approx(fmaf(x[kk], qscale, -mr));
+              const float p1 = ex2_approx(fmaf(x[kk + 1], qscale, -mr));
+              ps += p0 + p1;
+              pp[k >> 1] = pack_f16(p0 * ks[kk], p1 * ks[kk + 1]);
+            }
+            tmem_st16(scol + 16 * half, pp);
+          }
+        } else {
+          // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
+          // rounding of the weights alone would cost ~1e-3 relative error in O.
+  #pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t hi[16], lo[16];
+  #pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const int kk = 32 * half + k;
+              const float p0 = ex2_approx(fmaf(x[kk], qscale, -mr));
+              const float p1 = ex2_approx(fmaf(x[kk + 1], qscale, -mr));
+              ps += p0 + p1;
+              const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+              const float2 hf = __bfloat1622float2(hh);
+              hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+              lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+            }
+            tmem_st16(scol + 16 * half, hi);
+            tmem_st16(scol + 32 + 16 * half, lo);
+          }
+          if (ntok < kTileTok) {
+            // rows past the split's last token hold stale data: zero this CTA's V rows
+            uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
+            const int tail = kTileTok - ntok;
+            for (int e = wtid; e < 4 * tail * 8; e += kWgThreads) {
+              const int cch = e / (tail * 8), rem = e % (tail * 8);
+              v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+          }
+        }
+        l += ps;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[g]));
+      }
     }
     // ---- epilogue ----
     if (ok && ntiles > 0)
@@ -575,10 +756,16 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
       // running, and a parity wait on bar_o would then match an older phase.
       ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
     l_s[g][row] = l;
+    m_s[g][row] = m_own;
     mbar_arrive(smem_u32(&bar_l));
     const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
     ok = ok && l_ok;
-    const float l_tot = l_s[0][row] + l_s[1][row];
+    // O follows the latest reference (the larger, since the reference only grows);
+    // each warpgroup's sum is brought to it
+    const float m0 = m_s[0][row], m1 = m_s[1][row];
+    const float m_ref = fmaxf(m0, m1);
+    const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_ref)) +
+                        (m1 == -INFINITY ? 0.f : l_s[1][row] * ex2_approx(m1 - m_ref));
     tc_fence_after();
     const bool direct = !p.fused && p.num_splits == 1;
     // workspace slot of this (shard, split): split-major unfused, shard-major fused
