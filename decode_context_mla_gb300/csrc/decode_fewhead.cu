@@ -25,13 +25,16 @@
 //
 //   warp 0     TMA producer: Q^T of the unit (one 16-row box per 64-dim chunk),
 //              then 128-token KV tiles (one 2-D box per page and 64-dim chunk)
-//              into a 2-deep stage ring.
-//   warp 1     lane 0 issues the MMAs, lane 1 relays "exchange buffer read" to
-//              the peer.  QK: M 128, N 16; PV: M 128 (V^T MN-major), N 32 = P as a
-//              bf16 hi part (rows 0-15) and lo part (rows 16-31).
+//              into a 2-deep stage ring, and L2 prefetches of the tiles a few
+//              places further on, so that the ring's loads mostly hit L2.
+//   warp 1     lane 0 issues the QK MMAs: M 128, N 16.  QK may run ahead of PV:
+//              a score buffer is free once the softmax has loaded it.
 //   warps 2-9  softmax, one thread per token lane, two warpgroups of 8 query
 //              rows each: base-2 online softmax with a lazily moved per-row
 //              reference max, P^T to shared memory, unit epilogue.
+//   warp 10    lane 0 relays "exchange buffer read" to the peer.
+//   warp 11    lane 0 issues the PV MMAs: M 128 (V^T MN-major), N 32 = P as a
+//              bf16 hi part (rows 0-15) and lo part (rows 16-31).
 //
 // TMEM columns: S^T double buffer [0, 32), O^T double buffer (by unit) [64, 192):
 // buffer o, value block m (128 dims): hi rows at 64 + 64o + 32m, lo rows 16 later.
@@ -56,6 +59,7 @@ constexpr int kRp = 16;                        // query rows per tile (MMA N); r
 constexpr int kChunk = kTok * 128;             // one 64-dim column chunk of a tile: 16 KB
 constexpr int kStage = 5 * kChunk;             // room for CTA 1's five chunks
 constexpr int kStages = 2;
+constexpr int kLook = 4;                       // page-id lookahead (tiles); L2 prefetch kLook - 1 ahead
 constexpr int kQChunk = kRp * 128;             // Q^T chunk [16 rows x 64 dims]
 constexpr int kQBuf = 5 * kQChunk;
 constexpr int kPChunk = 2 * kRp * 128;         // P^T chunk [32 rows (hi, lo) x 64 tokens]
@@ -63,8 +67,10 @@ constexpr int kPBuf = 2 * kPChunk;             // 128 tokens
 constexpr int kXBytes = kTok * kRp * 4;        // one fp32 partial S^T tile
 constexpr int kMaxItems = 2048;                // (request, shard) pairs per launch
 constexpr int kUnitsPerCluster = 16;
-constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kRelayWarp = 10;
+constexpr int kPvWarp = 11;
+constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kColS = 0, kColO = 64, kTmemCols = 256;
 constexpr long long kWaitCycles = 2000000000LL;   // about one second
 
@@ -163,7 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int* sPre = reinterpret_cast<int*>(smem + kOffPre);
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ uint64_t bar_q_full[2], bar_q_free[2];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_p_free[2], bar_o_free[2], bar_o_full[2];
+  __shared__ uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_p_free[2], bar_o_free[2], bar_o_full[2];
   __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
   __shared__ uint64_t bar_o, bar_drain;
   __shared__ __align__(16) float red_s[2][2][4][8];     // [tile parity][warpgroup][quarter][row]
@@ -189,6 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_q_full[s]), 1);
       mbar_init(smem_u32(&bar_q_free[s]), 1);
       mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_s_free[s]), kSoftmaxThreads / 32);
       mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);
       mbar_init(smem_u32(&bar_p_free[s]), 1);
       mbar_init(smem_u32(&bar_o_free[s]), kSoftmaxThreads);
@@ -196,9 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&bar_x_full), 1);
     mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
-    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads / 32);
     mbar_init(smem_u32(&bar_o), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_drain), 2);                  // both MMA issuers
     abort_s = 0;
     total_s = 0;
     ubad_s[0] = ubad_s[1] = 0;
@@ -288,11 +295,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     bool ok = true;
     int gi = 0, kk = 0, issued = 0;
+    const int box = p.box_rows;
+    // Page ids run kLook tiles ahead of the loads (across unit boundaries) through a
+    // per-lane FIFO: entry k holds, for lane l, box l of the tile k places ahead
+    // (its raw page id, rows, offset in the page, and the tile's shard).  The tile
+    // kLook - 1 places ahead is also prefetched into L2, so the ring's loads mostly
+    // hit L2; no page-table read is waited on between a stage's release and its load.
+    int pu = cl, pi = 0;
+    Unit px{};
+    if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
+    auto skip_empty = [&]() {
+      while (pu < units && px.ntiles == 0) {
+        pu += G;
+        if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
+      }
+    };
+    auto lookup = [&](int& g_, int& rows_, int& off_, int& sr_) {
+      g_ = 0;
+      rows_ = 0;
+      off_ = 0;
+      sr_ = 0;
+      if (pu >= units) return;
+      const int pt0 = px.j0 + pi * kTok;
+      const int nb = (min(kTok, px.j1 - pt0) + box - 1) / box;
+      sr_ = px.sr;
+      if (lane < nb) {
+        const int tok = pt0 + lane * box;
+        rows_ = min(box, px.j1 - tok);
+        off_ = tok % a.P;
+        g_ = __ldg(a.pt + (int64_t)px.b * a.max_pages + tok / a.P);
+      }
+      if (++pi >= px.ntiles) {
+        pi = 0;
+        pu += G;
+        if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
+        skip_empty();
+      }
+    };
+    int fg[kLook], fr[kLook], fo[kLook], fs[kLook];
+    skip_empty();
+#pragma unroll
+    for (int k = 0; k < kLook; ++k) lookup(fg[k], fr[k], fo[k], fs[k]);
     for (int u = cl; ok && u < units; u += G) {
       const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
       if (x.ntiles == 0) continue;
       const int qb = kk & 1;
-      const int32_t* pt_row = a.pt + (int64_t)x.b * a.max_pages;
       const CUtensorMap* kvmap = &p.tm_kv[x.sr];
       bool okq = true;
       if (lane == 0) {
@@ -310,18 +357,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int st = gi & 1;
         const int t0 = x.j0 + i * kTok;
         const int ntok = min(kTok, x.j1 - t0);
-        const int box = p.box_rows;
         const int nbox = (ntok + box - 1) / box;
-        // page of each box (lane < nbox); a bad page id is reported and read as page 0
+        // page of each box (lane < nbox, from the FIFO's head); a bad page id is
+        // reported and read as page 0
         int y = 0;
         if (lane < nbox) {
-          const int tok = t0 + lane * box;
-          int g = __ldg(pt_row + tok / a.P);
+          int g = fg[0];
           if (g < 0 || (int64_t)g >= a.num_pages) {
             set_err(a.err, DCPMLA_DERR_PAGE);
             g = 0;
           }
-          y = g * a.P + tok % a.P;
+          y = g * a.P + fo[0];
         }
         bool okw = true;
         if (lane == 0 && gi >= kStages)
@@ -336,6 +382,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int c = 0; c < nck; ++c) tma_load_2d(dst + c * kChunk, kvmap, (int)(4 * h + c) * 64, y, full);
         }
         issued = gi + 1;
+        // L2 prefetch of the tile kLook - 1 places ahead: a box's rows are contiguous
+        // in the pool, and each CTA prefetches half of them
+        if (fr[kLook - 1] > 0) {
+          int g = fg[kLook - 1];
+          if (g < 0 || (int64_t)g >= a.num_pages) g = 0;   // reported when the tile is loaded
+          const int64_t py = (int64_t)g * a.P + fo[kLook - 1];
+          const uint32_t half = (uint32_t)fr[kLook - 1] * (kDK * 2 / 2);   // a multiple of 16 bytes
+          const uint8_t* src =
+              static_cast<const uint8_t*>(a.kv.pool[a.shard_begin + fs[kLook - 1]]) + py * (kDK * 2);
+          bulk_prefetch_l2(src + h * half, half);
+        }
+#pragma unroll
+        for (int k = 0; k + 1 < kLook; ++k) {
+          fg[k] = fg[k + 1];
+          fr[k] = fr[k + 1];
+          fo[k] = fo[k + 1];
+          fs[k] = fs[k + 1];
+        }
+        lookup(fg[kLook - 1], fr[kLook - 1], fo[kLook - 1], fs[kLook - 1]);
       }
       ++kk;
     }
@@ -354,13 +419,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kPvWarp) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA
-      // Polls its barriers and issues whichever is ready: the oldest tile's PV (its
-      // P is written; first, since it frees the tile's stage for the next load) or
-      // the next tile's QK (its KV landed, and the score buffer it overwrites was
-      // consumed: at most one tile ahead of the oldest PV).
+      // Two issuing threads, each blocking on its own barriers: warp 1 issues the QK
+      // of each tile once its KV landed and the softmax has loaded the scores two
+      // tiles back (whose TMEM buffer it overwrites), so QK runs ahead of PV; warp
+      // kPvWarp issues each tile's PV once its P is written, which frees the tile's
+      // stage for the next load.  A commit tracks the MMAs of the thread issuing it.
       constexpr uint32_t idesc_qk = idesc_bf16(kTok, kRp, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, false);
       // Base descriptors; the start-address field is the low 14 bits (address >> 4),
@@ -369,49 +435,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t vA0 = desc_sw128(smem_u32(sKV), kChunk, 1024);    // values, MN-major
       const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
       const uint64_t pB0 = desc_sw128(smem_u32(sP), 16, 1024);         // P^T, K-major
-      int total = 0;
-      for (int u = cl; u < units; u += G) total += get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
-      // QK cursor over this cluster's non-empty units
-      int uq = cl, iq = 0, kkq = 0, ntq = 0;
-      bool q_ready = false;
-      while (uq < units && (ntq = get_unit(a, sPre, nitems, chunk_tiles, uq).ntiles) == 0) uq += G;
-      int gq = 0, gp = 0;                 // next tile to QK / to PV
-      int pv_ob[2], pv_kk[2];
-      bool pv_first[2], pv_last[2];
-      long long t_idle = clock64();
-      while (gp < total) {
-        bool progressed = false;
-        if (gp < gq) {
-          const int sb = gp & 1;
-          const bool first = pv_first[sb];
-          const int ob = pv_ob[sb], kk = pv_kk[sb];
-          if (mbar_test_wait(smem_u32(&bar_p_full[sb]), (gp >> 1) & 1) &&
-              (!first || kk < 2 || mbar_test_wait(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1))) {
-            tc_fence_after();
-#pragma unroll
-            for (int mb = 0; mb < 2; ++mb) {
-              const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * kChunk + ks * 2048) >> 4);
-                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + (ks >> 2) * kPChunk + (ks & 3) * 32) >> 4);
-                mma_ss(d, ad, bd, idesc_pv, (first && ks == 0) ? 0u : 1u);
-              }
-            }
-            mma_commit(smem_u32(&bar_kv_empty[sb]));
-            mma_commit(smem_u32(&bar_p_free[sb]));
-            mma_commit(smem_u32(&bar_o));
-            // the unit's O^T is complete: one phase of its buffer's barrier per unit
-            if (pv_last[sb]) mma_commit(smem_u32(&bar_o_full[ob]));
-            ++gp;
-            progressed = true;
-          }
-        }
-        if (gq < total && gq - gp < 2) {
-          const int qb = kkq & 1;
-          if (!q_ready) q_ready = mbar_test_wait(smem_u32(&bar_q_full[qb]), (kkq >> 1) & 1);
-          const int sb = gq & 1;
-          if (q_ready && mbar_test_wait(smem_u32(&bar_kv_full[sb]), (gq >> 1) & 1)) {
+      const bool qk_role = warp == 1;
+      bool ok = true;
+      int gt = 0, kk = 0;                  // tiles and non-empty units so far
+      for (int u = cl; ok && u < units; u += G) {
+        const int ntiles = get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
+        if (ntiles == 0) continue;
+        const int qb = kk & 1, ob = kk & 1;
+        if (qk_role) {
+          ok = wait_bar<false>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag);
+          for (int i = 0; ok && i < ntiles; ++i, ++gt) {
+            const int sb = gt & 1;
+            if (gt >= 2) ok = wait_bar<false>(smem_u32(&bar_s_free[sb]), ((gt >> 1) - 1) & 1, abort_flag);
+            if (ok) ok = wait_bar<false>(smem_u32(&bar_kv_full[sb]), (gt >> 1) & 1, abort_flag);
+            if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
 #pragma unroll
@@ -423,38 +460,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                        qB0 + (uint64_t)((qb * kQBuf + c * kQChunk + k * 32) >> 4), idesc_qk, (c | k) != 0);
             }
             mma_commit(smem_u32(&bar_s_full[sb]));
-            pv_ob[sb] = kkq & 1;
-            pv_kk[sb] = kkq;
-            pv_first[sb] = iq == 0;
-            pv_last[sb] = iq == ntq - 1;
-            if (++iq == ntq) {               // last tile of the unit: its Q buffer may be refilled
-              mma_commit(smem_u32(&bar_q_free[qb]));
-              iq = 0;
-              ++kkq;
-              q_ready = false;
-              uq += G;
-              while (uq < units && (ntq = get_unit(a, sPre, nitems, chunk_tiles, uq).ntiles) == 0) uq += G;
+          }
+          if (ok) mma_commit(smem_u32(&bar_q_free[qb]));   // the unit's Q buffer may be refilled
+        } else {
+          for (int i = 0; ok && i < ntiles; ++i, ++gt) {
+            const int sb = gt & 1;
+            ok = wait_bar<false>(smem_u32(&bar_p_full[sb]), (gt >> 1) & 1, abort_flag);
+            if (ok && i == 0 && kk >= 2)
+              ok = wait_bar<false>(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+              const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * kChunk + ks * 2048) >> 4);
+                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + (ks >> 2) * kPChunk + (ks & 3) * 32) >> 4);
+                mma_ss(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
+              }
             }
-            ++gq;
-            progressed = true;
+            mma_commit(smem_u32(&bar_kv_empty[sb]));
+            mma_commit(smem_u32(&bar_p_free[sb]));
+            mma_commit(smem_u32(&bar_o));
+            // the unit's O^T is complete: one phase of its buffer's barrier per unit
+            if (i == ntiles - 1) mma_commit(smem_u32(&bar_o_full[ob]));
           }
         }
-        if (progressed) {
-          t_idle = clock64();
-        } else if (*abort_flag) {
-          break;
-        } else if (clock64() - t_idle > kWaitCycles) {
-          *abort_flag = 1;
-          break;
-        }
+        ++kk;
       }
-      // drain: every MMA issued above completes before TMEM is released
+      // drain: every MMA issued above completes before TMEM is released (one
+      // arrival per issuing thread)
       mma_commit(smem_u32(&bar_drain));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
       }
-    } else if (lane == 1) {
-      // relay: once all softmax threads have read the peer's partial for a tile,
+    }
+  } else if (warp == kRelayWarp) {
+    if (lane == 0) {
+      // relay: once all softmax warps have read the peer's partial for a tile,
       // tell the peer its next partial may overwrite this CTA's exchange buffer
       int total = 0;
       for (int u = cl; u < units; u += G) total += get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
@@ -504,16 +548,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int sb = gi & 1;
         const int t0 = x.j0 + i * kTok;
         const int ntok = min(kTok, x.j1 - t0);
-        if (tok < ntok) {
-          const int gpg = __ldg(pt_row + (t0 + tok) / a.P);
-          bad |= gpg < 0 || (int64_t)gpg >= a.num_pages;
-        }
+        // this thread's page id, checked at the end of the tile (its load is in
+        // flight meanwhile)
+        const int gpg = tok < ntok ? __ldg(pt_row + (t0 + tok) / a.P) : 0;
         ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         uint32_t own[8];
         tmem_ld8(tmem + lane_off + kColS + (uint32_t)(sb * kRp + 8 * g), own);
         tmem_ld_wait();
+        // the score buffer may take the QK two tiles ahead
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
         // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
         if (gi >= 1) {
           ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
@@ -538,7 +585,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[4 * v + 2] = h ? pv.z + o2 : o2 + pv.z;
           s[4 * v + 3] = h ? pv.w + o3 : o3 + pv.w;
         }
-        mbar_arrive(smem_u32(&bar_x_read));
+        // this warp has read the peer's partial (the relay tells the peer)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_x_read));
         // causal / tail / padding-row mask, base-2 scaling
         const bool full_vis = all_rows && ntok == kTok && shard_pos(t0 + kTok - 1, x.r, a.c, a.I) <= qpos_min;
         const int64_t kpos = shard_pos(t0 + tok, x.r, a.c, a.I);
@@ -588,6 +637,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (mv) m_ref[n] = tmax[n];
           }
           if (any_rescale) {   // the same decision in every thread of the warpgroup
+            // O^T holds every PV before this tile once PV(gi - 1) completes.  QK runs
+            // ahead of PV, so PV(gi - 2) may still be in flight: wait for it first
+            // (its P buffer's barrier), or the parity wait on bar_o could match the
+            // phase before.
+            if (gi >= 2) {
+              ok = __all_sync(0xffffffffu,
+                              wait_bar<false>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
+              if (!ok) break;
+            }
             ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -642,6 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p_full[sb]));
+        bad |= gpg < 0 || (int64_t)gpg >= a.num_pages;
       }
       if (!ok) break;
       // ---- unit epilogue: O^T / l, partial or final output ----
