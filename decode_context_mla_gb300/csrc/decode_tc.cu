@@ -398,8 +398,11 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
     const bool real = grow < R;                              // rows past R pad the tile
-    const int qpos = L - a.Tq + (int)(grow / a.H);
-    const int qpos_min = L - a.Tq;                           // earliest query of the request
+    // Shard positions grow with the shard-local index, so the keys a query sees form a
+    // prefix: shard-local tokens below shard_len(qpos + 1) (those at positions <= qpos),
+    // and below j1.  jvis: this row's prefix; jvis_min: every row's (the earliest query).
+    const int jvis = min(j1, shard_len(L - a.Tq + (int)(grow / a.H) + 1, r, a.c, a.I));
+    const int jvis_min = min(j1, shard_len(L - a.Tq + 1, r, a.c, a.I));
     const float qscale = a.sm_scale * kLog2e;
     const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
     // this warpgroup's partial sum l is relative to m_own (the reference max at its
@@ -493,14 +496,10 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
           for (int k = 0; k < 32; ++k) x[k] *= ks[k];
         }
         // causal / tail mask on raw scores (only tiles that need it)
-        const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
-        if (!full_vis) {
+        if (t0 + kTileTok > jvis_min) {
+          const int lim = jvis - t0 - 32 * g;
   #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int kk = 32 * g + k;
-            const bool vis = kk < ntok && shard_pos(t0 + kk, r, a.c, a.I) <= qpos;
-            x[k] = vis ? x[k] : -INFINITY;
-          }
+          for (int k = 0; k < 32; ++k) x[k] = k < lim ? x[k] : -INFINITY;
         }
         float tmax = fmaxf(x[0], x[1]);
   #pragma unroll
@@ -647,13 +646,10 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
           for (int k = 0; k < 64; ++k) x[k] *= ks[k];
         }
         // causal / tail mask on raw scores (only tiles that need it)
-        const bool full_vis = ntok == kTileTok && shard_pos(t0 + kTileTok - 1, r, a.c, a.I) <= qpos_min;
-        if (!full_vis) {
+        if (t0 + kTileTok > jvis_min) {
+          const int lim = jvis - t0;
   #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const bool vis = k < ntok && shard_pos(t0 + k, r, a.c, a.I) <= qpos;
-            x[k] = vis ? x[k] : -INFINITY;
-          }
+          for (int k = 0; k < 64; ++k) x[k] = k < lim ? x[k] : -INFINITY;
         }
         float tmax = fmaxf(x[0], x[1]);
   #pragma unroll
