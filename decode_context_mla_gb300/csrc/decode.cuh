@@ -28,6 +28,10 @@ struct DecodeArgs {
 // 2-D tensor map over a row-major bf16 matrix [rows, cols] with 128-byte swizzle.
 int tma_encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                        uint32_t box_rows);
+// A bf16 pool [rows, 576] viewed as {64 dims, 8 rows, 9 chunks of 64 dims, rows / 8 row
+// groups}: one box {64, 8, chunks, groups} lands as [group][chunk][8 rows x 128 B]
+// 128-byte-swizzle atoms (rows % 8 == 0).
+int tma_encode_kv_rowgroups(CUtensorMap* m, const void* base, uint64_t rows, uint32_t chunks, uint32_t groups);
 
 // Tensor-core path for few query rows (<= 16): KV tokens are the MMA's M dimension.
 bool fh_supported(const DecodeArgs& a, int sm_count);

@@ -58,6 +58,9 @@ constexpr int kTok = 128;                      // tokens per tile = MMA M of the
 constexpr int kRp = 16;                        // query rows per tile (MMA N); rows >= R are padding
 constexpr int kChunk = kTok * 128;             // one 64-dim column chunk of a tile: 16 KB
 constexpr int kStage = 5 * kChunk;             // room for CTA 1's five chunks
+// A stage is row-group major: [8-token group g][chunk c][8 tokens x 128 B], each 1 KB piece a
+// 128-byte-swizzle atom, so one 4-D TMA box lands all of a page box's chunks; for the MMAs the
+// 8-token groups of a chunk are nck KB apart and a chunk's groups start c KB in.
 constexpr int kStages = 2;
 constexpr int kLook = 4;                       // page-id lookahead (tiles); L2 prefetch kLook - 1 ahead
 constexpr int kQChunk = kRp * 128;             // Q^T chunk [16 rows x 64 dims]
@@ -83,7 +86,7 @@ constexpr size_t kSmemBytes = 1024 + kOffPre + (kMaxItems + 1) * 4;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffX % 1024 == 0, "1 KB aligned buffers");
 
 struct FhParams {
-  CUtensorMap tm_kv[kMaxFhShards];   // pool as [pool_rows, 576] bf16, box {64, box_rows}
+  CUtensorMap tm_kv[2][kMaxFhShards];   // [CTA] pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, nck, box_rows / 8}
   CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
   DecodeArgs a;
   int32_t box_rows;                  // rows per TMA box: min(P, 128)
@@ -94,6 +97,7 @@ struct FhParams {
   int32_t* ws_pre;                   // [B * shard_count + 1]: first unit of each (request, shard)
   int32_t fused;                     // 1: every unit to the workspace, merged over shards into o, lse
 };
+static_assert(sizeof(FhParams) <= 4096, "kernel parameter space");
 
 template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -291,7 +295,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
-      for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[i]);
+      for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[h][i]);
     }
     bool ok = true;
     int gi = 0, kk = 0, issued = 0;
@@ -340,7 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
       if (x.ntiles == 0) continue;
       const int qb = kk & 1;
-      const CUtensorMap* kvmap = &p.tm_kv[x.sr];
+      const CUtensorMap* kvmap = &p.tm_kv[h][x.sr];
       bool okq = true;
       if (lane == 0) {
         if (kk >= 2) okq = wait_bar<false>(smem_u32(&bar_q_free[qb]), ((kk >> 1) - 1) & 1, abort_flag);
@@ -378,8 +382,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * nck));
         __syncwarp();
         if (lane < nbox) {
-          const uint32_t dst = smem_u32(sKV + st * kStage + lane * box * 128);
-          for (int c = 0; c < nck; ++c) tma_load_2d(dst + c * kChunk, kvmap, (int)(4 * h + c) * 64, y, full);
+          // the box's rows (whole 8-token groups) and this CTA's chunks in one copy
+          tma_load_4d(smem_u32(sKV + st * kStage + lane * (box >> 3) * nck * 1024), kvmap, 0, 0, (int)(4 * h), y >> 3,
+                      full);
         }
         issued = gi + 1;
         // L2 prefetch of the tile kLook - 1 places ahead: a box's rows are contiguous
@@ -431,8 +436,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, false);
       // Base descriptors; the start-address field is the low 14 bits (address >> 4),
       // so a constant byte offset is added as (offset >> 4) without carries.
-      const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, 1024);        // keys, K-major
-      const uint64_t vA0 = desc_sw128(smem_u32(sKV), kChunk, 1024);    // values, MN-major
+      const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, nck * 1024);      // keys, K-major
+      const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, nck * 1024);    // values, MN-major
       const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
       const uint64_t pB0 = desc_sw128(smem_u32(sP), 16, 1024);         // P^T, K-major
       const bool qk_role = warp == 1;
@@ -456,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               if (c >= nck) break;
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_ss(d, kA0 + (uint64_t)((sb * kStage + c * kChunk + k * 32) >> 4),
+                mma_ss(d, kA0 + (uint64_t)((sb * kStage + c * 1024 + k * 32) >> 4),
                        qB0 + (uint64_t)((qb * kQBuf + c * kQChunk + k * 32) >> 4), idesc_qk, (c | k) != 0);
             }
             mma_commit(smem_u32(&bar_s_full[sb]));
@@ -475,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * kChunk + ks * 2048) >> 4);
+                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * nck * 1024) >> 4);
                 const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + (ks >> 2) * kPChunk + (ks & 3) * 32) >> 4);
                 mma_ss(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
               }
@@ -693,8 +698,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStage);
           const int tail = kTok - ntok;
           for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
-            const int cch = e / (tail * 8), rem = e % (tail * 8);
-            v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            const int cch = e / (tail * 8), rem = e % (tail * 8), t = ntok + rem / 8;
+            v[((t >> 3) * nck * 1024 + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async();
@@ -951,7 +956,7 @@ bool fh_supported(const DecodeArgs& a, int sm_count) {
   if (!(a.P % kTok == 0 || (kTok % a.P == 0 && a.P % 8 == 0))) return false;
   if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
   if ((int64_t)a.B * a.R < kRp || (int64_t)a.B * a.R > INT32_MAX) return false;   // Q box of 16 rows
-  if (a.pool_rows > INT32_MAX) return false;
+  if (a.pool_rows > INT32_MAX || a.pool_rows % 8 != 0) return false;   // 8-row TMA groups
   return true;
 }
 
@@ -968,9 +973,10 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   p.max_units = plan.max_units;
   p.fused = fused ? 1 : 0;
   int rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
-  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
-    rc = tma_encode_bf16_2d(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)kDK, (uint64_t)a.pool_rows, 64,
-                            (uint32_t)p.box_rows);
+  for (int hh = 0; hh < 2; ++hh)
+    for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
+      rc = tma_encode_kv_rowgroups(&p.tm_kv[hh][i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
+                                   hh ? 5u : 4u, (uint32_t)p.box_rows / 8);
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
   p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);

@@ -1030,6 +1030,20 @@ int tma_encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t
   return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
 
+int tma_encode_kv_rowgroups(CUtensorMap* m, const void* base, uint64_t rows, uint32_t chunks, uint32_t groups) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return DCPMLA_ERR_CUDA;
+  if (rows % 8 != 0) return DCPMLA_ERR_UNSUPPORTED;
+  cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)rows / 8};
+  cuuint64_t strides[3] = {(cuuint64_t)kDK * 2, 128, (cuuint64_t)kDK * 2 * 8};
+  cuuint32_t box[4] = {64, 8, chunks, groups};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
 bool tc_supported(const DecodeArgs& a) {
   // E4M3 scales arrive by 16-byte bulk copies: their pools must be 16-byte aligned
   if (a.fp8)
