@@ -368,18 +368,38 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
           break;
         const uint8_t* raw = sRaw + rs * kRawStageBytes;
         uint8_t* dst = sKV + st * kStageBytes;
-        for (int u = ct; u < nck * kTileTok * 8; u += C::kConvThreads) {
-          const int cl = u / (kTileTok * 8), rem = u % (kTileTok * 8);
-          const int t = rem >> 3, e8 = rem & 7;
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (t < ntok) {
-            const uint2 w = *reinterpret_cast<const uint2*>(raw + cl * kRawChunkBytes + t * 64 + e8 * 8);
-            o.x = e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFF));
-            o.y = e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
-            o.z = e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFF));
-            o.w = e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+        // 16 codes per item (a 16-byte load, two 16-byte stores), four items in flight
+        // per thread: the conversion is latency-bound with only two warps on it
+        constexpr int kU = 4;
+        const int n_items = nck * kTileTok * 4;
+        for (int base = ct; base < n_items; base += C::kConvThreads * kU) {
+          uint4 w[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int e = base + k * C::kConvThreads;
+            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
+            w[k] = (e < n_items && t < ntok)
+                       ? *reinterpret_cast<const uint4*>(raw + cl * kRawChunkBytes + t * 64 + e16 * 16)
+                       : make_uint4(0, 0, 0, 0);
           }
-          *reinterpret_cast<uint4*>(dst + cl * kChunkBytes + t * 128 + ((e8 ^ (t & 7)) << 4)) = o;
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int e = base + k * C::kConvThreads;
+            if (e >= n_items) break;
+            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
+            uint4 lo, hi;   // codes 0-7 and 8-15 of the item
+            lo.x = e4m3x2_to_f16x2((uint16_t)(w[k].x & 0xFFFF));
+            lo.y = e4m3x2_to_f16x2((uint16_t)(w[k].x >> 16));
+            lo.z = e4m3x2_to_f16x2((uint16_t)(w[k].y & 0xFFFF));
+            lo.w = e4m3x2_to_f16x2((uint16_t)(w[k].y >> 16));
+            hi.x = e4m3x2_to_f16x2((uint16_t)(w[k].z & 0xFFFF));
+            hi.y = e4m3x2_to_f16x2((uint16_t)(w[k].z >> 16));
+            hi.z = e4m3x2_to_f16x2((uint16_t)(w[k].w & 0xFFFF));
+            hi.w = e4m3x2_to_f16x2((uint16_t)(w[k].w >> 16));
+            uint8_t* drow = dst + cl * kChunkBytes + t * 128;
+            *reinterpret_cast<uint4*>(drow + (((2 * e16) ^ (t & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(drow + (((2 * e16 + 1) ^ (t & 7)) << 4)) = hi;
+          }
         }
         for (int t = ct; t < kTileTok; t += C::kConvThreads)
           kscale_s[st][t] = t < ntok ? reinterpret_cast<const float*>(raw + kRawScaleOff)[t] : 0.f;
