@@ -433,13 +433,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // kPvWarp issues each tile's PV once its P is written, which frees the tile's
       // stage for the next load.  A commit tracks the MMAs of the thread issuing it.
       constexpr uint32_t idesc_qk = idesc_bf16(kTok, kRp, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, true);
       // Base descriptors; the start-address field is the low 14 bits (address >> 4),
       // so a constant byte offset is added as (offset >> 4) without carries.
       const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, nck * 1024);      // keys, K-major
       const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, nck * 1024);    // values, MN-major
       const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
-      const uint64_t pB0 = desc_sw128(smem_u32(sP), 16, 1024);         // P^T, K-major
+      const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);         // P^T, MN-major (32 rows per token)
       const bool qk_role = warp == 1;
       bool ok = true;
       int gt = 0, kk = 0;                  // tiles and non-empty units so far
@@ -481,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * nck * 1024) >> 4);
-                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + (ks >> 2) * kPChunk + (ks & 3) * 32) >> 4);
+                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + ks * 1024) >> 4);
                 mma_ss(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
               }
             }
@@ -679,19 +679,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
           if (!ok) break;
         }
-        uint8_t* pbase = sP + sb * kPBuf + (tok >> 6) * kPChunk;
-        const int t64 = tok & 63;
+        // P^T is MN-major with a 64-byte swizzle: a token's 32 rows (hi 0-15, lo 16-31) are
+        // one 64-byte line, 8 tokens an atom; this thread's 8 hi and 8 lo rows are one
+        // 16-byte unit each (unit u of line t sits at u ^ ((t % 8) / 2))
+        uint32_t hp[4], lp[4];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          const float mr = m_ref[n] == -INFINITY ? 0.f : m_ref[n];   // every s is -inf then
-          const float pw = ex2_approx(s[n] - mr);
-          lt[n] += pw;
-          const uint16_t hb = bf16_bits(pw);
-          const float hf = __uint_as_float((uint32_t)hb << 16);
-          const uint16_t lb = bf16_bits(pw - hf);
-          const int row = 8 * g + n;
-          *reinterpret_cast<uint16_t*>(pbase + sw128_off(row, t64)) = hb;
-          *reinterpret_cast<uint16_t*>(pbase + sw128_off(kRp + row, t64)) = lb;
+        for (int n = 0; n < 8; n += 2) {
+          const float mr0 = m_ref[n] == -INFINITY ? 0.f : m_ref[n];   // every s is -inf then
+          const float mr1 = m_ref[n + 1] == -INFINITY ? 0.f : m_ref[n + 1];
+          const float p0 = ex2_approx(s[n] - mr0), p1 = ex2_approx(s[n + 1] - mr1);
+          lt[n] += p0;
+          lt[n + 1] += p1;
+          const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(hh);
+          hp[n >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          const __nv_bfloat162 ll = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+          lp[n >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
+        }
+        {
+          uint8_t* line = sP + sb * kPBuf + (tok >> 3) * 512 + (tok & 7) * 64;
+          const int sw = (tok & 7) >> 1;
+          *reinterpret_cast<uint4*>(line + ((g ^ sw) << 4)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+          *reinterpret_cast<uint4*>(line + (((2 + g) ^ sw) << 4)) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
         }
         if (ntok < kTok) {
           // rows past the unit's last token hold stale data: zero this CTA's V rows

@@ -290,6 +290,17 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr, uint32_t lbo,
   return d;
 }
 
+// Shared-memory matrix descriptor with 64-byte swizzle (atoms of 8 rows x 64 B).
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;        // descriptor version for the sm_100 family
+  d |= (uint64_t)4 << 61;        // swizzle: 64 B
+  return d;
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B, fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
