@@ -17,15 +17,15 @@
 // exchanged through distributed shared memory, so both CTAs hold the same
 // scores.  The latent dims a CTA owns are its half of the value dims.
 //
-// The grid is persistent: each CTA computes the same split of all (request,
-// shard) token ranges into units of equal tile count (about 16 units per
-// cluster), and cluster k takes units k, k + G, k + 2G, ...  The units of a
-// (request, shard) cut into several write fp32 partials that a small second
-// kernel merges.
+// The grid is persistent: the 128-token tiles of all (request, shard) items form one
+// sequence, and cluster k of G takes the contiguous share [T k / G, T (k + 1) / G), so
+// every cluster streams the same amount of KV with as few item switches as possible.
+// An item cut by a share boundary writes fp32 partials that a small second kernel
+// merges.
 //
 //   warp 0     TMA producer: Q^T of the unit (one 16-row box per 64-dim chunk),
-//              then 128-token KV tiles (one 2-D box per page and 64-dim chunk)
-//              into a 2-deep stage ring, and L2 prefetches of the tiles a few
+//              then 128-token KV tiles (one 4-D box per page box, all of the CTA's
+//              chunks) into a 2-deep stage ring, and L2 prefetches of the tiles a few
 //              places further on, so that the ring's loads mostly hit L2.
 //   warp 1     lane 0 issues the QK MMAs: M 128, N 16.  QK may run ahead of PV:
 //              a score buffer is free once the softmax has loaded it.
@@ -69,7 +69,6 @@ constexpr int kPChunk = 2 * kRp * 128;         // P^T chunk [32 rows (hi, lo) x 
 constexpr int kPBuf = 2 * kPChunk;             // 128 tokens
 constexpr int kXBytes = kTok * kRp * 4;        // one fp32 partial S^T tile
 constexpr int kMaxItems = 2048;                // (request, shard) pairs per launch
-constexpr int kUnitsPerCluster = 16;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kRelayWarp = 10;
 constexpr int kPvWarp = 11;
@@ -90,11 +89,10 @@ struct FhParams {
   CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
   DecodeArgs a;
   int32_t box_rows;                  // rows per TMA box: min(P, 128)
-  int32_t max_units;
-  float* ws_o;                       // [max_units, R, 512]
-  float* ws_lse;                     // [max_units, R] (base 2)
-  int32_t* ws_bad;                   // [max_units]: the unit needed a page outside the pools
-  int32_t* ws_pre;                   // [B * shard_count + 1]: first unit of each (request, shard)
+  float* ws_o;                       // [slots, R, 512]: slot item + cluster
+  float* ws_lse;                     // [slots, R] (base 2)
+  int32_t* ws_bad;                   // [slots]: the unit needed a page outside the pools
+  int32_t* ws_pre;                   // [B * shard_count + 1]: first tile of each (request, shard)
   int32_t fused;                     // 1: every unit to the workspace, merged over shards into o, lse
 };
 static_assert(sizeof(FhParams) <= 4096, "kernel parameter space");
@@ -118,36 +116,49 @@ __device__ __forceinline__ int shard_tokens(const DecodeArgs& a, int L, int r) {
   return shard_len(L, r, a.c, a.I);
 }
 
+// Work split.  All (request, shard) items' 128-token tiles form one sequence of T
+// tiles; cluster k of G takes tiles [T k / G, T (k + 1) / G), so every cluster streams
+// the same amount of KV.  A unit is the part of one item inside a cluster's share: an
+// item inside one share is written straight to the output, the others to workspace
+// slot item + k (unique: a later cluster starts at the same or a later item) and a
+// merge kernel combines them.
 struct Unit {
   int item, b, sr, r, L;
   int j0, j1, ntiles;   // shard-local token range and its 128-token tiles
-  int nch, first;       // units of the item, and the item's first unit
+  int slot;             // workspace slot of its partial
+  bool whole;           // every tile of the item: no merge
 };
 
-__device__ __forceinline__ Unit get_unit(const DecodeArgs& a, const int* pre, int nitems, int chunk_tiles,
-                                         int u) {
-  int lo = 0, hi = nitems;   // pre[lo] <= u < pre[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pre[mid] <= u) lo = mid;
-    else hi = mid;
-  }
-  Unit x;
-  x.item = lo;
-  x.b = lo / a.shard_count;
-  x.sr = lo % a.shard_count;
+__device__ __forceinline__ int fh_bound(int T, int k, int G) { return (int)((int64_t)T * k / G); }
+
+// The part of item `it` (tiles [pre[it], pre[it + 1]) of the sequence) in the share
+// [t_lo, t_hi) of cluster cl; false if they do not meet.
+__device__ __forceinline__ bool fh_unit(const DecodeArgs& a, const int* pre, int it, int t_lo, int t_hi, int cl,
+                                        Unit& x) {
+  const int s0 = pre[it], s1 = pre[it + 1];
+  const int s = max(s0, t_lo), e = min(s1, t_hi);
+  if (e <= s) return false;
+  x.item = it;
+  x.b = it / a.shard_count;
+  x.sr = it % a.shard_count;
   x.r = a.shard_begin + x.sr;
   x.L = __ldg(a.seq_lens + x.b);
   const int n = shard_tokens(a, x.L, x.r);
-  const int tiles = (n + kTok - 1) / kTok;
-  x.first = pre[lo];
-  x.nch = pre[lo + 1] - pre[lo];
-  const int tb = (u - x.first) * chunk_tiles;
-  const int te = min(tiles, tb + chunk_tiles);
-  x.ntiles = max(0, te - tb);
-  x.j0 = min(n, tb * kTok);
-  x.j1 = min(n, te * kTok);
-  return x;
+  x.j0 = (s - s0) * kTok;
+  x.j1 = min(n, (e - s0) * kTok);
+  x.ntiles = e - s;
+  x.slot = it + cl;
+  x.whole = s == s0 && e == s1;
+  return true;
+}
+
+// The cluster whose share holds tile t (T > 0).
+__device__ __forceinline__ int fh_cluster_of(int T, int t, int G) {
+  const int64_t k0 = (int64_t)t * G / T;
+  int k = (int)(k0 < G - 1 ? k0 : G - 1);
+  while (k + 1 < G && fh_bound(T, k + 1, G) <= t) ++k;
+  while (k > 0 && fh_bound(T, k, G) > t) --k;
+  return k;
 }
 
 // Byte offset of element (row, token t64) in a K-major, 128-byte-swizzled
@@ -180,7 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float lsum_s[2][2][4][8];   // [unit parity][warpgroup][quarter][row]
   __shared__ int seg_s[kThreads];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, total_s, ubad_s[2];
+  __shared__ int abort_s, ubad_s[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t h = cluster_ctarank();
@@ -211,7 +222,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 2);                  // both MMA issuers
     abort_s = 0;
-    total_s = 0;
     ubad_s[0] = ubad_s[1] = 0;
     fence_barrier_init();
   }
@@ -222,31 +232,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   // ---- work split, computed identically by every CTA ----
-  // tiles per item into sPre[item + 1], then units per item, then the prefix sum
+  // tiles per item into sPre[item + 1], then the prefix sum (each thread a segment)
+  const int seg = (nitems + kThreads - 1) / kThreads;
+  const int s0 = min(nitems, tid * seg), s1 = min(nitems, s0 + seg);
   {
-    int local = 0;
-    for (int it = tid; it < nitems; it += kThreads) {
+    int sum = 0;
+    for (int it = s0; it < s1; ++it) {
       const int b = it / a.shard_count, r = a.shard_begin + it % a.shard_count;
       const int L = __ldg(a.seq_lens + b);
       if (blockIdx.x == 0 && (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c))
         set_err(a.err, DCPMLA_DERR_LENGTH);
       const int t = (shard_tokens(a, L, r) + kTok - 1) / kTok;
       sPre[it + 1] = t;
-      local += t;
-    }
-    atomicAdd(&total_s, local);
-  }
-  __syncthreads();
-  const int chunk_tiles =
-      max(1, (int)(((int64_t)total_s + (int64_t)G * kUnitsPerCluster - 1) / ((int64_t)G * kUnitsPerCluster)));
-  const int seg = (nitems + kThreads - 1) / kThreads;
-  const int s0 = min(nitems, tid * seg), s1 = min(nitems, s0 + seg);
-  {
-    int sum = 0;
-    for (int it = s0; it < s1; ++it) {
-      const int units = max(1, (sPre[it + 1] + chunk_tiles - 1) / chunk_tiles);
-      sPre[it + 1] = units;
-      sum += units;
+      sum += t;
     }
     seg_s[tid] = sum;
   }
@@ -280,9 +278,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  const int units = sPre[nitems];
   if (blockIdx.x == 0)
     for (int it = tid; it <= nitems; it += kThreads) p.ws_pre[it] = sPre[it];
+  // this cluster's share of the tile sequence, and the items it meets
+  const int T = sPre[nitems];
+  const int t_lo = fh_bound(T, cl, G), t_hi = fh_bound(T, cl + 1, G);
+  int it_lo = 0, it_hi = -1;
+  if (t_hi > t_lo) {
+    int lo = 0, hi = nitems;   // pre[lo] <= t_lo < pre[lo + 1] (the first item holding t_lo)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sPre[mid] <= t_lo) lo = mid;
+      else hi = mid;
+    }
+    it_lo = lo;
+    hi = nitems;               // the last item starting before t_hi
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sPre[mid] < t_hi) lo = mid;
+      else hi = mid;
+    }
+    it_hi = lo;
+  }
 
   // both CTAs' barriers are initialised before either touches the other's
   cluster_arrive();
@@ -305,21 +322,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // (its raw page id, rows, offset in the page, and the tile's shard).  The tile
     // kLook - 1 places ahead is also prefetched into L2, so the ring's loads mostly
     // hit L2; no page-table read is waited on between a stage's release and its load.
-    int pu = cl, pi = 0;
+    int pu = it_lo, pi = 0;   // lookahead cursor: item, tile within its unit
     Unit px{};
-    if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
     auto skip_empty = [&]() {
-      while (pu < units && px.ntiles == 0) {
-        pu += G;
-        if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
-      }
+      while (pu <= it_hi && !fh_unit(a, sPre, pu, t_lo, t_hi, cl, px)) ++pu;
     };
     auto lookup = [&](int& g_, int& rows_, int& off_, int& sr_) {
       g_ = 0;
       rows_ = 0;
       off_ = 0;
       sr_ = 0;
-      if (pu >= units) return;
+      if (pu > it_hi) return;
       const int pt0 = px.j0 + pi * kTok;
       const int nb = (min(kTok, px.j1 - pt0) + box - 1) / box;
       sr_ = px.sr;
@@ -331,8 +344,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (++pi >= px.ntiles) {
         pi = 0;
-        pu += G;
-        if (pu < units) px = get_unit(a, sPre, nitems, chunk_tiles, pu);
+        ++pu;
         skip_empty();
       }
     };
@@ -340,9 +352,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     skip_empty();
 #pragma unroll
     for (int k = 0; k < kLook; ++k) lookup(fg[k], fr[k], fo[k], fs[k]);
-    for (int u = cl; ok && u < units; u += G) {
-      const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
-      if (x.ntiles == 0) continue;
+    for (int it = it_lo; ok && it <= it_hi; ++it) {
+      Unit x;
+      if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
       const int qb = kk & 1;
       const CUtensorMap* kvmap = &p.tm_kv[h][x.sr];
       bool okq = true;
@@ -442,10 +454,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);         // P^T, MN-major (32 rows per token)
       const bool qk_role = warp == 1;
       bool ok = true;
-      int gt = 0, kk = 0;                  // tiles and non-empty units so far
-      for (int u = cl; ok && u < units; u += G) {
-        const int ntiles = get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
-        if (ntiles == 0) continue;
+      int gt = 0, kk = 0;                  // tiles and units so far
+      for (int it = it_lo; ok && it <= it_hi; ++it) {
+        Unit x;
+        if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
+        const int ntiles = x.ntiles;
         const int qb = kk & 1, ob = kk & 1;
         if (qk_role) {
           ok = wait_bar<false>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag);
@@ -505,8 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // relay: once all softmax warps have read the peer's partial for a tile,
       // tell the peer its next partial may overwrite this CTA's exchange buffer
-      int total = 0;
-      for (int u = cl; u < units; u += G) total += get_unit(a, sPre, nitems, chunk_tiles, u).ntiles;
+      const int total = t_hi - t_lo;   // the cluster's share of tiles
       const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
       for (int gi = 0; gi < total; ++gi) {
         if (!wait_bar<false>(smem_u32(&bar_x_read), gi & 1, abort_flag)) break;
@@ -527,8 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
     bool ok = true;
     int gi = 0, kk = 0, uc = 0;
-    for (int u = cl; ok && u < units; u += G, ++uc) {
-      const Unit x = get_unit(a, sPre, nitems, chunk_tiles, u);
+    for (int it = it_lo; ok && it <= it_hi; ++it) {
+      Unit x;
+      if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
       const int ob = kk & 1;
       const int up = uc & 1;
       int qpos[8];
@@ -752,9 +765,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ltot[n] = ((lsum_s[up][g][0][n] + lsum_s[up][g][1][n]) + lsum_s[up][g][2][n]) + lsum_s[up][g][3][n];
         inv[n] = ltot[n] > 0.f ? 1.f / ltot[n] : 0.f;
       }
-      const bool direct = !p.fused && x.nch == 1;
+      const bool direct = !p.fused && x.whole;
       const bool empty_out = direct && unit_bad;
-      const int64_t orow0 = direct ? ((int64_t)x.sr * a.B + x.b) * R : (int64_t)u * R;
+      const int64_t orow0 = direct ? ((int64_t)x.sr * a.B + x.b) * R : (int64_t)x.slot * R;
       float* obase = direct ? a.o_part : p.ws_o;
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
@@ -790,7 +803,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++kk;
       }
       // a split item's units are merged by the combine kernel; it also reads this flag
-      if (!direct && h == 0 && stid == 0) p.ws_bad[u] = unit_bad ? 1 : 0;
+      if (!direct && h == 0 && stid == 0) p.ws_bad[x.slot] = unit_bad ? 1 : 0;
+      ++uc;
     }
   }
 
@@ -806,52 +820,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
 }
 
-// Merge of the units of each (request, shard) cut into several: one block per
-// (item, query row), 128 threads x 4 value dims.  The exact LSE merge of split
-// partials (base 2): lse = log2 sum_k 2^lse_k, o = sum_k 2^(lse_k - lse) o_k; an
-// item any unit of which needed a bad page is written as empty.
-__global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
+// Merge of the (request, shard) items split between clusters: one block per (item,
+// query row), 128 threads x 4 value dims.  The exact LSE merge of the partials (base 2):
+// lse = log2 sum_k 2^lse_k, o = sum_k 2^(lse_k - lse) o_k.  An item with no tiles (an
+// empty shard or a rejected length) is written as empty, and so is one any partial of
+// which needed a bad page; an item inside one cluster's share was written by the decode.
+// `pre` is the tile prefix over items; clusters with an empty share (more clusters
+// than tiles) hold no partial.
+__global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, const int32_t* __restrict__ pre, int G,
                                                          const float* __restrict__ ws_o,
                                                          const float* __restrict__ ws_lse,
                                                          const int32_t* __restrict__ ws_bad) {
   const int item = blockIdx.x, row = blockIdx.y, t = threadIdx.x;
-  const int first = pre[item], nch = pre[item + 1] - first;
-  if (nch <= 1) return;
+  const int nitems = a.B * a.shard_count;
+  const int T = pre[nitems], s0 = pre[item], s1 = pre[item + 1];
   const int64_t R = a.R;
+  int k0 = 0, k1 = -1;
+  if (s1 > s0) {
+    k0 = fh_cluster_of(T, s0, G);
+    k1 = fh_cluster_of(T, s1 - 1, G);
+    if (k0 == k1) return;
+  }
   bool bad = false;
   float m = -INFINITY;
-  for (int k = 0; k < nch; ++k) {
-    bad |= ws_bad[first + k] != 0;
-    m = fmaxf(m, ws_lse[(int64_t)(first + k) * R + row]);
+  for (int k = k0; k <= k1; ++k) {
+    if (fh_bound(T, k, G) == fh_bound(T, k + 1, G)) continue;
+    bad |= ws_bad[item + k] != 0;
+    m = fmaxf(m, ws_lse[(int64_t)(item + k) * R + row]);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lse2 = -INFINITY;
   if (!bad && m != -INFINITY) {
     float sum = 0.f;
-    for (int k = 0; k < nch; ++k) sum += exp2f(ws_lse[(int64_t)(first + k) * R + row] - m);
+    for (int k = k0; k <= k1; ++k)
+      if (fh_bound(T, k, G) != fh_bound(T, k + 1, G)) sum += exp2f(ws_lse[(int64_t)(item + k) * R + row] - m);
     lse2 = m + log2f(sum);
-    const float4* src = reinterpret_cast<const float4*>(ws_o + ((int64_t)first * R + row) * kDL) + t;
-    const int64_t step = R * (kDL / 4);
-    int k = 0;
-    for (; k + 4 <= nch; k += 4) {
-      float w[4];
-      float4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        w[j] = exp2f(ws_lse[(int64_t)(first + k + j) * R + row] - lse2);
-        v[j] = __ldcs(src + (k + j) * step);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc.x = fmaf(w[j], v[j].x, acc.x);
-        acc.y = fmaf(w[j], v[j].y, acc.y);
-        acc.z = fmaf(w[j], v[j].z, acc.z);
-        acc.w = fmaf(w[j], v[j].w, acc.w);
-      }
-    }
-    for (; k < nch; ++k) {
-      const float w = exp2f(ws_lse[(int64_t)(first + k) * R + row] - lse2);
-      const float4 v = __ldcs(src + k * step);
+    for (int k = k0; k <= k1; ++k) {
+      if (fh_bound(T, k, G) == fh_bound(T, k + 1, G)) continue;
+      const float w = exp2f(ws_lse[(int64_t)(item + k) * R + row] - lse2);
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(ws_o + ((int64_t)(item + k) * R + row) * kDL) + t);
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -864,80 +871,61 @@ __global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, con
   if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
 }
 
-// Fused decode + merge: one block per (request, query row) merges the partials of
-// every unit of every shard of the request (SGLang DCP docs, MLA decode dataflow:
-// the exact LSE merge; the split partials of one shard merge the same way), in
-// base 2, into o [B, R, 512] and lse [B, R] (base converted at the end).  A shard
-// any unit of which needed a bad page is left out, as the unfused path writes it
-// as empty (lse = -inf).
-__global__ void __launch_bounds__(32) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
+// Fused decode + merge: one block per (request, query row, quarter of the value dims)
+// merges the partials of every unit of every shard of the request (SGLang DCP docs,
+// MLA decode dataflow: the exact LSE merge; the partials of a split shard merge the
+// same way), in base 2, into o [B, R, 512] and lse [B, R] (base converted at the end).
+// A shard any unit of which needed a bad page is left out, as the unfused path writes
+// it as empty (lse = -inf).
+__global__ void __launch_bounds__(32) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre, int G,
                                                           const float* __restrict__ ws_o,
                                                           const float* __restrict__ ws_lse,
                                                           const int32_t* __restrict__ ws_bad) {
-  // block (b, row, quarter): 32 threads x 4 dims = a quarter of the 512 value dims
   const int b = blockIdx.x, row = blockIdx.y, t = blockIdx.z * 32 + threadIdx.x;
   const int64_t R = a.R;
+  const int nitems = a.B * a.shard_count;
+  const int T = pre[nitems];
   float m = -INFINITY;
-  for (int sr = 0; sr < a.shard_count; ++sr) {
-    const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
-    bool bad = false;
-    for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
-    if (bad) continue;
-    for (int k = 0; k < nch; ++k) m = fmaxf(m, ws_lse[(int64_t)(first + k) * R + row]);
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse2 = -INFINITY;
-  if (m != -INFINITY) {
+  for (int pass = 0; pass < 2; ++pass) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float sum = 0.f;
     for (int sr = 0; sr < a.shard_count; ++sr) {
-      const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
+      const int item = b * a.shard_count + sr, s0 = pre[item], s1 = pre[item + 1];
+      if (s1 <= s0) continue;
+      const int k0 = fh_cluster_of(T, s0, G), k1 = fh_cluster_of(T, s1 - 1, G);
       bool bad = false;
-      for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
+      for (int k = k0; k <= k1; ++k)
+        if (fh_bound(T, k, G) != fh_bound(T, k + 1, G)) bad |= ws_bad[item + k] != 0;
       if (bad) continue;
-      for (int k = 0; k < nch; ++k) sum += exp2f(ws_lse[(int64_t)(first + k) * R + row] - m);
+      for (int k = k0; k <= k1; ++k) {
+        if (fh_bound(T, k, G) == fh_bound(T, k + 1, G)) continue;
+        const float lk = ws_lse[(int64_t)(item + k) * R + row];
+        if (pass == 0) {
+          m = fmaxf(m, lk);
+        } else if (m != -INFINITY) {
+          const float w = exp2f(lk - m);
+          sum += w;
+          const float4 v = __ldcs(reinterpret_cast<const float4*>(ws_o + ((int64_t)(item + k) * R + row) * kDL) + t);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
     }
-    lse2 = m + log2f(sum);
-    for (int sr = 0; sr < a.shard_count; ++sr) {
-      const int item = b * a.shard_count + sr, first = pre[item], nch = pre[item + 1] - first;
-      bool bad = false;
-      for (int k = 0; k < nch; ++k) bad |= ws_bad[first + k] != 0;
-      if (bad) continue;
-      const float4* src = reinterpret_cast<const float4*>(ws_o + ((int64_t)first * R + row) * kDL) + t;
-      const int64_t step = R * (kDL / 4);
-      int k = 0;
-      for (; k + 4 <= nch; k += 4) {       // four partials' loads in flight
-        float w[4];
-        float4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          w[j] = exp2f(ws_lse[(int64_t)(first + k + j) * R + row] - lse2);
-          v[j] = __ldcs(src + (k + j) * step);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc.x = fmaf(w[j], v[j].x, acc.x);
-          acc.y = fmaf(w[j], v[j].y, acc.y);
-          acc.z = fmaf(w[j], v[j].z, acc.z);
-          acc.w = fmaf(w[j], v[j].w, acc.w);
-        }
-      }
-      for (; k < nch; ++k) {
-        const float w = exp2f(ws_lse[(int64_t)(first + k) * R + row] - lse2);
-        const float4 v = __ldcs(src + k * step);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
+    if (pass == 1) {
+      const float inv = sum > 0.f ? 1.f / sum : 0.f;
+      const float lse2 = sum > 0.f ? m + log2f(sum) : -INFINITY;
+      const int64_t orow = (int64_t)b * R + row;
+      reinterpret_cast<float4*>(a.o_part + orow * kDL)[t] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
     }
   }
-  const int64_t orow = (int64_t)b * R + row;
-  reinterpret_cast<float4*>(a.o_part + orow * kDL)[t] = acc;
-  if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
 }
 
 struct FhPlan {
-  int32_t clusters, max_units;
+  int32_t clusters, slots;
   size_t pre_off, bad_off, lse_off, o_off, bytes;
 };
 
@@ -947,13 +935,12 @@ FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
   FhPlan p{};
   p.clusters = std::max(1, sm_count / 2);
   const int64_t items = (int64_t)a.B * a.shard_count;
-  const int64_t tiles_max = std::max<int64_t>(1, ((int64_t)a.max_pages * a.P + kTok - 1) / kTok);
-  p.max_units = (int32_t)std::min<int64_t>((int64_t)p.clusters * kUnitsPerCluster + items, items * tiles_max);
+  p.slots = (int32_t)(items + p.clusters);   // partial of item it in cluster k: slot it + k
   p.pre_off = 0;
   p.bad_off = align256((size_t)(items + 1) * 4);
-  p.lse_off = p.bad_off + align256((size_t)p.max_units * 4);
-  p.o_off = p.lse_off + align256((size_t)p.max_units * a.R * 4);
-  p.bytes = p.o_off + (size_t)p.max_units * a.R * kDL * 4;
+  p.lse_off = p.bad_off + align256((size_t)p.slots * 4);
+  p.o_off = p.lse_off + align256((size_t)p.slots * a.R * 4);
+  p.bytes = p.o_off + (size_t)p.slots * a.R * kDL * 4;
   return p;
 }
 
@@ -964,6 +951,8 @@ bool fh_supported(const DecodeArgs& a, int sm_count) {
   if (a.shard_count > kMaxFhShards) return false;
   if (!(a.P % kTok == 0 || (kTok % a.P == 0 && a.P % 8 == 0))) return false;
   if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
+  // the tile sequence of all items fits 32-bit tile indices
+  if ((int64_t)a.B * a.shard_count * (((int64_t)a.max_pages * a.P + kTok - 1) / kTok) > INT32_MAX) return false;
   if ((int64_t)a.B * a.R < kRp || (int64_t)a.B * a.R > INT32_MAX) return false;   // Q box of 16 rows
   if (a.pool_rows > INT32_MAX || a.pool_rows % 8 != 0) return false;   // 8-row TMA groups
   return true;
@@ -979,7 +968,6 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   FhParams& p = *fp;
   p.a = a;
   p.box_rows = std::min(a.P, kTok);
-  p.max_units = plan.max_units;
   p.fused = fused ? 1 : 0;
   int rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
   for (int hh = 0; hh < 2; ++hh)
@@ -1001,11 +989,11 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   }
   if (rc == DCPMLA_OK && fused) {
     const dim3 grid((unsigned)a.B, (unsigned)a.R, 4);
-    fh_merge_all_kernel<<<grid, 32, 0, st>>>(a, p.ws_pre, p.ws_o, p.ws_lse, p.ws_bad);
+    fh_merge_all_kernel<<<grid, 32, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o, p.ws_lse, p.ws_bad);
     rc = launch_status();
   } else if (rc == DCPMLA_OK) {
     const dim3 grid((unsigned)(a.B * a.shard_count), (unsigned)a.R);
-    fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, p.ws_o, p.ws_lse, p.ws_bad);
+    fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o, p.ws_lse, p.ws_bad);
     rc = launch_status();
   }
   delete fp;
