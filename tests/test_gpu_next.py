@@ -142,6 +142,13 @@ def test_e4m3_quantising_append_bit_exact(I):
     x[8] = -0.0
     x[9, :] = 1e-30                                        # tiny values
     x[10, 5] = -3.0e4
+    # rows whose quotients land exactly on E4M3 rounding midpoints (scale = 1 and 2): the
+    # kernel's fast reciprocal path must hand these to the correctly rounded division
+    mids = torch.tensor([1.0625, -1.1875, 2.125, 0.28125, -0.0068359375, 13.0, 104.0, 432.0])
+    x[11, :] = mids.repeat(O.D_K // len(mids))
+    x[11, 0] = 448.0
+    x[12, :] = 2.0 * mids.repeat(O.D_K // len(mids))
+    x[12, 1] = -896.0
     rows = x.to(torch.bfloat16)
     pages = 40
     pools = [torch.full((pages * P, O.D_K), SENT, dtype=torch.uint8, device="cuda") for _ in range(c)]
