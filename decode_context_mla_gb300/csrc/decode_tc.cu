@@ -9,28 +9,30 @@
 // over the 576-d key, values over the 512-d latent.
 //
 // One CLUSTER of two CTAs = (request b, shard r, KV split, 128 query rows).
-// The key dims are split between the pair: CTA h = 0 owns dims [0, 256), CTA
-// h = 1 owns [256, 576) (latent 256..511 plus the 64 rope dims).  Each CTA
-// streams only its dims of every KV row, computes a partial score tile over
-// them, and the two partials are summed after an exchange through
-// distributed shared memory.  The latent dims a CTA owns are also its half
-// of the value dims, so O += P V needs no further data.  Both CTAs form the
-// same sum in the same order, so both see bit-identical scores and softmax.
+// The key dims are split between the pair, each CTA streams only its dims of
+// every KV row, computes a partial score tile over them, and the two partials
+// are summed after an exchange through distributed shared memory.  The latent
+// dims a CTA owns are also its half of the value dims, so O += P V needs no
+// further data.  Both CTAs form the same sum in the same order, so both see
+// bit-identical scores and softmax.  Online softmax is base 2 with a lazily
+// moved reference max (O is rescaled only when a tile's max exceeds it by more
+// than 8); the epilogue normalises O_h and writes it.
 //
-//   warp 0     TMA producer: 64-token KV tiles of this CTA's dims (4 or 5
-//              column chunks of 64 bf16, 128-byte swizzle) into the stage ring.
-//   warp 1     allocates TMEM; one thread issues the MMAs:
-//                S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; Q_h latent dims from TMEM)
-//                O_h += P V_h     (M 128, N 256, K 64; P from TMEM as a bf16 hi + lo
-//                                 pair, V MN-major)
-//   warps 2-9  softmax, two warpgroups; a query row's 64 tile columns are split
-//              between one thread of each: read S_h from TMEM, st.async it
-//              into the peer's exchange buffer, add the peer's partial, online
-//              softmax in base 2 with a lazily moved reference max (O is
-//              rescaled only when a tile's max exceeds it by more than 8),
-//              P back to TMEM; epilogue normalises O_h and writes it.
+// Two kernels share this plan:
+//   decode_tc_bf16_kernel   bf16 KV; CTA h owns latent dims [256h, 256h+256) and
+//                           rope dims [512+32h, 544+32h); three S/P tiles in TMEM
+//                           (layout and warp roles at decode_tc_bf16_body)
+//   decode_tc_e4m3_kernel   E4M3 KV with per-token scales; CTA 0 owns dims
+//                           [0, 256), CTA 1 [256, 576); codes are converted to
+//                           fp16 stages and all MMAs run in fp16:
+//     warp 0     TMA producer: raw 64-token tiles of this CTA's codes and scales
+//     warp 1     allocates TMEM; one thread issues the MMAs:
+//                  S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; Q_h latent dims from TMEM)
+//                  O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
+//     warps 2-9  softmax, two warpgroups on every tile, each 32 of its columns
+//     warps 10-11  E4M3 -> fp16 conversion into the stage ring
+//   TMEM columns: O_h [0,256), S/P double buffer [256,384), Q_h latent [384,512).
 //
-// TMEM columns: O_h [0,256), S/P double buffer [256,384), Q_h latent [384,512).
 // Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all
 // roles drain, both CTAs meet at the final cluster barrier, TMEM is freed.
 #include <cudaTypedefs.h>
@@ -83,6 +85,7 @@ struct TcParams {
   CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
                                       // E4M3 pool as [pool_rows, 576] bytes, box {64, box_rows}
   CUtensorMap tm_kv3[kMaxTcShards];   // bf16 pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
+  CUtensorMap tm_rope[kMaxTcShards];  // bf16 pool as [pool_rows, 576], box {32, box_rows}, 64-byte swizzle
   DecodeArgs a;
   int32_t box_rows;                   // rows per TMA box: min(P, 64)
   int32_t use3d;                      // 1: one 3-D box per 4 chunks (bf16, needs box_rows == 64)
@@ -116,6 +119,108 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 }
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// The last CTA of a split group merges the group's partials (exact LSE merge, base 2).
+// Unfused: the 2 * num_splits CTAs of (b, r, row tile), into o_part.  Fused: the
+// 2 * shard_count * num_splits CTAs of (b, row tile), every shard and split of the
+// request, straight into o = o_part [B, R, 512] and lse = lse_part.  `scratch` is
+// idle shared memory of `scratch_bytes`; `last_s` a shared flag.
+template <int kThreads>
+__device__ __noinline__ void tc_combine_tail(const TcParams& p, int b, int bz, int sr, int rt, uint8_t* scratch,
+                                             size_t scratch_bytes, int* last_s) {
+  const DecodeArgs& a = p.a;
+  const int64_t R = a.R;
+  const int tid = threadIdx.x;
+  __threadfence();
+  __syncthreads();
+  const int nparts = p.fused ? a.shard_count * p.num_splits : p.num_splits;
+  if (tid == 0) {
+    const int64_t ci = p.fused ? (int64_t)b * p.row_tiles + rt : (int64_t)bz * p.row_tiles + rt;
+    const uint32_t prev = atomicAdd(p.ws_cnt + ci, 1u);
+    *last_s = prev == (uint32_t)(2 * nparts - 1);
+  }
+  __syncthreads();
+  if (!*last_s) return;
+  __threadfence();
+  // partial k of this group's row: k * kstride + base.  The stage buffers are idle
+  // now (MMAs drained, peer past the cluster barrier): each row's merge weights go
+  // there once, then the partial rows stream through in float4s.
+  const int64_t kstride = p.fused ? (int64_t)a.B * R : (int64_t)a.B * a.shard_count * R;
+  const int rows_here = (int)min((long long)kRows, (long long)(R - (int64_t)rt * kRows));
+  const int64_t base0 = (p.fused ? (int64_t)b * R : (int64_t)bz * R) + (int64_t)rt * kRows;
+  float* wts = reinterpret_cast<float*>(scratch);            // [nparts][kRows]
+  float* lse_s = wts + (size_t)nparts * kRows;           // [kRows]
+  const bool fits = (size_t)(nparts + 1) * kRows * 4 <= scratch_bytes;
+  if (fits) {
+    for (int rr = tid; rr < rows_here; rr += kThreads) {
+      float m = -INFINITY;
+      for (int k = 0; k < nparts; ++k) m = fmaxf(m, __ldcg(p.ws_lse + k * kstride + base0 + rr));
+      float lse2 = -INFINITY;
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int k = 0; k < nparts; ++k) sum += exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - m);
+        lse2 = m + log2f(sum);
+      }
+      for (int k = 0; k < nparts; ++k)
+        wts[k * kRows + rr] =
+            lse2 == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - lse2);
+      lse_s[rr] = lse2;
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < rows_here * (kDL / 4); e += kThreads) {
+    const int rrow = e / (kDL / 4), d4 = e % (kDL / 4);
+    const int64_t base = base0 + rrow;
+    float lse2 = -INFINITY;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (fits) {
+      lse2 = lse_s[rrow];
+      const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * kDL) + d4;
+      const int64_t step = kstride * (kDL / 4);
+      int k = 0;
+      for (; k + 4 <= nparts; k += 4) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + (k + j) * step);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float w = wts[(k + j) * kRows + rrow];
+          acc.x = fmaf(w, v[j].x, acc.x);
+          acc.y = fmaf(w, v[j].y, acc.y);
+          acc.z = fmaf(w, v[j].z, acc.z);
+          acc.w = fmaf(w, v[j].w, acc.w);
+        }
+      }
+      for (; k < nparts; ++k) {
+        const float4 v = __ldcg(src + k * step);
+        const float w = wts[k * kRows + rrow];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    } else {
+      float m = -INFINITY;
+      for (int s = 0; s < nparts; ++s) m = fmaxf(m, __ldcg(p.ws_lse + s * kstride + base));
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int s = 0; s < nparts; ++s) sum += exp2f(__ldcg(p.ws_lse + s * kstride + base) - m);
+        lse2 = m + log2f(sum);
+        for (int s = 0; s < nparts; ++s) {
+          const float w = exp2f(__ldcg(p.ws_lse + s * kstride + base) - lse2);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * kstride + base) * kDL) + d4);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+    }
+    const int64_t orow = p.fused ? base : ((int64_t)sr * a.B + b) * R + (int64_t)rt * kRows + rrow;
+    reinterpret_cast<float4*>(a.o_part + orow * kDL)[d4] = acc;
+    if (d4 == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
+  }
 }
 
 template <bool kFp8>
@@ -827,104 +932,514 @@ __device__ __forceinline__ void decode_tc_body(const TcParams& p) {
   if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
   if (p.num_splits == 1 && !p.fused) return;
 
-  // ---- combine: the last CTA of a group merges the group's partials (exact LSE merge,
-  // base 2).  Unfused: the 2 * num_splits CTAs of (b, r, row tile), into o_part.
-  // Fused: the 2 * shard_count * num_splits CTAs of (b, row tile), every shard and
-  // split of the request, straight into o = o_part [B, R, 512] and lse = lse_part.
-  __threadfence();
-  __syncthreads();
-  const int nparts = p.fused ? a.shard_count * p.num_splits : p.num_splits;
-  if (tid == 0) {
-    const int64_t ci = p.fused ? (int64_t)b * p.row_tiles + rt : (int64_t)bz * p.row_tiles + rt;
-    const uint32_t prev = atomicAdd(p.ws_cnt + ci, 1u);
-    last_s = prev == (uint32_t)(2 * nparts - 1);
-  }
-  __syncthreads();
-  if (!last_s) return;
-  __threadfence();
-  // partial k of this group's row: k * kstride + base.  The stage buffers are idle
-  // now (MMAs drained, peer past the cluster barrier): each row's merge weights go
-  // there once, then the partial rows stream through in float4s.
-  const int64_t kstride = p.fused ? (int64_t)a.B * R : (int64_t)a.B * a.shard_count * R;
-  const int rows_here = (int)min((long long)kRows, (long long)(R - (int64_t)rt * kRows));
-  const int64_t base0 = (p.fused ? (int64_t)b * R : (int64_t)bz * R) + (int64_t)rt * kRows;
-  float* wts = reinterpret_cast<float*>(sKV);            // [nparts][kRows]
-  float* lse_s = wts + (size_t)nparts * kRows;           // [kRows]
-  const bool fits = (size_t)(nparts + 1) * kRows * 4 <= (size_t)kStages * kStageBytes;
-  if (fits) {
-    for (int rr = tid; rr < rows_here; rr += kThreads) {
-      float m = -INFINITY;
-      for (int k = 0; k < nparts; ++k) m = fmaxf(m, __ldcg(p.ws_lse + k * kstride + base0 + rr));
-      float lse2 = -INFINITY;
-      if (m != -INFINITY) {
-        float sum = 0.f;
-        for (int k = 0; k < nparts; ++k) sum += exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - m);
-        lse2 = m + log2f(sum);
-      }
-      for (int k = 0; k < nparts; ++k)
-        wts[k * kRows + rr] =
-            lse2 == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + k * kstride + base0 + rr) - lse2);
-      lse_s[rr] = lse2;
-    }
-    __syncthreads();
-  }
-  for (int e = tid; e < rows_here * (kDL / 4); e += kThreads) {
-    const int rrow = e / (kDL / 4), d4 = e % (kDL / 4);
-    const int64_t base = base0 + rrow;
-    float lse2 = -INFINITY;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (fits) {
-      lse2 = lse_s[rrow];
-      const float4* src = reinterpret_cast<const float4*>(p.ws_o + base * kDL) + d4;
-      const int64_t step = kstride * (kDL / 4);
-      int k = 0;
-      for (; k + 4 <= nparts; k += 4) {
-        float4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = __ldcg(src + (k + j) * step);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float w = wts[(k + j) * kRows + rrow];
-          acc.x = fmaf(w, v[j].x, acc.x);
-          acc.y = fmaf(w, v[j].y, acc.y);
-          acc.z = fmaf(w, v[j].z, acc.z);
-          acc.w = fmaf(w, v[j].w, acc.w);
-        }
-      }
-      for (; k < nparts; ++k) {
-        const float4 v = __ldcg(src + k * step);
-        const float w = wts[k * kRows + rrow];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-      }
-    } else {
-      float m = -INFINITY;
-      for (int s = 0; s < nparts; ++s) m = fmaxf(m, __ldcg(p.ws_lse + s * kstride + base));
-      if (m != -INFINITY) {
-        float sum = 0.f;
-        for (int s = 0; s < nparts; ++s) sum += exp2f(__ldcg(p.ws_lse + s * kstride + base) - m);
-        lse2 = m + log2f(sum);
-        for (int s = 0; s < nparts; ++s) {
-          const float w = exp2f(__ldcg(p.ws_lse + s * kstride + base) - lse2);
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (s * kstride + base) * kDL) + d4);
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
-        }
-      }
-    }
-    const int64_t orow = p.fused ? base : ((int64_t)sr * a.B + b) * R + (int64_t)rt * kRows + rrow;
-    reinterpret_cast<float4*>(a.o_part + orow * kDL)[d4] = acc;
-    if (d4 == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
-  }
+  tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStageBytes, &last_s);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<false>::kThreads, 1)
+// ------------------------------------------------------------ bf16 KV, three S/P slots
+// The bf16 kernel keeps three score/probability tiles in TMEM, so QK of tile i + 2
+// never waits for PV of tile i (P overwrites its own scores in place).  The TMEM
+// budget for that comes from Q: only 128 of a CTA's query dims stay in TMEM, the
+// other 128 latent dims and its 32 rope dims are MMA operands in shared memory.
+// The 64 rope dims are split 32 / 32 between the pair, so both CTAs stream 288 of
+// the 576 key dims (a 36 KB stage).
+//
+//   warp 0      TMA producer; looks page ids up kLook tiles ahead and prefetches the
+//               tile kLook - 1 places ahead into L2 (each CTA half of its rows)
+//   warp 1      TMEM allocation; lane 0 issues QK of every tile
+//   warps 2-9   softmax, warpgroup g takes tiles i with i % 2 == g
+//   warp 10     lane 0 issues PV of every tile
+//   warp 11     lane 0 relays "exchange buffer read" to the peer
+//
+// TMEM columns: O_h [0,256), S/P slots [256,448) (3 x 64), Q_h dims [256h, 256h+128) [448,512).
+namespace b16 {
+constexpr int kStages = 3;                          // KV stages = S/P slots: tile i uses i % 3
+constexpr int kChunk = kTileTok * 128;              // 64 tokens x 64 dims, 128-byte swizzle
+constexpr int kRopeOff = 4 * kChunk;                // then 64 tokens x 32 rope dims, 64-byte swizzle
+constexpr int kStage = kRopeOff + kTileTok * 64;    // 36 KB
+constexpr int kQChunk = kRows * 128;                // Q in shared memory: 2 latent chunks
+constexpr int kQRopeOff = 2 * kQChunk;              // then 128 rows x 32 rope dims, 64-byte swizzle
+constexpr int kQBytes = kQRopeOff + kRows * 64;
+constexpr int kThreads = 384;
+constexpr int kLook = 4;
+constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * kStage + 2 * kXBytes;
+constexpr uint32_t kColO3 = 0, kColS3 = 256, kColQ3 = 448;
+static_assert(kSmemBytes <= 227 * 1024 - 4096, "stages, Q and exchange buffers exceed shared memory");
+}  // namespace b16
+
+__device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
+  using namespace b16;
+  const DecodeArgs& a = p.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                                    // Q dims [256h+128, 256h+256) + rope piece
+  uint8_t* sKV = sQ + kQBytes;                           // kStages x kStage
+  uint8_t* sX = sKV + kStages * kStage;                  // the peer's partial scores, per warpgroup
+  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full[kStages], bar_p_full[kStages];
+  __shared__ uint64_t bar_o_par[2], bar_mref[2], bar_x_full[2], bar_x_empty[2], bar_x_read[2];
+  __shared__ uint64_t bar_q_full, bar_o_full, bar_drain_qk, bar_drain_pv, bar_l;
+  __shared__ float mref_s[2][kRows];                     // a warpgroup's reference max after its tile
+  __shared__ float l_s[2][kRows], m_s[2][kRows];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s, bad_s, last_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
+  const uint32_t peer = h ^ 1u;
+  const int split = blockIdx.x >> 1, rt = blockIdx.y, bz = blockIdx.z;
+  const int b = bz / a.shard_count, sr = bz % a.shard_count, r = a.shard_begin + sr;
+  const int L = a.seq_lens[b];
+  const int64_t R = a.R;
+  const int32_t* pt_row = a.pt + (int64_t)b * a.max_pages;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+      mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_p_full[s]), kWgThreads);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_o_par[s]), 1);
+      mbar_init(smem_u32(&bar_mref[s]), kWgThreads);
+      mbar_init(smem_u32(&bar_x_full[s]), 1);
+      mbar_init(smem_u32(&bar_x_empty[s]), 1);                 // the peer's relay thread
+      mbar_init(smem_u32(&bar_x_read[s]), kWgThreads);
+    }
+    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_o_full), 1);
+    mbar_init(smem_u32(&bar_drain_qk), 1);
+    mbar_init(smem_u32(&bar_drain_pv), 1);
+    mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
+    abort_s = 0;
+    bad_s = 0;
+    last_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  int j0 = 0, j1 = 0;
+  if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
+    if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
+  } else {
+    const int n = shard_len(L, r, a.c, a.I);
+    j0 = min(split * p.chunk, n);
+    j1 = min(n, j0 + p.chunk);
+    const int npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
+    for (int pg = tid; pg < npages; pg += kThreads) {
+      const int32_t g = pt_row[pg];
+      if (g < 0 || (int64_t)g >= a.num_pages) atomicOr(&bad_s, DCPMLA_DERR_PAGE);
+    }
+  }
+  __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  if (bad_s) {
+    if (tid == 0) set_err(a.err, bad_s);
+    j1 = j0;
+  }
+  const int ntiles = (j1 - j0 + kTileTok - 1) / kTileTok;
+  volatile int* abort_flag = &abort_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    // Lane l loads box l of a tile (box = min(P, 64) rows); the page id of box l of
+    // tile i + k sits in fg[k], so no page-table read is waited on between a stage's
+    // release and its load.  Every page id was range-checked above.
+    if (ntiles > 0) {
+      const CUtensorMap* kvmap = &p.tm_kv[sr];
+      const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
+      const CUtensorMap* ropemap = &p.tm_rope[sr];
+      if (lane == 0) {
+        prefetch_tmap(kvmap);
+        prefetch_tmap(ropemap);
+        if (p.use3d) prefetch_tmap(kvmap3);
+      }
+      const int box = p.box_rows;
+      const uint8_t* pool = static_cast<const uint8_t*>(a.kv.pool[r]);
+      auto lookup = [&](int tile) -> int {
+        if (tile >= ntiles) return -1;
+        const int t0 = j0 + tile * kTileTok;
+        const int nb = (min(kTileTok, j1 - t0) + box - 1) / box;
+        return lane < nb ? __ldg(pt_row + (t0 + lane * box) / a.P) : -1;
+      };
+      int fg[kLook];
+#pragma unroll
+      for (int k = 0; k < kLook; ++k) fg[k] = lookup(k);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages) {
+          bool okw = true;
+          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
+        }
+        const int t0 = j0 + i * kTileTok;
+        const int nbox = (min(kTileTok, j1 - t0) + box - 1) / box;
+        const uint32_t full = smem_u32(&bar_kv_full[st]);
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (4 * 128 + 64)));
+        __syncwarp();
+        if (lane < nbox) {
+          const int tok = t0 + lane * box;
+          const int y = fg[0] * a.P + tok % a.P;
+          const uint32_t dst = smem_u32(sKV + st * kStage);
+          if (p.use3d) {
+            tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
+          } else {
+            for (int cl = 0; cl < 4; ++cl)
+              tma_load_2d(dst + cl * kChunk + lane * box * 128, kvmap, (int)(4 * h + cl) * 64, y, full);
+          }
+          tma_load_2d(dst + kRopeOff + lane * box * 64, ropemap, 512 + 32 * (int)h, y, full);
+        }
+        issued = i + 1;
+        // L2 prefetch of the tile kLook - 1 places ahead: a box's rows are contiguous
+        // in the pool, and each CTA of the pair prefetches half of them
+        if (fg[kLook - 1] >= 0) {
+          const int tok = j0 + (i + kLook - 1) * kTileTok + lane * box;
+          const uint32_t half = (uint32_t)min(box, j1 - tok) * (kDK * 2 / 2);   // a multiple of 16 bytes
+          bulk_prefetch_l2(pool + ((int64_t)fg[kLook - 1] * a.P + tok % a.P) * (kDK * 2) + h * half, half);
+        }
+#pragma unroll
+        for (int k = 0; k + 1 < kLook; ++k) fg[k] = fg[k + 1];
+        fg[kLook - 1] = lookup(i + kLook);
+      }
+      if (lane == 0 && *abort_flag) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
+                 clock64() - t0 < kWaitCycles / 8) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ QK issuer
+    // S(i) = Q_h K_h(i)^T into slot i % 3: dims [256h, 256h+128) with Q from TMEM,
+    // [256h+128, 256h+256) and the rope piece with Q from shared memory.  The slot
+    // is free once tile i - 3's PV completed, which its stage's release implies.
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
+      const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
+      const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
+      const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
+      const uint32_t tq = tmem + kColQ3;
+      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
+      tc_fence_after();
+      for (int i = 0; ok && i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + kColS3 + st * kTileTok;
+        const uint64_t so = (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+        for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(d, tq + cl * 32 + k * 8, kd0 + so + ((cl * kChunk + k * 32) >> 4), idesc_qk, (cl | k) != 0);
+#pragma unroll
+        for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(d, qd0 + ((cl * kQChunk + k * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + k * 32) >> 4),
+                   idesc_qk, 1u);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) mma_ss(d, qr0 + ((k * 32) >> 4), kr0 + so + ((k * 32) >> 4), idesc_qk, 1u);
+        mma_commit(smem_u32(&bar_s_full[st]));
+      }
+      // drain: every MMA issued above completes before TMEM is released
+      mma_commit(smem_u32(&bar_drain_qk));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ PV issuer
+    // O_h += P(i) V_h(i), P as a bf16 hi + lo pair from slot i % 3 (hi columns 0-31,
+    // lo 32-63), V MN-major from the stage's four latent chunks.
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
+      const uint32_t to = tmem + kColO3;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (!wait_bar<false>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
+        const uint32_t pa = tmem + kColS3 + st * kTileTok;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bar_kv_empty[st]));
+        mma_commit(smem_u32(&bar_o_par[i & 1]));
+        if (i == ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // O complete
+      }
+      mma_commit(smem_u32(&bar_drain_pv));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+  } else if (warp == 11) {
+    // ---------------------------------------------------------------- relay
+    // once all of a warpgroup's threads have read the peer's partial for a tile, tell
+    // the peer its next partial may overwrite that exchange buffer
+    if (lane == 0) {
+      for (int i = 0; i < ntiles; ++i) {
+        if (!wait_bar<false>(smem_u32(&bar_x_read[i & 1]), (i >> 1) & 1, abort_flag)) break;
+        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[i & 1]), peer));
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    // Warpgroup g (warps 2-5, 6-9) takes tiles i with i % 2 == g, each thread one
+    // query row (TMEM lane quarter = warp % 4) over all 64 columns of the tile.
+    const int g = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
+    const bool real = grow < R;                              // rows past R pad the tile
+    // Shard positions grow with the shard-local index, so the keys a query sees form a
+    // prefix: shard-local tokens below shard_len(qpos + 1) (those at positions <= qpos),
+    // and below j1.  jvis: this row's prefix; jvis_min: every row's (the earliest query).
+    const int jvis = min(j1, shard_len(L - a.Tq + (int)(grow / a.H) + 1, r, a.c, a.I));
+    const int jvis_min = min(j1, shard_len(L - a.Tq + 1, r, a.c, a.I));
+    const float qscale = a.sm_scale * kLog2e;
+    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
+    // this warpgroup's partial sum l is relative to m_own (the reference max at its
+    // last tile); the current reference is the latest one any warpgroup published
+    float m_own = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (ntiles > 0) {
+      const __nv_bfloat16* qrow = a.q + ((int64_t)b * R + grow) * kDK;
+      if (g == 0) {
+        // query dims [256h, 256h+128) into TMEM as packed 16-bit pairs
+        const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256);
+        for (int c16 = 0; c16 < 4; ++c16) {
+          uint32_t rr[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
+            rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
+          }
+          tmem_st16(tmem + lane_off + kColQ3 + c16 * 16, rr);
+        }
+        tmem_st_wait();
+      } else {
+        // dims [256h+128, 256h+256) as two 128-byte-swizzle chunks and the rope dims
+        // [512+32h, 544+32h) with a 64-byte swizzle, in the layouts the MMA reads
+        const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256 + 128);
+#pragma unroll
+        for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = real ? __ldg(qsrc + cl * 8 + u) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sQ + cl * kQChunk + row * 128 + ((u ^ (row & 7)) << 4)) = v;
+          }
+        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + 512 + 32 * h);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = real ? __ldg(rsrc + u) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sQ + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) = v;
+        }
+        fence_proxy_async();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_q_full));
+    }
+    for (int i = g; ok && i < ntiles; i += 2) {
+      const int st = i % kStages;
+      const int t0 = j0 + i * kTileTok;
+      const int ntok = min(kTileTok, j1 - t0);
+      const uint32_t scol = tmem + lane_off + kColS3 + st * kTileTok;
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (i / kStages) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      // send this CTA's partial into the peer's buffer g ([16 column groups][128 rows]
+      // of float4), once the peer has read what this warpgroup sent two tiles ago
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((i >> 1) - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
+      const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
+      // this CTA's partial stays in x (as bits) while it is sent and the peer's arrives
+      float x[64];
+      uint32_t* xb = reinterpret_cast<uint32_t*>(x);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld16(scol + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(xb + 16 * q));
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async_v4(x_remote + g * kXBytes + (c * kRows + row) * 16,
+                    make_uint4(xb[4 * c], xb[4 * c + 1], xb[4 * c + 2], xb[4 * c + 3]), xfull_remote);
+      if (row == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
+      ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (i >> 1) & 1, abort_flag));
+      if (!ok) break;
+      const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 pv = xin[c * kRows + row];
+        // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+        float* xx = x + 4 * c;
+        xx[0] = h ? pv.x + xx[0] : xx[0] + pv.x;
+        xx[1] = h ? pv.y + xx[1] : xx[1] + pv.y;
+        xx[2] = h ? pv.z + xx[2] : xx[2] + pv.z;
+        xx[3] = h ? pv.w + xx[3] : xx[3] + pv.w;
+      }
+      mbar_arrive(smem_u32(&bar_x_read[g]));
+      // causal / tail mask on raw scores (only tiles that need it)
+      if (t0 + kTileTok > jvis_min) {
+        const int lim = jvis - t0;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) x[k] = k < lim ? x[k] : -INFINITY;
+      }
+      float mx[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int k = 4; k < 64; ++k) mx[k & 3] = fmaxf(mx[k & 3], x[k]);
+      float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * qscale;
+      // the reference max as the previous tile (the other warpgroup's) left it
+      float m_ref = -INFINITY;
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[g ^ 1]), ((i - 1) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        m_ref = mref_s[g ^ 1][row];
+      }
+      // Lazy reference max: move it only when this tile's max exceeds it by more
+      // than 8 (so every weight 2^(x - m_ref) stays <= 256).  A row that moves it
+      // after O holds data rescales its O columns (all 256 of this CTA) once PV of
+      // tile i - 1 has completed (PV(i - 3) had, since S(i) was computed).
+      const bool move = tmax > m_ref + 8.f;
+      const bool rescale_me = move && m_ref != -INFINITY;
+      if (__any_sync(0xffffffffu, rescale_me)) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bar<false>(smem_u32(&bar_o_par[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+        for (int q = 0; q < 16; ++q) {
+          uint32_t u[16];
+          const uint32_t oc = tmem + lane_off + kColO3 + q * 16;
+          tmem_ld16(oc, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+          tmem_st16(oc, u);
+        }
+        tmem_st_wait();
+      }
+      if (move) m_ref = tmax;
+      mref_s[g][row] = m_ref;
+      mbar_arrive(smem_u32(&bar_mref[g]));
+      // this warpgroup's partial sum follows the reference
+      if (m_own != m_ref) {
+        l = m_own == -INFINITY ? 0.f : l * ex2_approx(m_own - m_ref);
+        m_own = m_ref;
+      }
+      const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
+      float ps = 0.f;
+      // P as a bf16 pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
+      // rounding of the weights alone would cost ~1e-3 relative error in O.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const int kk = 32 * half + k;
+          const float p0 = ex2_approx(fmaf(x[kk], qscale, -mr));
+          const float p1 = ex2_approx(fmaf(x[kk + 1], qscale, -mr));
+          ps += p0 + p1;
+          const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(hh);
+          hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+        }
+        tmem_st16(scol + 16 * half, hi);
+        tmem_st16(scol + 32 + 16 * half, lo);
+      }
+      if (ntok < kTileTok) {
+        // rows past the split's last token hold stale data: zero this CTA's V rows
+        uint4* v = reinterpret_cast<uint4*>(sKV + st * kStage);
+        const int tail = kTileTok - ntok;
+        for (int e = row; e < 4 * tail * 8; e += kWgThreads) {
+          const int cch = e / (tail * 8), rem = e % (tail * 8);
+          v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      l += ps;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p_full[st]));
+    }
+    // ---- epilogue ----
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
+    l_s[g][row] = l;
+    m_s[g][row] = m_own;
+    mbar_arrive(smem_u32(&bar_l));
+    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
+    ok = ok && l_ok;
+    // O follows the latest reference (the larger, since the reference only grows);
+    // each warpgroup's sum is brought to it
+    const float m0 = m_s[0][row], m1 = m_s[1][row];
+    const float m_ref = fmaxf(m0, m1);
+    const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_ref)) +
+                        (m1 == -INFINITY ? 0.f : l_s[1][row] * ex2_approx(m1 - m_ref));
+    tc_fence_after();
+    const bool direct = !p.fused && p.num_splits == 1;
+    // workspace slot of this (shard, split): split-major unfused, shard-major fused
+    const int64_t wrow = p.fused ? ((int64_t)(sr * p.num_splits + split) * a.B + b) * R + grow
+                                 : ((int64_t)split * a.B * a.shard_count + bz) * R + grow;
+    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL : p.ws_o + wrow * kDL) +
+                 h * 256 + g * 128;
+    const bool read_o = ok && ntiles > 0;                   // uniform across the warp
+    const bool live = read_o && l_tot > 0.f;
+    const float inv = live ? 1.f / l_tot : 0.f;
+    for (int q = 0; q < 8; ++q) {
+      uint32_t u[16];
+      if (read_o) {
+        tmem_ld16(tmem + lane_off + kColO3 + g * 128 + q * 16, u);
+        tmem_ld_wait();
+      }
+      if (!real) continue;
+      float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        d4[v] = live ? make_float4(__uint_as_float(u[4 * v]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
+                                   __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (h == 0 && g == 0 && real) {
+      const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
+      if (direct)
+        a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
+      else
+        p.ws_lse[wrow] = lse2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // the peer may still be writing into this CTA's exchange buffer or barriers
+  cluster_arrive();
+  cluster_wait();
+  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (p.num_splits == 1 && !p.fused) return;
+  tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
     decode_tc_bf16_kernel(const __grid_constant__ TcParams p) {
-  decode_tc_body<false>(p);
+  decode_tc_bf16_body(p);
 }
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<true>::kThreads, 1)
     decode_tc_e4m3_kernel(const __grid_constant__ TcParams p) {
@@ -973,6 +1488,20 @@ int encode_rows_576_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32
   cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
+// The 32 rope dims one CTA owns: bf16 pool as [rows, 576], box {32, box_rows}, 64-byte swizzle.
+int encode_rows_rope(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return DCPMLA_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDK * 2};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
@@ -1081,14 +1610,14 @@ size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
 
 template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
-  using C = Cfg<kFp8>;
   auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes) !=
-      cudaSuccess)
+  const int threads = kFp8 ? Cfg<true>::kThreads : b16::kThreads;
+  const size_t smem = kFp8 ? Cfg<true>::kSmemBytes : b16::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DCPMLA_ERR_CUDA;
   const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
                   (unsigned)(p.a.B * p.a.shard_count));
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(p);
+  kern<<<grid, threads, smem, st>>>(p);
   return launch_status();
 }
 
@@ -1111,6 +1640,9 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     rc = a.fp8 ? encode_rows_576_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows)
                : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
   }
+  for (int i = 0; rc == DCPMLA_OK && !a.fp8 && i < a.shard_count; ++i)
+    rc = encode_rows_rope(&p.tm_rope[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
+                          (uint32_t)p.box_rows);
   p.use3d = !a.fp8 && p.box_rows == kTileTok;
   for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
     if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
