@@ -52,34 +52,11 @@ using namespace sm100;
 constexpr int kMaxTcShards = 8;
 constexpr int kRows = 128;
 constexpr int kTileTok = 64;
-constexpr int kChunkBytes = kTileTok * 128;          // 64 tokens x 64 16-bit values
-constexpr int kStageBytes = 5 * kChunkBytes;         // room for CTA 1's five chunks
-constexpr int kRawChunkBytes = kTileTok * 64;        // 64 tokens x 64 E4M3 codes
-constexpr int kRawScaleOff = 5 * kRawChunkBytes;     // then the tile's 64 fp32 scales
-constexpr int kRawStageBytes = kRawScaleOff + kTileTok * 4;
-constexpr int kRawStages = 2;
-constexpr int kQropeBytes = kRows * 128;             // 64 rope dims x 128 rows
 constexpr int kXBytes = kRows * kTileTok * 4;        // one fp32 partial score tile
 constexpr int kSoftmaxThreads = 256;
 constexpr int kWgThreads = 128;                     // one softmax warpgroup
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384, kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 2000000000LL;     // about one second
-
-// Layout per KV format.  bf16: warps 0 TMA, 1 MMA (lane 1 relays exchange-buffer
-// releases), 2-9 softmax, and a 4-deep ring of bf16 stages.  E4M3: warps 10-11
-// convert a 2-deep ring of raw E4M3 stages (codes + per-token scales) into a
-// 3-deep ring of fp16 stages, and all MMAs run in fp16.
-template <bool kFp8>
-struct Cfg {
-  static constexpr int kStages = 3;
-  // bf16: the two softmax warpgroups take alternate tiles, each with its own exchange
-  // buffer; E4M3 keeps both warpgroups on one tile (its converter stages need the room)
-  static constexpr int kXBufs = kFp8 ? 1 : 2;
-  static constexpr int kThreads = kFp8 ? 384 : 320;   // <= 3 warps per SM sub-partition
-  static constexpr int kConvThreads = 64;
-  static constexpr size_t kSmemBytes = 1024 + kQropeBytes + kStages * kStageBytes + kXBufs * kXBytes +
-                                       (kFp8 ? kRawStages * kRawStageBytes : 0);
-};
 
 struct TcParams {
   CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
@@ -223,718 +200,6 @@ __device__ __noinline__ void tc_combine_tail(const TcParams& p, int b, int bz, i
   }
 }
 
-template <bool kFp8>
-__device__ __forceinline__ void decode_tc_body(const TcParams& p) {
-  using C = Cfg<kFp8>;
-  constexpr int kStages = C::kStages;
-  constexpr int kThreads = C::kThreads;
-  const DecodeArgs& a = p.a;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
-  uint8_t* sKV = smem + kQropeBytes;                     // kStages x kStageBytes (16-bit values)
-  uint8_t* sX = sKV + kStages * kStageBytes;             // the peer's partial scores, per warpgroup
-  uint8_t* sRaw = sX + C::kXBufs * kXBytes;              // E4M3 only: raw stages
-  constexpr int kXB = C::kXBufs;
-  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
-  __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
-  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_mref[2], bar_max[2];
-  __shared__ uint64_t bar_x_full[2], bar_x_empty[2], bar_x_read[2];
-  __shared__ uint64_t bar_q_full, bar_o, bar_o_full, bar_drain, bar_l;
-  __shared__ float mref_s[2][kRows];                       // a warpgroup's reference max after its tile
-  __shared__ float xmax_s[kFp8 ? 2 : 1][2][kFp8 ? kRows : 1];   // E4M3: the two halves' row maxima
-  __shared__ float l_s[2][kRows], m_s[2][kRows];
-  __shared__ float kscale_s[kFp8 ? kStages : 1][kTileTok];
-  __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, bad_s, last_s;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t h = cluster_ctarank();                 // which key dims this CTA owns
-  const uint32_t peer = h ^ 1u;
-  const int nck = h ? 5 : 4;                             // 64-wide key chunks owned
-  const int split = blockIdx.x >> 1, rt = blockIdx.y, bz = blockIdx.z;
-  const int b = bz / a.shard_count, sr = bz % a.shard_count, r = a.shard_begin + sr;
-  const int L = a.seq_lens[b];
-  const int64_t R = a.R;
-  const int32_t* pt_row = a.pt + (int64_t)b * a.max_pages;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_kv_full[s]), kFp8 ? C::kConvThreads : 1);
-      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
-    }
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(smem_u32(&bar_raw_full[s]), 1);
-      mbar_init(smem_u32(&bar_raw_empty[s]), C::kConvThreads);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bar_s_full[s]), 1);
-      // bf16: one warpgroup per tile parity; E4M3: both warpgroups on every tile
-      mbar_init(smem_u32(&bar_p_full[s]), kFp8 ? kSoftmaxThreads : kWgThreads);
-      mbar_init(smem_u32(&bar_mref[s]), kWgThreads);
-      mbar_init(smem_u32(&bar_max[s]), kSoftmaxThreads);
-      mbar_init(smem_u32(&bar_x_full[s]), 1);
-      mbar_init(smem_u32(&bar_x_empty[s]), 1);                 // the peer's relay thread
-      mbar_init(smem_u32(&bar_x_read[s]), kFp8 ? kSoftmaxThreads : kWgThreads);
-    }
-    mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
-    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
-    mbar_init(smem_u32(&bar_o), 1);
-    mbar_init(smem_u32(&bar_o_full), 1);
-    mbar_init(smem_u32(&bar_drain), 1);
-    abort_s = 0;
-    bad_s = 0;
-    last_s = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
-    tmem_relinquish();
-  }
-  int j0 = 0, j1 = 0, npages = 0;
-  if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
-    if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
-  } else {
-    const int n = shard_len(L, r, a.c, a.I);
-    j0 = min(split * p.chunk, n);
-    j1 = min(n, j0 + p.chunk);
-    npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
-    for (int pg = tid; pg < npages; pg += kThreads) {
-      const int32_t g = pt_row[pg];
-      if (g < 0 || (int64_t)g >= a.num_pages) atomicOr(&bad_s, DCPMLA_DERR_PAGE);
-    }
-  }
-  __syncthreads();
-  // both CTAs' barriers are initialised before either touches the other's
-  cluster_arrive();
-  cluster_wait();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_s;
-  if (bad_s) {
-    if (tid == 0) set_err(a.err, bad_s);
-    j1 = j0;
-  }
-  const int ntiles = (j1 - j0 + kTileTok - 1) / kTileTok;
-  volatile int* abort_flag = &abort_s;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    // The whole warp keeps a window of 32 page ids; lane 0 issues the copies.
-    if (ntiles > 0) {
-      const CUtensorMap* kvmap = &p.tm_kv[sr];
-      const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
-      if (lane == 0) {
-        prefetch_tmap(kvmap);
-        if (!kFp8 && p.use3d) prefetch_tmap(kvmap3);
-      }
-      // E4M3 tiles go to the raw ring; bf16 tiles straight to the MMA ring.
-      constexpr int ring = kFp8 ? kRawStages : kStages;
-      int win_base = -64, win_val = 0, issued = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % ring;
-        if (i >= ring) {
-          bool okw = true;
-          if (lane == 0)
-            okw = wait_bar<false>(kFp8 ? smem_u32(&bar_raw_empty[st]) : smem_u32(&bar_kv_empty[st]),
-                                  ((i / ring) - 1) & 1, abort_flag);
-          if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
-        }
-        const int t0 = j0 + i * kTileTok;
-        const int ntok = min(kTileTok, j1 - t0);
-        const int box = p.box_rows;
-        const int nbox = box >= kTileTok ? 1 : (ntok + box - 1) / box;
-        const uint32_t full = kFp8 ? smem_u32(&bar_raw_full[st]) : smem_u32(&bar_kv_full[st]);
-        const int row_bytes = kFp8 ? 64 : 128;
-        // E4M3 also brings each box's per-token scales (box * 4 bytes)
-        if (lane == 0)
-          mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (row_bytes * nck + (kFp8 ? 4 : 0))));
-        for (int pb = 0; pb < nbox; ++pb) {
-          const int tok = t0 + pb * box;
-          const int pidx = tok / a.P;
-          if (pidx < win_base || pidx >= win_base + 32) {      // uniform across the warp
-            win_base = pidx;
-            win_val = pidx + lane < npages ? pt_row[pidx + lane] : 0;
-          }
-          const int g = __shfl_sync(0xffffffffu, win_val, pidx - win_base);
-          if (lane == 0) {
-            const int y = (int)((int64_t)g * a.P + (tok % a.P));
-            if (kFp8) {
-              const uint32_t dst = smem_u32(sRaw + st * kRawStageBytes + pb * box * 64);
-              for (int cl = 0; cl < nck; ++cl)
-                tma_load_2d(dst + cl * kRawChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
-              bulk_load(smem_u32(sRaw + st * kRawStageBytes + kRawScaleOff + pb * box * 4),
-                        a.kv.scale[r] + y, (uint32_t)(box * 4), full);
-            } else {
-              const uint32_t dst = smem_u32(sKV + st * kStageBytes + pb * box * 128);
-              if (p.use3d) {
-                tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
-                if (h) tma_load_2d(dst + 4 * kChunkBytes, kvmap, 512, y, full);
-              } else {
-                for (int cl = 0; cl < nck; ++cl)
-                  tma_load_2d(dst + cl * kChunkBytes, kvmap, (int)(4 * h + cl) * 64, y, full);
-              }
-            }
-          }
-        }
-        issued = i + 1;
-      }
-      if (lane == 0 && *abort_flag) {
-        // let copies already in flight land before the CTA's shared memory goes away
-        for (int i = max(0, issued - ring); i < issued; ++i) {
-          const uint32_t full = kFp8 ? smem_u32(&bar_raw_full[i % ring]) : smem_u32(&bar_kv_full[i % ring]);
-          const long long t0 = clock64();
-          while (!mbar_try_wait(full, (i / ring) & 1) && clock64() - t0 < kWaitCycles / 8) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_qk =
-          kFp8 ? idesc_f16(kRows, kTileTok, false, false) : idesc_bf16(kRows, kTileTok, false, false);
-      constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(kRows, 256, false, true) : idesc_bf16(kRows, 256, false, true);
-      constexpr int kPvSteps = kFp8 ? 4 : 8;   // bf16: P as hi + lo, two MMAs per 16 tokens
-      // Base descriptors; the start-address field is the low 14 bits (address >> 4),
-      // so a constant byte offset is added as (offset >> 4) without carries.
-      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);            // K-major keys
-      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunkBytes, 1024);   // MN-major values
-      const uint64_t qd0 = desc_sw128(smem_u32(sQr), 16, 1024);            // rope part of Q
-      const uint32_t tq = tmem + kColQ, to = tmem + kColO;
-      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
-      tc_fence_after();
-      for (int i = 0; ok && i <= ntiles; ++i) {
-        if (i < ntiles) {
-          const int st = i % kStages, sb = i & 1;
-          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t d = tmem + kColS + sb * kTileTok;
-          const uint64_t kd = kd0 + (uint64_t)((st * kStageBytes) >> 4);
-#pragma unroll
-          for (int cl = 0; cl < 4; ++cl)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ts(d, tq + cl * 32 + k * 8, kd + ((cl * kChunkBytes + k * 32) >> 4), idesc_qk,
-                     (cl | k) != 0);
-          if (h) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(d, qd0 + ((k * 32) >> 4), kd + ((4 * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
-          }
-          mma_commit(smem_u32(&bar_s_full[sb]));
-        }
-        if (i >= 1) {
-          const int pi = i - 1, st = pi % kStages, sb = pi & 1;
-          if (!wait_bar<false>(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint64_t vd = vd0 + (uint64_t)((st * kStageBytes) >> 4);
-          const uint32_t pa = tmem + kColS + sb * kTileTok;
-          mma_ts(to, pa, vd, idesc_pv, pi > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 1; k < kPvSteps; ++k)
-            mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, 1u);
-          mma_commit(smem_u32(&bar_kv_empty[st]));
-          mma_commit(smem_u32(&bar_o));
-          if (pi == ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // O complete
-        }
-      }
-      // drain: every MMA issued above completes before TMEM is released
-      mma_commit(smem_u32(&bar_drain));
-      const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
-      }
-    }
-    if (lane == 1) {
-      // relay: once all softmax threads have read the peer's partial for a tile,
-      // tell the peer its next partial may overwrite our exchange buffer.  This
-      // thread has no stores in flight, so its cluster-scope release is cheap.
-      // tile i goes through exchange buffer i % kXB (bf16: its warpgroup's)
-      for (int i = 0; i < ntiles; ++i) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read[i % kXB]), (i / kXB) & 1, abort_flag)) break;
-        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[i % kXB]), peer));
-      }
-    }
-  } else if (warp >= 10) {
-    // --------------------------------------------------- E4M3 -> fp16 convert
-    // Each 8 codes of a raw row become one 16-byte unit of the fp16 row, placed
-    // at its 128-byte-swizzle position; rows past the tile's last token are
-    // written as zeros.  Also stages the tile's per-token scales.
-    if (kFp8 && ntiles > 0) {
-      const int ct = tid - 10 * 32;                           // 0..63
-      for (int i = 0; i < ntiles; ++i) {
-        const int rs = i % kRawStages, st = i % kStages;
-        const int t0 = j0 + i * kTileTok;
-        const int ntok = min(kTileTok, j1 - t0);
-        if (!__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_raw_full[rs]), (i / kRawStages) & 1, abort_flag)))
-          break;
-        if (i >= kStages &&
-            !__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag)))
-          break;
-        const uint8_t* raw = sRaw + rs * kRawStageBytes;
-        uint8_t* dst = sKV + st * kStageBytes;
-        // 16 codes per item (a 16-byte load, two 16-byte stores), four items in flight
-        // per thread: the conversion is latency-bound with only two warps on it
-        constexpr int kU = 4;
-        const int n_items = nck * kTileTok * 4;
-        for (int base = ct; base < n_items; base += C::kConvThreads * kU) {
-          uint4 w[kU];
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const int e = base + k * C::kConvThreads;
-            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
-            w[k] = (e < n_items && t < ntok)
-                       ? *reinterpret_cast<const uint4*>(raw + cl * kRawChunkBytes + t * 64 + e16 * 16)
-                       : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const int e = base + k * C::kConvThreads;
-            if (e >= n_items) break;
-            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
-            uint4 lo, hi;   // codes 0-7 and 8-15 of the item
-            lo.x = e4m3x2_to_f16x2((uint16_t)(w[k].x & 0xFFFF));
-            lo.y = e4m3x2_to_f16x2((uint16_t)(w[k].x >> 16));
-            lo.z = e4m3x2_to_f16x2((uint16_t)(w[k].y & 0xFFFF));
-            lo.w = e4m3x2_to_f16x2((uint16_t)(w[k].y >> 16));
-            hi.x = e4m3x2_to_f16x2((uint16_t)(w[k].z & 0xFFFF));
-            hi.y = e4m3x2_to_f16x2((uint16_t)(w[k].z >> 16));
-            hi.z = e4m3x2_to_f16x2((uint16_t)(w[k].w & 0xFFFF));
-            hi.w = e4m3x2_to_f16x2((uint16_t)(w[k].w >> 16));
-            uint8_t* drow = dst + cl * kChunkBytes + t * 128;
-            *reinterpret_cast<uint4*>(drow + (((2 * e16) ^ (t & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(drow + (((2 * e16 + 1) ^ (t & 7)) << 4)) = hi;
-          }
-        }
-        for (int t = ct; t < kTileTok; t += C::kConvThreads)
-          kscale_s[st][t] = t < ntok ? reinterpret_cast<const float*>(raw + kRawScaleOff)[t] : 0.f;
-        fence_proxy_async();
-        mbar_arrive(smem_u32(&bar_raw_empty[rs]));
-        mbar_arrive(smem_u32(&bar_kv_full[st]));
-      }
-    }
-  } else {
-    // -------------------------------------------------------------- softmax
-    // Warps 2..9: two warpgroups; warpgroup g handles tile columns [32g, 32g + 32)
-    // of every query row (TMEM lane quarter = warp % 4).
-    const int g = (warp - 2) >> 2;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
-    const bool real = grow < R;                              // rows past R pad the tile
-    // Shard positions grow with the shard-local index, so the keys a query sees form a
-    // prefix: shard-local tokens below shard_len(qpos + 1) (those at positions <= qpos),
-    // and below j1.  jvis: this row's prefix; jvis_min: every row's (the earliest query).
-    const int jvis = min(j1, shard_len(L - a.Tq + (int)(grow / a.H) + 1, r, a.c, a.I));
-    const int jvis_min = min(j1, shard_len(L - a.Tq + 1, r, a.c, a.I));
-    const float qscale = a.sm_scale * kLog2e;
-    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
-    // this warpgroup's partial sum l is relative to m_own (the reference max at its
-    // last tile); the current reference is the latest one any warpgroup published
-    float m_own = -INFINITY, l = 0.f;
-    bool ok = true;
-    if (ntiles > 0) {
-      // this CTA's latent dims of the query row into TMEM as packed 16-bit pairs
-      const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK +
-                                                         h * 256 + g * 128);
-      for (int c16 = 0; c16 < 4; ++c16) {
-        uint32_t rr[16];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
-          rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
-        }
-        if (kFp8) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) rr[k] = bf16x2_to_f16x2(rr[k]);
-        }
-        tmem_st16(tmem + lane_off + kColQ + g * 64 + c16 * 16, rr);
-      }
-      // CTA 1: the rope part of the query row (64 dims) into shared memory in the
-      // 128-byte-swizzle layout the MMA reads (fp16 for E4M3 runs); pad rows get zeros
-      if (h && g == 0) {
-        const uint4* rsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK + 512);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint4 v = real ? __ldg(rsrc + u) : make_uint4(0, 0, 0, 0);
-          if (kFp8) {
-            v.x = bf16x2_to_f16x2(v.x); v.y = bf16x2_to_f16x2(v.y);
-            v.z = bf16x2_to_f16x2(v.z); v.w = bf16x2_to_f16x2(v.w);
-          }
-          *reinterpret_cast<uint4*>(sQr + row * 128 + ((u ^ (row & 7)) << 4)) = v;
-        }
-        fence_proxy_async();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_q_full));
-    }
-    if constexpr (kFp8) {
-      // both warpgroups on every tile, warpgroup g on tile columns [32g, 32g + 32)
-      const int stid = g * kRows + row;                      // 0..255
-      const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[0]), peer);
-      float m_ref = -INFINITY;
-      for (int i = 0; ok && i < ntiles; ++i) {
-        const int sb = i & 1, st = i % kStages;
-        const int t0 = j0 + i * kTileTok;
-        const int ntok = min(kTileTok, j1 - t0);
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t own[32];
-        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
-        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
-                  *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
-        tmem_ld_wait();
-        // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
-        // float4), once the peer has read the previous one
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[0]), (i - 1) & 1, abort_flag));
-          if (!ok) break;
-        }
-  #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
-                      make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
-        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[0]), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[0]), i & 1, abort_flag));
-        if (!ok) break;
-        float x[32];
-        const float4* xin = reinterpret_cast<const float4*>(sX);
-  #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 pv = xin[(8 * g + c) * kRows + row];
-          const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
-          const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
-          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
-          x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
-          x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
-          x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
-          x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
-        }
-        mbar_arrive(smem_u32(&bar_x_read[0]));
-        const float* ks = kscale_s[st] + 32 * g;
-        if (kFp8) {
-          // E4M3: the key's per-token scale multiplies its score
-  #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] *= ks[k];
-        }
-        // causal / tail mask on raw scores (only tiles that need it)
-        if (t0 + kTileTok > jvis_min) {
-          const int lim = jvis - t0 - 32 * g;
-  #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = k < lim ? x[k] : -INFINITY;
-        }
-        float tmax = fmaxf(x[0], x[1]);
-  #pragma unroll
-        for (int k = 2; k < 32; ++k) tmax = fmaxf(tmax, x[k]);
-        // row max across the two warpgroups; this sync also orders every thread's
-        // S reads before any P write into the same TMEM columns
-        xmax_s[i & 1][g][row] = tmax;
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_max[i & 1]));
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
-        // Lazy reference max: move it only when this tile's max exceeds it by more
-        // than 8 (so every weight 2^(x - m_ref) stays <= 256).  Rows that move it
-        // after O holds data rescale O (each warpgroup its 128 columns).
-        const bool move = tmax > m_ref + 8.f;
-        const bool rescale_me = move && m_ref != -INFINITY;
-        if (__any_sync(0xffffffffu, rescale_me)) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
-          for (int q = 0; q < 8; ++q) {
-            uint32_t u[16];
-            const uint32_t oc = tmem + lane_off + kColO + g * 128 + q * 16;
-            tmem_ld16(oc, u);
-            tmem_ld_wait();
-  #pragma unroll
-            for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-            tmem_st16(oc, u);
-          }
-          l *= alpha;
-        }
-        if (move) m_ref = tmax;
-        const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
-        const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
-        float ps = 0.f;
-        if (kFp8) {
-          // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
-          uint32_t pp[16];
-  #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
-            const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
-            ps += p0 + p1;
-            pp[k >> 1] = pack_f16(p0 * ks[k], p1 * ks[k + 1]);
-          }
-          tmem_st16(pcol + 16 * g, pp);
-        } else {
-          // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
-          // rounding of the weights alone would cost ~1e-3 relative error in O.
-          uint32_t hi[16], lo[16];
-  #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
-            const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
-            ps += p0 + p1;
-            const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-            const float2 hf = __bfloat1622float2(hh);
-            hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
-            lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
-          }
-          tmem_st16(pcol + 16 * g, hi);
-          tmem_st16(pcol + 32 + 16 * g, lo);
-          if (ntok < kTileTok) {
-            // rows past the split's last token hold stale data: zero this CTA's V rows
-            uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
-            const int tail = kTileTok - ntok;
-            for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
-              const int cch = e / (tail * 8), rem = e % (tail * 8);
-              v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async();
-          }
-        }
-        l += ps;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p_full[sb]));
-      }
-      m_own = m_ref;                                           // the same in both warpgroups
-    } else {
-      // Tiles alternate between the warpgroups: warpgroup g takes tiles i with i % 2 == g,
-      // each thread one query row over all 64 columns, so two tiles' exchanges and
-      // softmax chains are in flight at once.  The lazy reference max is handed from
-      // tile to tile through shared memory.
-      const int wtid = row;                                    // thread within its warpgroup
-      for (int i = g; ok && i < ntiles; i += 2) {
-        const int st = i % kStages;
-        const int t0 = j0 + i * kTileTok;
-        const int ntok = min(kTileTok, j1 - t0);
-        const uint32_t scol = tmem + lane_off + kColS + g * kTileTok;
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[g]), (i >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        // send this CTA's partial into the peer's buffer g ([16 column groups][128 rows]
-        // of float4), once the peer has read what this warpgroup sent two tiles ago
-        if (i >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((i >> 1) - 1) & 1, abort_flag));
-          if (!ok) break;
-        }
-        const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
-  #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t own[32];
-          tmem_ld16(scol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
-          tmem_ld16(scol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
-          tmem_ld_wait();
-  #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_async_v4(x_remote + g * kXBytes + ((8 * half + c) * kRows + row) * 16,
-                        make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
-        }
-        if (wtid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (i >> 1) & 1, abort_flag));
-        if (!ok) break;
-        float x[64];
-        const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
-  #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t own[32];   // this CTA's partial again (still in TMEM: P(i) is not written yet)
-          tmem_ld16(scol + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
-          tmem_ld16(scol + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
-          tmem_ld_wait();
-  #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 pv = xin[(8 * half + c) * kRows + row];
-            const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
-            const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
-            // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
-            float* xx = x + 32 * half + 4 * c;
-            xx[0] = h ? pv.x + o0 : o0 + pv.x;
-            xx[1] = h ? pv.y + o1 : o1 + pv.y;
-            xx[2] = h ? pv.z + o2 : o2 + pv.z;
-            xx[3] = h ? pv.w + o3 : o3 + pv.w;
-          }
-        }
-        mbar_arrive(smem_u32(&bar_x_read[g]));
-        const float* ks = kscale_s[kFp8 ? st : 0];
-        if (kFp8) {
-          // E4M3: the key's per-token scale multiplies its score
-  #pragma unroll
-          for (int k = 0; k < 64; ++k) x[k] *= ks[k];
-        }
-        // causal / tail mask on raw scores (only tiles that need it)
-        if (t0 + kTileTok > jvis_min) {
-          const int lim = jvis - t0;
-  #pragma unroll
-          for (int k = 0; k < 64; ++k) x[k] = k < lim ? x[k] : -INFINITY;
-        }
-        float tmax = fmaxf(x[0], x[1]);
-  #pragma unroll
-        for (int k = 2; k < 64; ++k) tmax = fmaxf(tmax, x[k]);
-        tmax *= qscale;
-        // the reference max as the previous tile (the other warpgroup's) left it
-        float m_ref = -INFINITY;
-        if (i >= 1) {
-          const int pg = g ^ 1;
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[pg]), ((i - 1) >> 1) & 1, abort_flag));
-          if (!ok) break;
-          m_ref = mref_s[pg][row];
-        }
-        // Lazy reference max: move it only when this tile's max exceeds it by more
-        // than 8 (so every weight 2^(x - m_ref) stays <= 256).  A row that moves it
-        // after O holds data rescales its O columns (all 256 of this CTA).
-        const bool move = tmax > m_ref + 8.f;
-        const bool rescale_me = move && m_ref != -INFINITY;
-        if (__any_sync(0xffffffffu, rescale_me)) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
-          for (int q = 0; q < 16; ++q) {
-            uint32_t u[16];
-            const uint32_t oc = tmem + lane_off + kColO + q * 16;
-            tmem_ld16(oc, u);
-            tmem_ld_wait();
-  #pragma unroll
-            for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-            tmem_st16(oc, u);
-          }
-          tmem_st_wait();
-        }
-        if (move) m_ref = tmax;
-        mref_s[g][row] = m_ref;
-        mbar_arrive(smem_u32(&bar_mref[g]));
-        // this warpgroup's partial sum follows the reference
-        if (m_own != m_ref) {
-          l = m_own == -INFINITY ? 0.f : l * ex2_approx(m_own - m_ref);
-          m_own = m_ref;
-        }
-        const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
-        float ps = 0.f;
-        if (kFp8) {
-          // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
-  #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pp[16];
-  #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const int kk = 32 * half + k;
-              const float p0 = ex2_approx(fmaf(x[kk], qscale, -mr));
-              const float p1 = ex2_approx(fmaf(x[kk + 1], qscale, -mr));
-              ps += p0 + p1;
-              pp[k >> 1] = pack_f16(p0 * ks[kk], p1 * ks[kk + 1]);
-            }
-            tmem_st16(scol + 16 * half, pp);
-          }
-        } else {
-          // bf16 P as a pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi)): one bf16
-          // rounding of the weights alone would cost ~1e-3 relative error in O.
-  #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t hi[16], lo[16];
-  #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const int kk = 32 * half + k;
-              const float p0 = ex2_approx(fmaf(x[kk], qscale, -mr));
-              const float p1 = ex2_approx(fmaf(x[kk + 1], qscale, -mr));
-              ps += p0 + p1;
-              const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-              const float2 hf = __bfloat1622float2(hh);
-              hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
-              lo[k >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
-            }
-            tmem_st16(scol + 16 * half, hi);
-            tmem_st16(scol + 32 + 16 * half, lo);
-          }
-          if (ntok < kTileTok) {
-            // rows past the split's last token hold stale data: zero this CTA's V rows
-            uint4* v = reinterpret_cast<uint4*>(sKV + st * kStageBytes);
-            const int tail = kTileTok - ntok;
-            for (int e = wtid; e < 4 * tail * 8; e += kWgThreads) {
-              const int cch = e / (tail * 8), rem = e % (tail * 8);
-              v[(cch * kChunkBytes + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async();
-          }
-        }
-        l += ps;
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p_full[g]));
-      }
-    }
-    // ---- epilogue ----
-    if (ok && ntiles > 0)
-      // Not bar_o: when the last tile's softmax ends, PV(ntiles - 2) may still be
-      // running, and a parity wait on bar_o would then match an older phase.
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
-    l_s[g][row] = l;
-    m_s[g][row] = m_own;
-    mbar_arrive(smem_u32(&bar_l));
-    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
-    ok = ok && l_ok;
-    // O follows the latest reference (the larger, since the reference only grows);
-    // each warpgroup's sum is brought to it
-    const float m0 = m_s[0][row], m1 = m_s[1][row];
-    const float m_ref = fmaxf(m0, m1);
-    const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_ref)) +
-                        (m1 == -INFINITY ? 0.f : l_s[1][row] * ex2_approx(m1 - m_ref));
-    tc_fence_after();
-    const bool direct = !p.fused && p.num_splits == 1;
-    // workspace slot of this (shard, split): split-major unfused, shard-major fused
-    const int64_t wrow = p.fused ? ((int64_t)(sr * p.num_splits + split) * a.B + b) * R + grow
-                                 : ((int64_t)split * a.B * a.shard_count + bz) * R + grow;
-    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL : p.ws_o + wrow * kDL) +
-                 h * 256 + g * 128;
-    const bool read_o = ok && ntiles > 0;                   // uniform across the warp
-    const bool live = read_o && l_tot > 0.f;
-    const float inv = live ? 1.f / l_tot : 0.f;
-    for (int q = 0; q < 8; ++q) {
-      uint32_t u[16];
-      if (read_o) {
-        tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
-        tmem_ld_wait();
-      }
-      if (!real) continue;
-      float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        d4[v] = live ? make_float4(__uint_as_float(u[4 * v]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
-                                   __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (h == 0 && g == 0 && real) {
-      const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
-      if (direct)
-        a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
-      else
-        p.ws_lse[wrow] = lse2;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-  // the peer may still be writing into this CTA's exchange buffer or barriers
-  cluster_arrive();
-  cluster_wait();
-  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
-  if (p.num_splits == 1 && !p.fused) return;
-
-  tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStageBytes, &last_s);
-}
-
 // ------------------------------------------------------------ bf16 KV, three S/P slots
 // The bf16 kernel keeps three score/probability tiles in TMEM, so QK of tile i + 2
 // never waits for PV of tile i (P overwrites its own scores in place).  The TMEM
@@ -962,7 +227,7 @@ constexpr int kQBytes = kQRopeOff + kRows * 64;
 constexpr int kThreads = 384;
 constexpr int kLook = 4;
 constexpr size_t kSmemBytes = 1024 + kQBytes + kStages * kStage + 2 * kXBytes;
-constexpr uint32_t kColO3 = 0, kColS3 = 256, kColQ3 = 448;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 448;
 static_assert(kSmemBytes <= 227 * 1024 - 4096, "stages, Q and exchange buffers exceed shared memory");
 }  // namespace b16
 
@@ -1129,14 +394,14 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
       const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
       const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
-      const uint32_t tq = tmem + kColQ3;
+      const uint32_t tq = tmem + kColQ;
       bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
       tc_fence_after();
       for (int i = 0; ok && i < ntiles; ++i) {
         const int st = i % kStages;
         if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem + kColS3 + st * kTileTok;
+        const uint32_t d = tmem + kColS + st * kTileTok;
         const uint64_t so = (uint64_t)((st * kStage) >> 4);
 #pragma unroll
         for (int cl = 0; cl < 2; ++cl)
@@ -1166,13 +431,13 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
       const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
-      const uint32_t to = tmem + kColO3;
+      const uint32_t to = tmem + kColO;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (!wait_bar<false>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag)) break;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
-        const uint32_t pa = tmem + kColS3 + st * kTileTok;
+        const uint32_t pa = tmem + kColS + st * kTileTok;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
@@ -1228,7 +493,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
             const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
             rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
           }
-          tmem_st16(tmem + lane_off + kColQ3 + c16 * 16, rr);
+          tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
         }
         tmem_st_wait();
       } else {
@@ -1257,7 +522,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const int st = i % kStages;
       const int t0 = j0 + i * kTileTok;
       const int ntok = min(kTileTok, j1 - t0);
-      const uint32_t scol = tmem + lane_off + kColS3 + st * kTileTok;
+      const uint32_t scol = tmem + lane_off + kColS + st * kTileTok;
       ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (i / kStages) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
@@ -1324,7 +589,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
         for (int q = 0; q < 16; ++q) {
           uint32_t u[16];
-          const uint32_t oc = tmem + lane_off + kColO3 + q * 16;
+          const uint32_t oc = tmem + lane_off + kColO + q * 16;
           tmem_ld16(oc, u);
           tmem_ld_wait();
 #pragma unroll
@@ -1403,7 +668,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     for (int q = 0; q < 8; ++q) {
       uint32_t u[16];
       if (read_o) {
-        tmem_ld16(tmem + lane_off + kColO3 + g * 128 + q * 16, u);
+        tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
         tmem_ld_wait();
       }
       if (!real) continue;
@@ -1437,13 +702,524 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
   tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
 }
 
+// ------------------------------------------------------------ E4M3 KV
+// E4M3 codes (one fp32 scale per token) are converted exactly to fp16 stages and
+// every MMA runs in fp16 (E4M3 is a subset of fp16).  CTA 0 owns key dims
+// [0, 256), CTA 1 [256, 576) (latent 256..511 and the 64 rope dims).
+//
+//   warp 0      TMA producer: raw 64-token tiles of this CTA's codes (64-code
+//               chunks) and the tokens' scales into a 2-deep ring
+//   warp 1      allocates TMEM; lane 0 issues QK(i) then PV(i - 1):
+//                 S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; latent Q from TMEM)
+//                 O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
+//   warps 2-9   softmax, both warpgroups on every tile, each 32 of its columns
+//   warps 10-11 convert raw tiles into the 3-deep fp16 stage ring
+//
+// TMEM columns: O_h [0,256), S/P slots [256,384) (slot = tile % 2, P overwrites S
+// in place; in issue order QK(i + 2) follows PV(i)), Q_h latent [384,512).
+namespace e4 {
+constexpr int kStages = 3;                          // fp16 stages
+constexpr int kRawStages = 2;
+constexpr int kChunk = kTileTok * 128;              // 64 tokens x 64 fp16 dims, 128-byte swizzle
+constexpr int kStage = 5 * kChunk;                  // room for CTA 1's five chunks
+constexpr int kRawChunk = kTileTok * 64;            // 64 tokens x 64 codes
+constexpr int kRawScaleOff = 5 * kRawChunk;         // then the tile's 64 fp32 scales
+constexpr int kRawStage = kRawScaleOff + kTileTok * 4;
+constexpr int kQRope = kRows * 128;                 // CTA 1: 64 rope dims of Q, fp16
+constexpr int kThreads = 384;
+constexpr int kConvThreads = 64;
+constexpr size_t kSmemBytes = 1024 + kQRope + kStages * kStage + kXBytes + kRawStages * kRawStage;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
+static_assert(kSmemBytes <= 227 * 1024 - 6144, "stages, Q and exchange buffer exceed shared memory");
+}  // namespace e4
+
+__device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
+  using namespace e4;
+  const DecodeArgs& a = p.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
+  uint8_t* sKV = smem + kQRope;                          // kStages x kStage (fp16)
+  uint8_t* sX = sKV + kStages * kStage;                  // the peer's partial scores of one tile
+  uint8_t* sRaw = sX + kXBytes;                          // kRawStages x kRawStage
+  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
+  __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
+  __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
+  __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
+  __shared__ uint64_t bar_q_full, bar_o, bar_o_full, bar_drain, bar_l;
+  __shared__ float xmax_s[2][2][kRows];                  // the two warpgroups' row maxima of a tile
+  __shared__ float l_s[2][kRows], m_s[2][kRows];
+  __shared__ float kscale_s[kStages][kTileTok];          // the stage's per-token scales
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s, bad_s, last_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
+  const uint32_t peer = h ^ 1u;
+  const int nck = h ? 5 : 4;                             // 64-wide key chunks owned
+  const int split = blockIdx.x >> 1, rt = blockIdx.y, bz = blockIdx.z;
+  const int b = bz / a.shard_count, sr = bz % a.shard_count, r = a.shard_begin + sr;
+  const int L = a.seq_lens[b];
+  const int64_t R = a.R;
+  const int32_t* pt_row = a.pt + (int64_t)b * a.max_pages;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), kConvThreads);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(smem_u32(&bar_raw_full[s]), 1);
+      mbar_init(smem_u32(&bar_raw_empty[s]), kConvThreads);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_p_full[s]), kSoftmaxThreads);     // both warpgroups on every tile
+      mbar_init(smem_u32(&bar_max[s]), kSoftmaxThreads);
+    }
+    mbar_init(smem_u32(&bar_x_full), 1);
+    mbar_init(smem_u32(&bar_x_empty), 1);                      // the peer's relay thread
+    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);
+    mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_o_full), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_s = 0;
+    bad_s = 0;
+    last_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  int j0 = 0, j1 = 0, npages = 0;
+  if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
+    if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
+  } else {
+    const int n = shard_len(L, r, a.c, a.I);
+    j0 = min(split * p.chunk, n);
+    j1 = min(n, j0 + p.chunk);
+    npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
+    for (int pg = tid; pg < npages; pg += kThreads) {
+      const int32_t g = pt_row[pg];
+      if (g < 0 || (int64_t)g >= a.num_pages) atomicOr(&bad_s, DCPMLA_DERR_PAGE);
+    }
+  }
+  __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  if (bad_s) {
+    if (tid == 0) set_err(a.err, bad_s);
+    j1 = j0;
+  }
+  const int ntiles = (j1 - j0 + kTileTok - 1) / kTileTok;
+  volatile int* abort_flag = &abort_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    // The whole warp keeps a window of 32 page ids; lane 0 issues the copies.
+    if (ntiles > 0) {
+      const CUtensorMap* kvmap = &p.tm_kv[sr];
+      if (lane == 0) prefetch_tmap(kvmap);
+      int win_base = -64, win_val = 0, issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kRawStages;
+        if (i >= kRawStages) {
+          bool okw = true;
+          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_raw_empty[st]), ((i / kRawStages) - 1) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
+        }
+        const int t0 = j0 + i * kTileTok;
+        const int ntok = min(kTileTok, j1 - t0);
+        const int box = p.box_rows;
+        const int nbox = box >= kTileTok ? 1 : (ntok + box - 1) / box;
+        const uint32_t full = smem_u32(&bar_raw_full[st]);
+        // each box brings its rows' codes (64 per chunk) and per-token scales
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (64 * nck + 4)));
+        for (int pb = 0; pb < nbox; ++pb) {
+          const int tok = t0 + pb * box;
+          const int pidx = tok / a.P;
+          if (pidx < win_base || pidx >= win_base + 32) {      // uniform across the warp
+            win_base = pidx;
+            win_val = pidx + lane < npages ? pt_row[pidx + lane] : 0;
+          }
+          const int g = __shfl_sync(0xffffffffu, win_val, pidx - win_base);
+          if (lane == 0) {
+            const int y = (int)((int64_t)g * a.P + (tok % a.P));
+            const uint32_t dst = smem_u32(sRaw + st * kRawStage + pb * box * 64);
+            for (int cl = 0; cl < nck; ++cl)
+              tma_load_2d(dst + cl * kRawChunk, kvmap, (int)(4 * h + cl) * 64, y, full);
+            bulk_load(smem_u32(sRaw + st * kRawStage + kRawScaleOff + pb * box * 4), a.kv.scale[r] + y,
+                      (uint32_t)(box * 4), full);
+          }
+        }
+        issued = i + 1;
+      }
+      if (lane == 0 && *abort_flag) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int i = max(0, issued - kRawStages); i < issued; ++i) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&bar_raw_full[i % kRawStages]), (i / kRawStages) & 1) &&
+                 clock64() - t0 < kWaitCycles / 8) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(kRows, kTileTok, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(kRows, 256, false, true);
+      // Base descriptors; the start-address field is the low 14 bits (address >> 4),
+      // so a constant byte offset is added as (offset >> 4) without carries.
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);            // K-major keys
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);        // MN-major values
+      const uint64_t qd0 = desc_sw128(smem_u32(sQr), 16, 1024);            // rope part of Q
+      const uint32_t tq = tmem + kColQ, to = tmem + kColO;
+      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
+      tc_fence_after();
+      for (int i = 0; ok && i <= ntiles; ++i) {
+        if (i < ntiles) {
+          const int st = i % kStages, sb = i & 1;
+          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + sb * kTileTok;
+          const uint64_t kd = kd0 + (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+          for (int cl = 0; cl < 4; ++cl)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(d, tq + cl * 32 + k * 8, kd + ((cl * kChunk + k * 32) >> 4), idesc_qk, (cl | k) != 0);
+          if (h) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mma_ss(d, qd0 + ((k * 32) >> 4), kd + ((4 * kChunk + k * 32) >> 4), idesc_qk, 1u);
+          }
+          mma_commit(smem_u32(&bar_s_full[sb]));
+        }
+        if (i >= 1) {
+          const int pi = i - 1, st = pi % kStages, sb = pi & 1;
+          if (!wait_bar<false>(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
+          const uint32_t pa = tmem + kColS + sb * kTileTok;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(to, pa + k * 8, vd + ((k * 2048) >> 4), idesc_pv, (pi > 0 || k > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_kv_empty[st]));
+          mma_commit(smem_u32(&bar_o));
+          if (pi == ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // O complete
+        }
+      }
+      // drain: every MMA issued above completes before TMEM is released
+      mma_commit(smem_u32(&bar_drain));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+    if (lane == 1) {
+      // relay: once all softmax threads have read the peer's partial for a tile,
+      // tell the peer its next partial may overwrite our exchange buffer.  This
+      // thread has no stores in flight, so its cluster-scope release is cheap.
+      for (int i = 0; i < ntiles; ++i) {
+        if (!wait_bar<false>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
+        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty), peer));
+      }
+    }
+  } else if (warp >= 10) {
+    // --------------------------------------------------- E4M3 -> fp16 convert
+    // Each 16 codes of a raw row become two 16-byte units of the fp16 row at their
+    // 128-byte-swizzle positions; rows past the tile's last token are written as
+    // zeros.  Also stages the tile's per-token scales.
+    if (ntiles > 0) {
+      const int ct = tid - 10 * 32;                           // 0..63
+      for (int i = 0; i < ntiles; ++i) {
+        const int rs = i % kRawStages, st = i % kStages;
+        const int t0 = j0 + i * kTileTok;
+        const int ntok = min(kTileTok, j1 - t0);
+        if (!__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_raw_full[rs]), (i / kRawStages) & 1, abort_flag)))
+          break;
+        if (i >= kStages &&
+            !__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag)))
+          break;
+        const uint8_t* raw = sRaw + rs * kRawStage;
+        uint8_t* dst = sKV + st * kStage;
+        // 16 codes per item (a 16-byte load, two 16-byte stores), four items in flight
+        // per thread: the conversion is latency-bound with only two warps on it
+        constexpr int kU = 4;
+        const int n_items = nck * kTileTok * 4;
+        for (int base = ct; base < n_items; base += kConvThreads * kU) {
+          uint4 w[kU];
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int e = base + k * kConvThreads;
+            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
+            w[k] = (e < n_items && t < ntok)
+                       ? *reinterpret_cast<const uint4*>(raw + cl * kRawChunk + t * 64 + e16 * 16)
+                       : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int e = base + k * kConvThreads;
+            if (e >= n_items) break;
+            const int cl = e >> 8, t = (e & 255) >> 2, e16 = e & 3;
+            uint4 lo, hi;   // codes 0-7 and 8-15 of the item
+            lo.x = e4m3x2_to_f16x2((uint16_t)(w[k].x & 0xFFFF));
+            lo.y = e4m3x2_to_f16x2((uint16_t)(w[k].x >> 16));
+            lo.z = e4m3x2_to_f16x2((uint16_t)(w[k].y & 0xFFFF));
+            lo.w = e4m3x2_to_f16x2((uint16_t)(w[k].y >> 16));
+            hi.x = e4m3x2_to_f16x2((uint16_t)(w[k].z & 0xFFFF));
+            hi.y = e4m3x2_to_f16x2((uint16_t)(w[k].z >> 16));
+            hi.z = e4m3x2_to_f16x2((uint16_t)(w[k].w & 0xFFFF));
+            hi.w = e4m3x2_to_f16x2((uint16_t)(w[k].w >> 16));
+            uint8_t* drow = dst + cl * kChunk + t * 128;
+            *reinterpret_cast<uint4*>(drow + (((2 * e16) ^ (t & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(drow + (((2 * e16 + 1) ^ (t & 7)) << 4)) = hi;
+          }
+        }
+        for (int t = ct; t < kTileTok; t += kConvThreads)
+          kscale_s[st][t] = t < ntok ? reinterpret_cast<const float*>(raw + kRawScaleOff)[t] : 0.f;
+        fence_proxy_async();
+        mbar_arrive(smem_u32(&bar_raw_empty[rs]));
+        mbar_arrive(smem_u32(&bar_kv_full[st]));
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    // Warps 2..9: two warpgroups; warpgroup g handles tile columns [32g, 32g + 32)
+    // of every query row (TMEM lane quarter = warp % 4).
+    const int g = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int64_t grow = (int64_t)rt * kRows + row;          // row within the request
+    const bool real = grow < R;                              // rows past R pad the tile
+    // Shard positions grow with the shard-local index, so the keys a query sees form a
+    // prefix: shard-local tokens below shard_len(qpos + 1) (those at positions <= qpos),
+    // and below j1.  jvis: this row's prefix; jvis_min: every row's (the earliest query).
+    const int jvis = min(j1, shard_len(L - a.Tq + (int)(grow / a.H) + 1, r, a.c, a.I));
+    const int jvis_min = min(j1, shard_len(L - a.Tq + 1, r, a.c, a.I));
+    const float qscale = a.sm_scale * kLog2e;
+    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
+    // this warpgroup's partial sum over its columns, relative to m_own
+    float m_own = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (ntiles > 0) {
+      // this CTA's latent dims of the query row into TMEM as packed 16-bit pairs
+      const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK +
+                                                         h * 256 + g * 128);
+      for (int c16 = 0; c16 < 4; ++c16) {
+        uint32_t rr[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
+          rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) rr[k] = bf16x2_to_f16x2(rr[k]);   // Q as fp16 pairs
+        tmem_st16(tmem + lane_off + kColQ + g * 64 + c16 * 16, rr);
+      }
+      // CTA 1: the rope part of the query row (64 dims) into shared memory in the
+      // 128-byte-swizzle layout the MMA reads, as fp16; pad rows get zeros
+      if (h && g == 0) {
+        const uint4* rsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * R + grow) * kDK + 512);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 v = real ? __ldg(rsrc + u) : make_uint4(0, 0, 0, 0);
+          v.x = bf16x2_to_f16x2(v.x); v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z); v.w = bf16x2_to_f16x2(v.w);
+          *reinterpret_cast<uint4*>(sQr + row * 128 + ((u ^ (row & 7)) << 4)) = v;
+        }
+        fence_proxy_async();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_q_full));
+    }
+    {
+      // both warpgroups on every tile, warpgroup g on tile columns [32g, 32g + 32)
+      const int stid = g * kRows + row;                      // 0..255
+      const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
+      float m_ref = -INFINITY;
+      for (int i = 0; ok && i < ntiles; ++i) {
+        const int sb = i & 1, st = i % kStages;
+        const int t0 = j0 + i * kTileTok;
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t own[32];
+        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g, *reinterpret_cast<uint32_t(*)[16]>(&own[0]));
+        tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
+                  *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
+        tmem_ld_wait();
+        // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
+        // float4), once the peer has read the previous one
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
+                      make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
+        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), i & 1, abort_flag));
+        if (!ok) break;
+        float x[32];
+        const float4* xin = reinterpret_cast<const float4*>(sX);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 pv = xin[(8 * g + c) * kRows + row];
+          const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
+          const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
+          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+          x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
+          x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
+          x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
+          x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
+        }
+        mbar_arrive(smem_u32(&bar_x_read));
+        // the key's per-token scale multiplies its score
+        const float* ks = kscale_s[st] + 32 * g;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] *= ks[k];
+        // causal / tail mask on raw scores (only tiles that need it)
+        if (t0 + kTileTok > jvis_min) {
+          const int lim = jvis - t0 - 32 * g;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = k < lim ? x[k] : -INFINITY;
+        }
+        float tmax = fmaxf(x[0], x[1]);
+#pragma unroll
+        for (int k = 2; k < 32; ++k) tmax = fmaxf(tmax, x[k]);
+        // row max across the two warpgroups; this sync also orders every thread's
+        // S reads before any P write into the same TMEM columns
+        xmax_s[i & 1][g][row] = tmax;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_max[i & 1]));
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
+        // Lazy reference max: move it only when this tile's max exceeds it by more
+        // than 8 (so every weight 2^(x - m_ref) stays <= 256).  Rows that move it
+        // after O holds data rescale O (each warpgroup its 128 columns).
+        const bool move = tmax > m_ref + 8.f;
+        const bool rescale_me = move && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale_me)) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+          for (int q = 0; q < 8; ++q) {
+            uint32_t u[16];
+            const uint32_t oc = tmem + lane_off + kColO + g * 128 + q * 16;
+            tmem_ld16(oc, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+            tmem_st16(oc, u);
+          }
+          l *= alpha;
+        }
+        if (move) m_ref = tmax;
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;    // every x is -inf then
+        const uint32_t pcol = tmem + lane_off + kColS + sb * kTileTok;
+        float ps = 0.f;
+        // fp16 P (2^-11 rounding), pre-multiplied by the value's per-token scale
+        uint32_t pp[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = ex2_approx(fmaf(x[k], qscale, -mr));
+          const float p1 = ex2_approx(fmaf(x[k + 1], qscale, -mr));
+          ps += p0 + p1;
+          pp[k >> 1] = pack_f16(p0 * ks[k], p1 * ks[k + 1]);
+        }
+        tmem_st16(pcol + 16 * g, pp);
+        l += ps;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[sb]));
+      }
+      m_own = m_ref;                                           // the same in both warpgroups
+    }
+    // ---- epilogue ----
+    if (ok && ntiles > 0)
+      // Not bar_o: when the last tile's softmax ends, PV(ntiles - 2) may still be
+      // running, and a parity wait on bar_o would then match an older phase.
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
+    l_s[g][row] = l;
+    m_s[g][row] = m_own;
+    mbar_arrive(smem_u32(&bar_l));
+    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
+    ok = ok && l_ok;
+    // O follows the latest reference (the larger, since the reference only grows);
+    // each warpgroup's sum is brought to it
+    const float m0 = m_s[0][row], m1 = m_s[1][row];
+    const float m_ref = fmaxf(m0, m1);
+    const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_ref)) +
+                        (m1 == -INFINITY ? 0.f : l_s[1][row] * ex2_approx(m1 - m_ref));
+    tc_fence_after();
+    const bool direct = !p.fused && p.num_splits == 1;
+    // workspace slot of this (shard, split): split-major unfused, shard-major fused
+    const int64_t wrow = p.fused ? ((int64_t)(sr * p.num_splits + split) * a.B + b) * R + grow
+                                 : ((int64_t)split * a.B * a.shard_count + bz) * R + grow;
+    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL : p.ws_o + wrow * kDL) +
+                 h * 256 + g * 128;
+    const bool read_o = ok && ntiles > 0;                   // uniform across the warp
+    const bool live = read_o && l_tot > 0.f;
+    const float inv = live ? 1.f / l_tot : 0.f;
+    for (int q = 0; q < 8; ++q) {
+      uint32_t u[16];
+      if (read_o) {
+        tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
+        tmem_ld_wait();
+      }
+      if (!real) continue;
+      float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        d4[v] = live ? make_float4(__uint_as_float(u[4 * v]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
+                                   __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (h == 0 && g == 0 && real) {
+      const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
+      if (direct)
+        a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
+      else
+        p.ws_lse[wrow] = lse2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // the peer may still be writing into this CTA's exchange buffer or barriers
+  cluster_arrive();
+  cluster_wait();
+  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (p.num_splits == 1 && !p.fused) return;
+
+  tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
+}
+
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
     decode_tc_bf16_kernel(const __grid_constant__ TcParams p) {
   decode_tc_bf16_body(p);
 }
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<true>::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(e4::kThreads, 1)
     decode_tc_e4m3_kernel(const __grid_constant__ TcParams p) {
-  decode_tc_body<true>(p);
+  decode_tc_e4m3_body(p);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1478,13 +1254,13 @@ int encode_rows_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
   return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
 
-// E4M3 pool as [rows, 576] bytes; a box {64 codes, box_rows} lands unswizzled.
-int encode_rows_576_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// E4M3 pool as [rows, 576] bytes; a box {box_cols codes, box_rows} lands unswizzled.
+int encode_rows_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return DCPMLA_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)kDK, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kDK};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1611,8 +1387,8 @@ size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
 template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
   auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
-  const int threads = kFp8 ? Cfg<true>::kThreads : b16::kThreads;
-  const size_t smem = kFp8 ? Cfg<true>::kSmemBytes : b16::kSmemBytes;
+  const int threads = kFp8 ? e4::kThreads : b16::kThreads;
+  const size_t smem = kFp8 ? e4::kSmemBytes : b16::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DCPMLA_ERR_CUDA;
   const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
@@ -1637,7 +1413,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   int rc = DCPMLA_OK;
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
     const void* pool = a.kv.pool[a.shard_begin + i];
-    rc = a.fp8 ? encode_rows_576_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows)
+    rc = a.fp8 ? encode_rows_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, 64, (uint32_t)p.box_rows)
                : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
   }
   for (int i = 0; rc == DCPMLA_OK && !a.fp8 && i < a.shard_count; ++i)
