@@ -30,7 +30,7 @@
 //                  S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; Q_h latent dims from TMEM)
 //                  O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
 //     warps 2-9  softmax, two warpgroups on every tile, each 32 of its columns
-//     warps 10-11  E4M3 -> fp16 conversion into the stage ring
+//     warps 10-13  E4M3 -> fp16 conversion into the stage ring (one per SM sub-partition)
 //   TMEM columns: O_h [0,256), S/P double buffer [256,384), Q_h latent [384,512).
 //
 // Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all
@@ -713,7 +713,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
 //                 S_h  = Q_h K_h^T (M 128, N 64, K 256 or 320; latent Q from TMEM)
 //                 O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
 //   warps 2-9   softmax, both warpgroups on every tile, each 32 of its columns
-//   warps 10-11 convert raw tiles into the 3-deep fp16 stage ring
+//   warps 10-13 convert raw tiles into the 3-deep fp16 stage ring (one per SM sub-partition)
 //
 // TMEM columns: O_h [0,256), S/P slots [256,384) (slot = tile % 2, P overwrites S
 // in place; in issue order QK(i + 2) follows PV(i)), Q_h latent [384,512).
@@ -726,8 +726,8 @@ constexpr int kRawChunk = kTileTok * 64;            // 64 tokens x 64 codes
 constexpr int kRawScaleOff = 5 * kRawChunk;         // then the tile's 64 fp32 scales
 constexpr int kRawStage = kRawScaleOff + kTileTok * 4;
 constexpr int kQRope = kRows * 128;                 // CTA 1: 64 rope dims of Q, fp16
-constexpr int kThreads = 384;
-constexpr int kConvThreads = 64;
+constexpr int kThreads = 448;
+constexpr int kConvThreads = 128;
 constexpr size_t kSmemBytes = 1024 + kQRope + kStages * kStage + kXBytes + kRawStages * kRawStage;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 static_assert(kSmemBytes <= 227 * 1024 - 6144, "stages, Q and exchange buffer exceed shared memory");
@@ -937,7 +937,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
     // 128-byte-swizzle positions; rows past the tile's last token are written as
     // zeros.  Also stages the tile's per-token scales.
     if (ntiles > 0) {
-      const int ct = tid - 10 * 32;                           // 0..63
+      const int ct = tid - 10 * 32;                           // 0..127
       for (int i = 0; i < ntiles; ++i) {
         const int rs = i % kRawStages, st = i % kStages;
         const int t0 = j0 + i * kTileTok;
