@@ -75,6 +75,17 @@ SMALL = {
     "ilv8_fp8": W.scaled(W.WORKLOADS["fp8"], B=1, L=2000, interleave=8),
     "ilv2_c16": W.Workload("il16", B=4, H=16, Tq=1, c=16, P=4, kv_dtype="bf16", lse_base="e",
                            seed=23, lengths_mix=(2, 100, 300, 1, 40), interleave=2),
+    # 128-row tensor-core path: 8-token pages (eight page boxes per tile) with odd c, 32-token
+    # pages with causal query pairs, pages longer than a tile with four row tiles per request,
+    # and the E4M3 kernel with 8-token pages; every length leaves a ragged last tile
+    "tc_p8_c3": W.Workload("tcp8", B=2, H=128, Tq=1, c=3, P=8, kv_dtype="bf16", lse_base="e",
+                           seed=25, L=1234),
+    "tc_p32_tq2": W.Workload("tcp32", B=2, H=64, Tq=2, c=2, P=32, kv_dtype="bf16", lse_base="2",
+                             seed=26, L=2101),
+    "tc_p256_tq4": W.Workload("tcp256", B=2, H=128, Tq=4, c=4, P=256, kv_dtype="bf16",
+                              lse_base="2", seed=27, L=3001),
+    "tc_e4m3_p8": W.Workload("tce8", B=2, H=128, Tq=1, c=2, P=8, kv_dtype="e4m3", lse_base="e",
+                             seed=28, L=999),
 }
 
 SENTINEL = 0xA5
@@ -272,7 +283,7 @@ def test_decode_path_per_workload():
 
 FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
                "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
-               "ilv2_c16"]
+               "ilv2_c16", "tc_p8_c3", "tc_p256_tq4"]
 
 
 @needs_cuda
