@@ -129,7 +129,12 @@ struct Unit {
   bool whole;           // every tile of the item: no merge
 };
 
-__device__ __forceinline__ int fh_bound(int T, int k, int G) { return (int)((int64_t)T * k / G); }
+// Start of cluster k's share of the T-tile sequence: floor(T k / G), in 32 bits when T G
+// fits (the common case; a 64-bit division costs several times more).
+__device__ __forceinline__ int fh_bound(int T, int k, int G) {
+  if ((uint32_t)T <= 0xFFFFFFFFu / (uint32_t)G) return (int)((uint32_t)T * (uint32_t)k / (uint32_t)G);
+  return (int)((int64_t)T * k / G);
+}
 
 // The part of item `it` (tiles [pre[it], pre[it + 1]) of the sequence) in the share
 // [t_lo, t_hi) of cluster cl; false if they do not meet.
@@ -154,21 +159,12 @@ __device__ __forceinline__ bool fh_unit(const DecodeArgs& a, const int* pre, int
 
 // The cluster whose share holds tile t (T > 0).
 __device__ __forceinline__ int fh_cluster_of(int T, int t, int G) {
-  const int64_t k0 = (int64_t)t * G / T;
+  const int64_t k0 = (uint32_t)T <= 0xFFFFFFFFu / (uint32_t)G ? (int64_t)((uint32_t)t * (uint32_t)G / (uint32_t)T)
+                                                             : (int64_t)t * G / T;
   int k = (int)(k0 < G - 1 ? k0 : G - 1);
   while (k + 1 < G && fh_bound(T, k + 1, G) <= t) ++k;
   while (k > 0 && fh_bound(T, k, G) > t) --k;
   return k;
-}
-
-// Byte offset of element (row, token t64) in a K-major, 128-byte-swizzled
-// [rows x 64] bf16 tile (8-row atoms of 1 KB).
-__device__ __forceinline__ uint32_t sw128_off(int row, int t64) {
-  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((t64 >> 3) ^ (row & 7))) << 4) + (t64 & 7) * 2);
-}
-
-__device__ __forceinline__ uint16_t bf16_bits(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -933,8 +929,12 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
   FhPlan p{};
-  p.clusters = std::max(1, sm_count / 2);
   const int64_t items = (int64_t)a.B * a.shard_count;
+  // one cluster per SM pair, but no more clusters than tiles can exist: a shard holds at most
+  // max_pages * P of a request's tokens (small problems then launch few clusters and the
+  // combine walks few shares)
+  const int64_t tiles_max = items * (((int64_t)a.max_pages * a.P + kTok - 1) / kTok);
+  p.clusters = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sm_count / 2, tiles_max));
   p.slots = (int32_t)(items + p.clusters);   // partial of item it in cluster k: slot it + k
   p.pre_off = 0;
   p.bad_off = align256((size_t)(items + 1) * 4);
