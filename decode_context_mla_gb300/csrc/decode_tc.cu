@@ -208,8 +208,8 @@ __device__ __noinline__ void tc_combine_tail(const TcParams& p, int b, int bz, i
 // The 64 rope dims are split 32 / 32 between the pair, so both CTAs stream 288 of
 // the 576 key dims (a 36 KB stage).
 //
-//   warp 0      TMA producer; looks page ids up kLook tiles ahead and prefetches the
-//               tile kLook - 1 places ahead into L2 (each CTA half of its rows)
+//   warp 0      TMA producer; page ids from a 32-entry window, the tile kLook - 1
+//               places ahead prefetched into L2 (each CTA half of its rows)
 //   warp 1      TMEM allocation; lane 0 issues QK of every tile
 //   warps 2-9   softmax, warpgroup g takes tiles i with i % 2 == g
 //   warp 10     lane 0 issues PV of every tile
@@ -285,14 +285,14 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
-  int j0 = 0, j1 = 0;
+  int j0 = 0, j1 = 0, npages = 0;
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
     if (tid == 0) atomicOr(&bad_s, DCPMLA_DERR_LENGTH);
   } else {
     const int n = shard_len(L, r, a.c, a.I);
     j0 = min(split * p.chunk, n);
     j1 = min(n, j0 + p.chunk);
-    const int npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
+    npages = (int)(((int64_t)L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
     for (int pg = tid; pg < npages; pg += kThreads) {
       const int32_t g = pt_row[pg];
       if (g < 0 || (int64_t)g >= a.num_pages) atomicOr(&bad_s, DCPMLA_DERR_PAGE);
@@ -313,9 +313,10 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
-    // Lane l loads box l of a tile (box = min(P, 64) rows); the page id of box l of
-    // tile i + k sits in fg[k], so no page-table read is waited on between a stage's
-    // release and its load.  Every page id was range-checked above.
+    // Lane l loads box l of a tile (box = min(P, 64) rows).  The warp keeps a window
+    // of 32 page ids (lane l holds entry win + l), refreshed only when a tile up to
+    // the L2 prefetch distance leaves it (one read of the page table per 32 pages, all
+    // lanes at once).  Every page id was range-checked above.
     if (ntiles > 0) {
       const CUtensorMap* kvmap = &p.tm_kv[sr];
       const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
@@ -327,31 +328,52 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       }
       const int box = p.box_rows;
       const uint8_t* pool = static_cast<const uint8_t*>(a.kv.pool[r]);
-      auto lookup = [&](int tile) -> int {
-        if (tile >= ntiles) return -1;
-        const int t0 = j0 + tile * kTileTok;
-        const int nb = (min(kTileTok, j1 - t0) + box - 1) / box;
-        return lane < nb ? __ldg(pt_row + (t0 + lane * box) / a.P) : -1;
+      int win = -64, win_val = 0, issued = 0;
+      // page id of box `lane` of tile `tile`, if that box exists (all lanes take part)
+      auto box_page = [&](int tile, int& tok, bool& has) -> int {
+        const int tb = j0 + tile * kTileTok;
+        const int nb = (min(kTileTok, j1 - tb) + box - 1) / box;
+        tok = tb + lane * box;
+        has = lane < nb;
+        return __shfl_sync(0xffffffffu, win_val, has ? tok / a.P - win : 0);
       };
-      int fg[kLook];
-#pragma unroll
-      for (int k = 0; k < kLook; ++k) fg[k] = lookup(k);
-      int issued = 0;
+      // L2 prefetch of one tile: a box's rows are contiguous in the pool, and each CTA
+      // of the pair prefetches half of them
+      auto prefetch_tile = [&](int tile) {
+        int tok;
+        bool has;
+        const int g = box_page(tile, tok, has);
+        if (has) {
+          const uint32_t half = (uint32_t)min(box, j1 - tok) * (kDK * 2 / 2);   // a multiple of 16 bytes
+          bulk_prefetch_l2(pool + ((int64_t)g * a.P + tok % a.P) * (kDK * 2) + h * half, half);
+        }
+      };
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
+        const int ip = i + kLook - 1;                        // the tile prefetched into L2
+        const int first = (j0 + i * kTileTok) / a.P;
+        const int last = (j0 + min(ip, ntiles - 1) * kTileTok + kTileTok - 1) / a.P;
+        if (first < win || last >= win + 32) {               // uniform across the warp
+          win = first;
+          win_val = win + lane < npages ? __ldg(pt_row + win + lane) : 0;
+          // the first tiles come from DRAM: pull the ones after tile 0 into L2 at once
+          if (i == 0)
+            for (int k = 1; k < kLook - 1 && k < ntiles; ++k) prefetch_tile(k);
+        }
         if (i >= kStages) {
           bool okw = true;
           if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
         }
-        const int t0 = j0 + i * kTileTok;
-        const int nbox = (min(kTileTok, j1 - t0) + box - 1) / box;
+        int tok;
+        bool has;
+        const int g = box_page(i, tok, has);
+        const int nbox = (min(kTileTok, j1 - (j0 + i * kTileTok)) + box - 1) / box;
         const uint32_t full = smem_u32(&bar_kv_full[st]);
         if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (4 * 128 + 64)));
         __syncwarp();
-        if (lane < nbox) {
-          const int tok = t0 + lane * box;
-          const int y = fg[0] * a.P + tok % a.P;
+        if (has) {
+          const int y = g * a.P + tok % a.P;
           const uint32_t dst = smem_u32(sKV + st * kStage);
           if (p.use3d) {
             tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
@@ -362,16 +384,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
           tma_load_2d(dst + kRopeOff + lane * box * 64, ropemap, 512 + 32 * (int)h, y, full);
         }
         issued = i + 1;
-        // L2 prefetch of the tile kLook - 1 places ahead: a box's rows are contiguous
-        // in the pool, and each CTA of the pair prefetches half of them
-        if (fg[kLook - 1] >= 0) {
-          const int tok = j0 + (i + kLook - 1) * kTileTok + lane * box;
-          const uint32_t half = (uint32_t)min(box, j1 - tok) * (kDK * 2 / 2);   // a multiple of 16 bytes
-          bulk_prefetch_l2(pool + ((int64_t)fg[kLook - 1] * a.P + tok % a.P) * (kDK * 2) + h * half, half);
-        }
-#pragma unroll
-        for (int k = 0; k + 1 < kLook; ++k) fg[k] = fg[k + 1];
-        fg[kLook - 1] = lookup(i + kLook);
+        if (ip < ntiles) prefetch_tile(ip);
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -484,35 +497,42 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     if (ntiles > 0) {
       const __nv_bfloat16* qrow = a.q + ((int64_t)b * R + grow) * kDK;
       if (g == 0) {
-        // query dims [256h, 256h+128) into TMEM as packed 16-bit pairs
+        // query dims [256h, 256h+128) into TMEM as packed 16-bit pairs (every load in
+        // flight before the first store)
         const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256);
+        uint4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = real ? __ldg(qsrc + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
           uint32_t rr[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 u = real ? __ldg(qsrc + c16 * 4 + v) : make_uint4(0, 0, 0, 0);
-            rr[v * 4 + 0] = u.x; rr[v * 4 + 1] = u.y; rr[v * 4 + 2] = u.z; rr[v * 4 + 3] = u.w;
+          for (int k = 0; k < 4; ++k) {
+            const uint4 u = v[c16 * 4 + k];
+            rr[k * 4 + 0] = u.x; rr[k * 4 + 1] = u.y; rr[k * 4 + 2] = u.z; rr[k * 4 + 3] = u.w;
           }
           tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
         }
         tmem_st_wait();
       } else {
         // dims [256h+128, 256h+256) as two 128-byte-swizzle chunks and the rope dims
-        // [512+32h, 544+32h) with a 64-byte swizzle, in the layouts the MMA reads
+        // [512+32h, 544+32h) with a 64-byte swizzle, in the layouts the MMA reads (every
+        // load in flight before the first store)
         const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256 + 128);
+        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + 512 + 32 * h);
+        uint4 v[20];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = real ? __ldg(qsrc + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[16 + k] = real ? __ldg(rsrc + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 v = real ? __ldg(qsrc + cl * 8 + u) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sQ + cl * kQChunk + row * 128 + ((u ^ (row & 7)) << 4)) = v;
-          }
-        const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + 512 + 32 * h);
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(sQ + cl * kQChunk + row * 128 + ((u ^ (row & 7)) << 4)) = v[cl * 8 + u];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = real ? __ldg(rsrc + u) : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sQ + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) = v;
-        }
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(sQ + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) = v[16 + u];
         fence_proxy_async();
       }
       tc_fence_before();
@@ -660,24 +680,36 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // workspace slot of this (shard, split): split-major unfused, shard-major fused
     const int64_t wrow = p.fused ? ((int64_t)(sr * p.num_splits + split) * a.B + b) * R + grow
                                  : ((int64_t)split * a.B * a.shard_count + bz) * R + grow;
-    float* dst = (direct ? a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL : p.ws_o + wrow * kDL) +
-                 h * 256 + g * 128;
+    // row 0 of this 128-row tile in o_part, or in the workspace slot
+    const int64_t row0 = direct ? ((int64_t)sr * a.B + b) * R + (int64_t)rt * kRows : wrow - grow + (int64_t)rt * kRows;
+    float* obuf = (direct ? a.o_part : p.ws_o) + row0 * kDL + h * 256 + g * 128;
     const bool read_o = ok && ntiles > 0;                   // uniform across the warp
     const bool live = read_o && l_tot > 0.f;
     const float inv = live ? 1.f / l_tot : 0.f;
+    // O leaves through shared memory (the stage ring and exchange buffers are idle now:
+    // every MMA and every exchange has completed): each thread writes its row's 128
+    // normalised values as 16-byte units, unit u at u ^ (row % 8), then each warp
+    // stores whole 512-byte rows, 32 lanes x 16 bytes
+    uint8_t* stg = sKV + g * (kRows * 512);
     for (int q = 0; q < 8; ++q) {
       uint32_t u[16];
       if (read_o) {
         tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, u);
         tmem_ld_wait();
       }
-      if (!real) continue;
-      float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        d4[v] = live ? make_float4(__uint_as_float(u[4 * v]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
-                                   __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int v = 0; v < 4; ++v) {
+        const float4 f = live ? make_float4(__uint_as_float(u[4 * v]) * inv, __uint_as_float(u[4 * v + 1]) * inv,
+                                            __uint_as_float(u[4 * v + 2]) * inv, __uint_as_float(u[4 * v + 3]) * inv)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(stg + row * 512 + (((q * 4 + v) ^ (row & 7)) << 4)) = f;
+      }
+    }
+    named_bar_sync(1 + g, kWgThreads);
+    for (int rr = quarter * 32; rr < quarter * 32 + 32; ++rr) {
+      if ((int64_t)rt * kRows + rr >= R) break;             // rows past R pad the tile
+      const float4 f = *reinterpret_cast<const float4*>(stg + rr * 512 + ((lane ^ (rr & 7)) << 4));
+      reinterpret_cast<float4*>(obuf + (int64_t)rr * kDL)[lane] = f;
     }
     if (h == 0 && g == 0 && real) {
       const float lse2 = live ? m_ref + log2f(l_tot) : -INFINITY;
