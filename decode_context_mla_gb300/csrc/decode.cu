@@ -99,6 +99,7 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
     n = 2;   // decode + merge of split units
   } else if (tc_supported(a)) {
     pth = DCPMLA_PATH_TC_ROWS;
+    n = tc_kernel_launches(a);
   }
   if (path) *path = pth;
   if (kernel_launches) *kernel_launches = B == 0 ? 0 : n;

@@ -44,6 +44,8 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
 // Tensor-core path (tcgen05 / TMEM / TMA): 128-row query tiles, bf16 or e4m3 KV.
 bool tc_supported(const DecodeArgs& a);
 size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused = false);
+// kernel launches of one launch_decode_tc call (the persistent bf16 grid: prefix, decode, combine)
+int tc_kernel_launches(const DecodeArgs& a, bool fused = false);
 // fused: as for launch_decode_fh (every shard and split merged into o, lse).
 int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
                      bool fused = false);

@@ -57,6 +57,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kWgThreads = 128;                     // one softmax warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitCycles = 2000000000LL;     // about one second
+constexpr int kMaxCombineParts = 80;                // clusters one item may span (<= SM pairs)
 
 struct TcParams {
   CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
@@ -71,6 +72,10 @@ struct TcParams {
   float* ws_lse;
   uint32_t* ws_cnt;
   int32_t fused;                      // 1: merge all shards and splits of a row tile into o, lse
+  // persistent bf16 grid: tile prefix sums over items, per-slot bad-page flags, clusters
+  int32_t* ws_pre;
+  int32_t* ws_bad;
+  int32_t clusters, items;
 };
 
 template <bool kCluster>
@@ -734,6 +739,697 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
   tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
 }
 
+// ------------------------------------------------------------ bf16 KV, persistent grid
+// The same tile pipeline as decode_tc_bf16_body, run by a persistent grid: the 64-token
+// tiles of all items (item = request, shard, 128-row tile) form one sequence of T tiles
+// and cluster k takes the contiguous share [T k / G, T (k + 1) / G).  The stage ring, the
+// S/P slots and the score exchange run on across item boundaries; at a boundary the
+// softmax warpgroups write the finished unit's O (after its last PV) and load the next
+// unit's Q, and the next unit's first PV waits until O has been read.  A unit that covers
+// its whole item writes o_part and lse_part; an item cut by share boundaries leaves one
+// partial per unit in workspace slot item + k (unique: a later cluster starts at the same
+// or a later item), merged by tc_unit_combine_kernel, which also writes the empty output
+// of items with no tiles.  The tile prefix sums come from tc_prefix_kernel.
+namespace pp {
+constexpr int kUnitFlags = 8;                       // ring of per-unit bad-page flags
+
+// Start of cluster k's share of T tiles: floor(T k / G) (32-bit when T G fits).
+__host__ __device__ __forceinline__ int bound(int T, int k, int G) {
+  if ((uint32_t)T <= 0xFFFFFFFFu / (uint32_t)G) return (int)((uint32_t)T * (uint32_t)k / (uint32_t)G);
+  return (int)((int64_t)T * k / G);
+}
+__device__ __forceinline__ int cluster_of(int T, int t, int G) {
+  int k = (int)((int64_t)t * G / T);
+  k = min(k, G - 1);
+  while (k + 1 < G && bound(T, k + 1, G) <= t) ++k;
+  while (k > 0 && bound(T, k, G) > t) --k;
+  return k;
+}
+
+struct Unit {
+  int it, b, sr, r, rt, L, j0, j1, ntiles, slot;
+  bool whole;                                       // the unit covers its whole item
+};
+// The part of item `it` (tiles [pre[it], pre[it + 1])) in the share [t_lo, t_hi) of
+// cluster k; false if they do not meet.
+__device__ __forceinline__ bool unit_of(const TcParams& p, int it, int t_lo, int t_hi, int k, Unit& u) {
+  const int s0 = __ldg(p.ws_pre + it), s1 = __ldg(p.ws_pre + it + 1);
+  const int s = max(s0, t_lo), e = min(s1, t_hi);
+  if (e <= s) return false;
+  const DecodeArgs& a = p.a;
+  const int bz = it / p.row_tiles;
+  u.it = it;
+  u.rt = it % p.row_tiles;
+  u.b = bz / a.shard_count;
+  u.sr = bz % a.shard_count;
+  u.r = a.shard_begin + u.sr;
+  u.L = __ldg(a.seq_lens + u.b);
+  const int n = shard_len(u.L, u.r, a.c, a.I);
+  u.j0 = (s - s0) * kTileTok;
+  u.j1 = min(n, (e - s0) * kTileTok);
+  u.ntiles = e - s;
+  u.slot = it + k;
+  u.whole = s == s0 && e == s1;
+  return true;
+}
+// First item whose tiles reach past t_lo.
+__device__ __forceinline__ int first_item(const TcParams& p, int t_lo) {
+  int lo = 0, hi = p.items - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.ws_pre + mid + 1) > t_lo) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+}  // namespace pp
+
+// Tiles per item (0 for a request whose length fails the check, which is reported) and
+// their exclusive prefix sums pre[0 .. items]; one block.
+__global__ void __launch_bounds__(1024) tc_prefix_kernel(const DecodeArgs a, int row_tiles, int items,
+                                                         int32_t* __restrict__ pre) {
+  __shared__ int32_t warp_sum[32];
+  __shared__ int32_t carry_s;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  if (t == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < items; base += 1024) {
+    const int it = base + t;
+    int v = 0;
+    if (it < items) {
+      const int bz = it / row_tiles, b = bz / a.shard_count, r = a.shard_begin + bz % a.shard_count;
+      const int L = a.seq_lens[b];
+      if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
+        if (bz % a.shard_count == 0 && it % row_tiles == 0) set_err(a.err, DCPMLA_DERR_LENGTH);
+      } else {
+        v = (shard_len(L, r, a.c, a.I) + kTileTok - 1) / kTileTok;
+      }
+    }
+    int x = v;   // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int s = warp_sum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sum[lane] = s;
+    }
+    __syncthreads();
+    const int carry = carry_s;
+    const int incl = x + (w > 0 ? warp_sum[w - 1] : 0) + carry;
+    if (it < items) pre[it + 1] = incl;
+    if (base == 0 && t == 0) pre[0] = 0;
+    __syncthreads();
+    if (t == 1023) carry_s = incl;
+    __syncthreads();
+  }
+}
+
+// Merges the partials of each item cut by share boundaries (exact LSE merge, base 2) into
+// o_part / lse_part, and writes the empty output (o = 0, lse = -inf) of items with no
+// tiles.  An item any part of which met a bad page is written as empty.  One block of 256
+// threads per (item, group of 16 rows of its 128-row tile): the item's cluster range and
+// each row's merge weights are formed once, then the rows stream through as float4s.
+namespace pp {
+constexpr int kCombineRows = 16;
+}
+__global__ void __launch_bounds__(256) tc_unit_combine_kernel(const TcParams p) {
+  const DecodeArgs& a = p.a;
+  const int item = blockIdx.x, r0 = blockIdx.y * pp::kCombineRows, t = threadIdx.x;
+  const int bz = item / p.row_tiles, rt = item % p.row_tiles;
+  const int b = bz / a.shard_count, sr = bz % a.shard_count;
+  const int64_t R = a.R;
+  const int G = p.clusters;
+  __shared__ int k0_s, k1_s, bad_s;
+  __shared__ float w_s[pp::kCombineRows][kMaxCombineParts];
+  if (t == 0) {
+    const int T = p.ws_pre[p.items], s0 = p.ws_pre[item], s1 = p.ws_pre[item + 1];
+    int k0 = 0, k1 = -1, bad = 0;
+    if (s1 > s0) {
+      k0 = pp::cluster_of(T, s0, G);
+      k1 = pp::cluster_of(T, s1 - 1, G);
+      for (int k = k0; k <= k1 && k0 != k1; ++k)
+        if (pp::bound(T, k, G) != pp::bound(T, k + 1, G)) bad |= p.ws_bad[item + k];
+    }
+    k0_s = k0;
+    k1_s = k1;
+    bad_s = bad;
+  }
+  __syncthreads();
+  const int k0 = k0_s, k1 = k1_s;
+  if (k1 >= k0 && k0 == k1) return;                    // one unit: written by the decode
+  const int nparts = k1 - k0 + 1;                        // 0 for an item with no tiles
+  // per row: the merged LSE and each part's weight (0 for a cluster with an empty share)
+  if (t < pp::kCombineRows) {
+    const int row = r0 + t;
+    const int64_t grow = (int64_t)rt * kRows + row;
+    float lse2 = -INFINITY;
+    if (nparts > 0 && !bad_s) {
+      const int T = p.ws_pre[p.items];
+      float m = -INFINITY;
+      for (int k = k0; k <= k1; ++k)
+        if (pp::bound(T, k, G) != pp::bound(T, k + 1, G)) m = fmaxf(m, p.ws_lse[(int64_t)(item + k) * kRows + row]);
+      if (m != -INFINITY) {
+        float sum = 0.f;
+        for (int k = k0; k <= k1; ++k)
+          if (pp::bound(T, k, G) != pp::bound(T, k + 1, G)) sum += exp2f(p.ws_lse[(int64_t)(item + k) * kRows + row] - m);
+        lse2 = m + log2f(sum);
+      }
+      for (int k = k0; k <= k1; ++k)
+        w_s[t][k - k0] = (lse2 == -INFINITY || pp::bound(T, k, G) == pp::bound(T, k + 1, G))
+                             ? 0.f : exp2f(p.ws_lse[(int64_t)(item + k) * kRows + row] - lse2);
+    } else {
+      for (int k = 0; k < nparts; ++k) w_s[t][k] = 0.f;
+    }
+    if (grow < R) a.lse_part[((int64_t)sr * a.B + b) * R + grow] = a.base2 ? lse2 : lse2 * kLn2;
+  }
+  __syncthreads();
+  for (int e = t; e < pp::kCombineRows * (kDL / 4); e += 256) {
+    const int rr = e / (kDL / 4), c4 = e % (kDL / 4), row = r0 + rr;
+    const int64_t grow = (int64_t)rt * kRows + row;
+    if (grow >= R) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < nparts; ++k) {
+      const float w = w_s[rr][k];
+      if (w == 0.f) continue;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(p.ws_o + ((int64_t)(item + k0 + k) * kRows + row) * kDL) + c4);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL)[c4] = acc;
+  }
+}
+
+__device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
+  using namespace b16;
+  const DecodeArgs& a = p.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                                    // Q dims [256h+128, 256h+256) + rope piece
+  uint8_t* sKV = sQ + kQBytes;                           // kStages x kStage
+  uint8_t* sX = sKV + kStages * kStage;                  // the peer's partial scores, per warpgroup
+  __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full[kStages], bar_p_full[kStages];
+  __shared__ uint64_t bar_o_par[2], bar_mref[2], bar_x_full[2], bar_x_empty[2], bar_x_read[2];
+  __shared__ uint64_t bar_q_full, bar_o_full, bar_o_free, bar_drain_qk, bar_drain_pv, bar_l;
+  __shared__ float mref_s[2][kRows];                     // a warpgroup's reference max after its tile
+  __shared__ float l_s[2][kRows], m_s[2][kRows];
+  __shared__ int unit_bad_s[pp::kUnitFlags];             // unit u met a bad page: entry u % 8
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
+  const uint32_t peer = h ^ 1u;
+  const int k = blockIdx.x >> 1, G = p.clusters;
+  const int64_t R = a.R;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+      mbar_init(smem_u32(&bar_s_full[s]), 1);
+      mbar_init(smem_u32(&bar_p_full[s]), kWgThreads);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bar_o_par[s]), 1);
+      mbar_init(smem_u32(&bar_mref[s]), kWgThreads);
+      mbar_init(smem_u32(&bar_x_full[s]), 1);
+      mbar_init(smem_u32(&bar_x_empty[s]), 1);                 // the peer's relay thread
+      mbar_init(smem_u32(&bar_x_read[s]), kWgThreads);
+    }
+    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);         // once per unit
+    mbar_init(smem_u32(&bar_o_full), 1);                        // once per unit
+    mbar_init(smem_u32(&bar_o_free), kSoftmaxThreads);         // once per unit
+    mbar_init(smem_u32(&bar_drain_qk), 1);
+    mbar_init(smem_u32(&bar_drain_pv), 1);
+    mbar_init(smem_u32(&bar_l), kSoftmaxThreads);              // once per unit
+    abort_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  const int T = __ldg(p.ws_pre + p.items);
+  const int t_lo = pp::bound(T, k, G), t_hi = pp::bound(T, k + 1, G);
+  const int it0 = t_hi > t_lo ? pp::first_item(p, t_lo) : p.items;
+  __syncthreads();
+  // both CTAs' barriers are initialised before either touches the other's
+  cluster_arrive();
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    // Per unit: the request's page ids as a 32-entry window (lane l holds entry win + l),
+    // the unit's Q rows prefetched into L2 for the softmax, then its tiles into the ring
+    // (gi counts tiles across units).  A page id outside the pools is reported, its unit
+    // marked bad (its output is written empty) and page 0 loaded in its place.
+    const int box = p.box_rows;
+    int gi = 0, issued = 0, ui = 0;
+    bool ok = true;
+    for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
+      pp::Unit u;
+      if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
+      const CUtensorMap* kvmap = &p.tm_kv[u.sr];
+      const CUtensorMap* kvmap3 = &p.tm_kv3[u.sr];
+      const CUtensorMap* ropemap = &p.tm_rope[u.sr];
+      const uint8_t* pool = static_cast<const uint8_t*>(a.kv.pool[u.r]);
+      const int32_t* pt_row = a.pt + (int64_t)u.b * a.max_pages;
+      const int npages = (int)(((int64_t)u.L + (int64_t)a.P * a.c - 1) / ((int64_t)a.P * a.c));
+      if (lane == 0) {
+        unit_bad_s[ui % pp::kUnitFlags] = 0;
+        prefetch_tmap(kvmap);
+        prefetch_tmap(ropemap);
+        if (p.use3d) prefetch_tmap(kvmap3);
+        // this unit's query rows (contiguous), each CTA of the pair half of them
+        const int64_t q0 = (int64_t)u.b * R + (int64_t)u.rt * kRows;
+        const uint32_t half = (uint32_t)min((int64_t)kRows, R - (int64_t)u.rt * kRows) * (kDK * 2 / 2);
+        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(a.q + q0 * kDK) + h * half, half);
+      }
+      __syncwarp();
+      int win = -64, win_val = 0;
+      auto box_page = [&](int tile, int& tok, bool& has) -> int {
+        const int tb = u.j0 + tile * kTileTok;
+        const int nb = (min(kTileTok, u.j1 - tb) + box - 1) / box;
+        tok = tb + lane * box;
+        has = lane < nb;
+        int g = __shfl_sync(0xffffffffu, win_val, has ? tok / a.P - win : 0);
+        if (has && (g < 0 || (int64_t)g >= a.num_pages)) {
+          unit_bad_s[ui % pp::kUnitFlags] = 1;
+          set_err(a.err, DCPMLA_DERR_PAGE);
+          g = 0;
+        }
+        return g;
+      };
+      for (int i = 0; i < u.ntiles; ++i, ++gi) {
+        const int st = gi % kStages;
+        const int ip = i + kLook - 1;                      // the unit's tile prefetched into L2
+        const int first = (u.j0 + i * kTileTok) / a.P;
+        const int last = (u.j0 + min(ip, u.ntiles - 1) * kTileTok + kTileTok - 1) / a.P;
+        if (first < win || last >= win + 32) {             // uniform across the warp
+          win = first;
+          win_val = win + lane < npages ? __ldg(pt_row + win + lane) : 0;
+        }
+        if (gi >= kStages) {
+          bool okw = true;
+          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((gi / kStages) - 1) & 1, abort_flag);
+          if (!__shfl_sync(0xffffffffu, (int)okw, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        int tok;
+        bool has;
+        const int g = box_page(i, tok, has);
+        const int nbox = (min(kTileTok, u.j1 - (u.j0 + i * kTileTok)) + box - 1) / box;
+        const uint32_t full = smem_u32(&bar_kv_full[st]);
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * (4 * 128 + 64)));
+        __syncwarp();
+        if (has) {
+          const int y = g * a.P + tok % a.P;
+          const uint32_t dst = smem_u32(sKV + st * kStage);
+          if (p.use3d) {
+            tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
+          } else {
+            for (int cl = 0; cl < 4; ++cl)
+              tma_load_2d(dst + cl * kChunk + lane * box * 128, kvmap, (int)(4 * h + cl) * 64, y, full);
+          }
+          tma_load_2d(dst + kRopeOff + lane * box * 64, ropemap, 512 + 32 * (int)h, y, full);
+        }
+        issued = gi + 1;
+        if (ip < u.ntiles) {
+          int tokp;
+          bool hasp;
+          const int gp = box_page(ip, tokp, hasp);
+          if (hasp) {
+            const uint32_t half = (uint32_t)min(box, u.j1 - tokp) * (kDK * 2 / 2);   // a multiple of 16 bytes
+            bulk_prefetch_l2(pool + ((int64_t)gp * a.P + tokp % a.P) * (kDK * 2) + h * half, half);
+          }
+        }
+      }
+      ++ui;
+    }
+    if (lane == 0 && *abort_flag) {
+      // let copies already in flight land before the CTA's shared memory goes away
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
+               clock64() - t0 < kWaitCycles / 8) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ QK issuer
+    // S(gi) = Q_h K_h(gi)^T into slot gi % 3, once the unit's Q is loaded; the slot is
+    // free once tile gi - 3's PV completed, which its stage's release implies.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
+      const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
+      const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
+      const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
+      const uint32_t tq = tmem + kColQ;
+      int gi = 0, ui = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
+        pp::Unit u;
+        if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
+        if (!wait_bar<false>(smem_u32(&bar_q_full), ui & 1, abort_flag)) break;
+        tc_fence_after();
+        for (int i = 0; i < u.ntiles; ++i, ++gi) {
+          const int st = gi % kStages;
+          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (gi / kStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + st * kTileTok;
+          const uint64_t so = (uint64_t)((st * kStage) >> 4);
+#pragma unroll
+          for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(d, tq + cl * 32 + kk * 8, kd0 + so + ((cl * kChunk + kk * 32) >> 4), idesc_qk, (cl | kk) != 0);
+#pragma unroll
+          for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(d, qd0 + ((cl * kQChunk + kk * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + kk * 32) >> 4),
+                     idesc_qk, 1u);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) mma_ss(d, qr0 + ((kk * 32) >> 4), kr0 + so + ((kk * 32) >> 4), idesc_qk, 1u);
+          mma_commit(smem_u32(&bar_s_full[st]));
+        }
+        ++ui;
+      }
+      mma_commit(smem_u32(&bar_drain_qk));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ PV issuer
+    // O_h += P(gi) V_h(gi); a unit's first PV overwrites O, once the softmax has read the
+    // previous unit's O; its last PV commits the unit's O.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
+      const uint32_t to = tmem + kColO;
+      int gi = 0, ui = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
+        pp::Unit u;
+        if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
+        for (int i = 0; i < u.ntiles; ++i, ++gi) {
+          const int st = gi % kStages;
+          if (!wait_bar<false>(smem_u32(&bar_p_full[st]), (gi / kStages) & 1, abort_flag) ||
+              (i == 0 && ui > 0 && !wait_bar<false>(smem_u32(&bar_o_free), (ui - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
+          const uint32_t pa = tmem + kColS + st * kTileTok;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(to, pa + kk * 8, vd + (((kk & 3) * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_kv_empty[st]));
+          mma_commit(smem_u32(&bar_o_par[gi & 1]));
+          if (i == u.ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // the unit's O is complete
+        }
+        ++ui;
+      }
+      mma_commit(smem_u32(&bar_drain_pv));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+  } else if (warp == 11) {
+    // ---------------------------------------------------------------- relay
+    if (lane == 0) {
+      for (int gi = 0; gi < t_hi - t_lo; ++gi) {
+        if (!wait_bar<false>(smem_u32(&bar_x_read[gi & 1]), (gi >> 1) & 1, abort_flag)) break;
+        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[gi & 1]), peer));
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    // Per unit: load the unit's Q, take the unit's tiles with gi % 2 == g (each thread one
+    // query row over a tile's 64 columns), then write the unit's O and LSE.
+    const int g = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float qscale = a.sm_scale * kLog2e;
+    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
+    int gi = 0, ui = 0;
+    bool ok = true;
+    for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
+      pp::Unit u;
+      if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
+      const int64_t grow = (int64_t)u.rt * kRows + row;      // row within the request
+      const bool real = grow < R;                            // rows past R pad the tile
+      // the keys a query sees form a prefix of the shard's tokens (positions <= qpos)
+      const int jvis = min(u.j1, shard_len(u.L - a.Tq + (int)(grow / a.H) + 1, u.r, a.c, a.I));
+      const int jvis_min = min(u.j1, shard_len(u.L - a.Tq + 1, u.r, a.c, a.I));
+      {
+        // the unit's Q (every QK of the previous unit has completed: its O was read)
+        const __nv_bfloat16* qrow = a.q + ((int64_t)u.b * R + grow) * kDK;
+        if (g == 0) {
+          const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256);
+          uint4 v[16];
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) v[kk] = real ? __ldg(qsrc + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t rr[16];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint4 w4 = v[c16 * 4 + kk];
+              rr[kk * 4 + 0] = w4.x; rr[kk * 4 + 1] = w4.y; rr[kk * 4 + 2] = w4.z; rr[kk * 4 + 3] = w4.w;
+            }
+            tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
+          }
+          tmem_st_wait();
+        } else {
+          const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256 + 128);
+          const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + 512 + 32 * h);
+          uint4 v[20];
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) v[kk] = real ? __ldg(qsrc + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) v[16 + kk] = real ? __ldg(rsrc + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int cl = 0; cl < 2; ++cl)
+#pragma unroll
+            for (int uu = 0; uu < 8; ++uu)
+              *reinterpret_cast<uint4*>(sQ + cl * kQChunk + row * 128 + ((uu ^ (row & 7)) << 4)) = v[cl * 8 + uu];
+#pragma unroll
+          for (int uu = 0; uu < 4; ++uu)
+            *reinterpret_cast<uint4*>(sQ + kQRopeOff + row * 64 + ((uu ^ ((row >> 1) & 3)) << 4)) = v[16 + uu];
+          fence_proxy_async();
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_q_full));
+      }
+      float m_own = -INFINITY, l = 0.f;
+      const int gs = gi;                                     // the unit's first tile
+      for (int i = (g - gs) & 1; ok && i < u.ntiles; i += 2) {
+        const int gt = gs + i;                               // tile index in the share, gt % 2 == g
+        const int st = gt % kStages;
+        const int t0 = u.j0 + i * kTileTok;
+        const int ntok = min(kTileTok, u.j1 - t0);
+        const uint32_t scol = tmem + lane_off + kColS + st * kTileTok;
+        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (gt / kStages) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        // send this CTA's partial into the peer's buffer g, once the peer has read what
+        // this warpgroup sent two tiles ago
+        if (gt >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((gt >> 1) - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+        const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
+        float x[64];
+        uint32_t* xb = reinterpret_cast<uint32_t*>(x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld16(scol + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(xb + 16 * q));
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_async_v4(x_remote + g * kXBytes + (c * kRows + row) * 16,
+                      make_uint4(xb[4 * c], xb[4 * c + 1], xb[4 * c + 2], xb[4 * c + 3]), xfull_remote);
+        if (row == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (gt >> 1) & 1, abort_flag));
+        if (!ok) break;
+        const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 pv = xin[c * kRows + row];
+          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
+          float* xx = x + 4 * c;
+          xx[0] = h ? pv.x + xx[0] : xx[0] + pv.x;
+          xx[1] = h ? pv.y + xx[1] : xx[1] + pv.y;
+          xx[2] = h ? pv.z + xx[2] : xx[2] + pv.z;
+          xx[3] = h ? pv.w + xx[3] : xx[3] + pv.w;
+        }
+        mbar_arrive(smem_u32(&bar_x_read[g]));
+        if (t0 + kTileTok > jvis_min) {
+          const int lim = jvis - t0;
+#pragma unroll
+          for (int kk = 0; kk < 64; ++kk) x[kk] = kk < lim ? x[kk] : -INFINITY;
+        }
+        float mx[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int kk = 4; kk < 64; ++kk) mx[kk & 3] = fmaxf(mx[kk & 3], x[kk]);
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * qscale;
+        // the reference max as the unit's previous tile (the other warpgroup's) left it
+        float m_ref = -INFINITY;
+        if (i >= 1) {
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[g ^ 1]), ((gt - 1) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          m_ref = mref_s[g ^ 1][row];
+        }
+        // lazy reference max; a row that moves it after O holds data rescales its O
+        // columns once PV of tile gt - 1 has completed (PV(gt - 3) had: S(gt) reused its slot)
+        const bool move = tmax > m_ref + 8.f;
+        const bool rescale_me = move && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale_me)) {
+          ok = __all_sync(0xffffffffu,
+                          wait_bar<false>(smem_u32(&bar_o_par[(gt - 1) & 1]), ((gt - 1) >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
+          for (int q = 0; q < 16; ++q) {
+            uint32_t w16[16];
+            const uint32_t oc = tmem + lane_off + kColO + q * 16;
+            tmem_ld16(oc, w16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) w16[kk] = __float_as_uint(__uint_as_float(w16[kk]) * alpha);
+            tmem_st16(oc, w16);
+          }
+          tmem_st_wait();
+        }
+        if (move) m_ref = tmax;
+        mref_s[g][row] = m_ref;
+        mbar_arrive(smem_u32(&bar_mref[g]));
+        if (m_own != m_ref) {
+          l = m_own == -INFINITY ? 0.f : l * ex2_approx(m_own - m_ref);
+          m_own = m_ref;
+        }
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // every x is -inf then
+        float ps = 0.f;
+        // P as a bf16 pair P = hi + lo (hi = bf16(p), lo = bf16(p - hi))
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int kk = 0; kk < 32; kk += 2) {
+            const int k2 = 32 * half + kk;
+            const float p0 = ex2_approx(fmaf(x[k2], qscale, -mr));
+            const float p1 = ex2_approx(fmaf(x[k2 + 1], qscale, -mr));
+            ps += p0 + p1;
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+            const float2 hf = __bfloat1622float2(hh);
+            hi[kk >> 1] = *reinterpret_cast<const uint32_t*>(&hh);
+            lo[kk >> 1] = pack_bf16(p0 - hf.x, p1 - hf.y);
+          }
+          tmem_st16(scol + 16 * half, hi);
+          tmem_st16(scol + 32 + 16 * half, lo);
+        }
+        if (ntok < kTileTok) {
+          // rows past the unit's last token hold stale data: zero this CTA's V rows
+          uint4* v = reinterpret_cast<uint4*>(sKV + st * kStage);
+          const int tail = kTileTok - ntok;
+          for (int e = row; e < 4 * tail * 8; e += kWgThreads) {
+            const int cch = e / (tail * 8), rem = e % (tail * 8);
+            v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        l += ps;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p_full[st]));
+      }
+      gi = gs + u.ntiles;
+      // ---- the unit's epilogue ----
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), ui & 1, abort_flag));
+      l_s[g][row] = l;
+      m_s[g][row] = m_own;
+      mbar_arrive(smem_u32(&bar_l));
+      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), ui & 1, abort_flag)) && ok;
+      const float m0 = m_s[0][row], m1 = m_s[1][row];
+      const float m_tot = fmaxf(m0, m1);
+      const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_tot)) +
+                          (m1 == -INFINITY ? 0.f : l_s[1][row] * ex2_approx(m1 - m_tot));
+      tc_fence_after();
+      const bool bad = unit_bad_s[ui % pp::kUnitFlags] != 0;
+      const bool live = ok && !bad && l_tot > 0.f;
+      const float inv = live ? 1.f / l_tot : 0.f;
+      const int64_t orow = ((int64_t)u.sr * a.B + u.b) * R + grow;
+      const int64_t wrow = (int64_t)u.slot * kRows + row;
+      float* dst = (u.whole ? a.o_part + orow * kDL : p.ws_o + wrow * kDL) + h * 256 + g * 128;
+      for (int q = 0; q < 8; ++q) {
+        uint32_t w16[16];
+        if (ok) {
+          tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, w16);
+          tmem_ld_wait();
+        }
+        if (!real) continue;
+        float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          d4[v] = live ? make_float4(__uint_as_float(w16[4 * v]) * inv, __uint_as_float(w16[4 * v + 1]) * inv,
+                                     __uint_as_float(w16[4 * v + 2]) * inv, __uint_as_float(w16[4 * v + 3]) * inv)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (h == 0 && g == 0 && real) {
+        const float lse2 = live ? m_tot + log2f(l_tot) : -INFINITY;
+        if (u.whole)
+          a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
+        else
+          p.ws_lse[wrow] = lse2;
+      }
+      if (!u.whole && h == 0 && g == 0 && row == 0) p.ws_bad[u.slot] = bad ? 1 : 0;
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_o_free));
+      ++ui;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // the peer may still be writing into this CTA's exchange buffers or barriers
+  cluster_arrive();
+  cluster_wait();
+  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
+    decode_tc_bf16_persist_kernel(const __grid_constant__ TcParams p) {
+  decode_tc_bf16_persist_body(p);
+}
+
 // ------------------------------------------------------------ E4M3 KV
 // E4M3 codes (one fp32 scale per token) are converted exactly to fp16 stages and
 // every MMA runs in fp16 (E4M3 is a subset of fp16).  CTA 0 owns key dims
@@ -1334,6 +2030,38 @@ struct TcPlan {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Persistent bf16 grid (unfused calls): G clusters over the tile sequence of all items,
+// workspace = tile prefix sums, then per slot (item + cluster) a bad flag, 128 LSEs and
+// 128 output rows for the partial of an item cut by share boundaries.
+struct PpPlan {
+  int32_t clusters, items, row_tiles, slots;
+  size_t pre_off, bad_off, lse_off, o_off, bytes;
+};
+
+PpPlan plan_pp(const DecodeArgs& a, int sm_count) {
+  PpPlan p{};
+  p.row_tiles = (a.R + kRows - 1) / kRows;
+  p.items = (int32_t)((int64_t)a.B * a.shard_count * p.row_tiles);
+  const int64_t tiles_item = ((int64_t)a.max_pages * a.P + kTileTok - 1) / kTileTok;   // a shard's share bound
+  p.clusters = (int32_t)std::max<int64_t>(
+      1, std::min<int64_t>(std::min(sm_count / 2, kMaxCombineParts), (int64_t)p.items * tiles_item));
+  p.slots = p.items + p.clusters;
+  p.pre_off = 0;
+  p.bad_off = align256((size_t)(p.items + 1) * 4);
+  p.lse_off = p.bad_off + align256((size_t)p.slots * 4);
+  p.o_off = p.lse_off + align256((size_t)p.slots * kRows * 4);
+  p.bytes = p.o_off + (size_t)p.slots * kRows * kDL * 4;
+  return p;
+}
+
+// The persistent grid runs unfused bf16 calls whose tile sequence fits 32-bit indices.
+bool use_pp(const DecodeArgs& a, bool fused) {
+  if (fused || a.fp8) return false;
+  const int64_t items = (int64_t)a.B * a.shard_count * ((a.R + kRows - 1) / kRows);
+  const int64_t tiles_item = ((int64_t)a.max_pages * a.P + kTileTok - 1) / kTileTok;
+  return items <= (1 << 24) && items * tiles_item <= INT32_MAX;
+}
+
 TcPlan plan_tc(const DecodeArgs& a, int sm_count, bool fused) {
   TcPlan p{};
   p.row_tiles = (a.R + kRows - 1) / kRows;
@@ -1412,9 +2140,68 @@ bool tc_supported(const DecodeArgs& a) {
   return true;
 }
 
-size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
-  return plan_tc(a, sm_count, fused).bytes;
+namespace {
+// Tensor maps shared by both bf16 launch paths.
+int encode_bf16_maps(TcParams& p, const DecodeArgs& a) {
+  int rc = DCPMLA_OK;
+  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
+    const void* pool = a.kv.pool[a.shard_begin + i];
+    rc = encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+    if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_rope[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+  }
+  p.use3d = p.box_rows == kTileTok;
+  for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
+    if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
+      p.use3d = 0;   // fall back to one 2-D box per chunk
+  return rc;
 }
+
+int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
+  const PpPlan plan = plan_pp(a, sm_count);
+  if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
+  TcParams* tp = new (std::nothrow) TcParams();
+  if (!tp) return DCPMLA_ERR_CAPACITY;
+  TcParams& p = *tp;
+  p.a = a;
+  p.box_rows = std::min(a.P, kTileTok);
+  p.num_splits = 1;
+  p.chunk = 0;
+  p.row_tiles = plan.row_tiles;
+  p.fused = 0;
+  p.clusters = plan.clusters;
+  p.items = plan.items;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
+  p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
+  p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
+  p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
+  int rc = encode_bf16_maps(p, a);
+  if (rc == DCPMLA_OK) {
+    tc_prefix_kernel<<<1, 1024, 0, st>>>(a, plan.row_tiles, plan.items, p.ws_pre);
+    rc = launch_status();
+  }
+  if (rc == DCPMLA_OK &&
+      cudaFuncSetAttribute(decode_tc_bf16_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)b16::kSmemBytes) != cudaSuccess)
+    rc = DCPMLA_ERR_CUDA;
+  if (rc == DCPMLA_OK) {
+    decode_tc_bf16_persist_kernel<<<2 * plan.clusters, b16::kThreads, b16::kSmemBytes, st>>>(p);
+    rc = launch_status();
+  }
+  if (rc == DCPMLA_OK) {
+    tc_unit_combine_kernel<<<dim3((unsigned)plan.items, kRows / pp::kCombineRows), 256, 0, st>>>(p);
+    rc = launch_status();
+  }
+  delete tp;
+  return rc;
+}
+}  // namespace
+
+size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
+  return use_pp(a, fused) ? plan_pp(a, sm_count).bytes : plan_tc(a, sm_count, fused).bytes;
+}
+
+int tc_kernel_launches(const DecodeArgs& a, bool fused) { return use_pp(a, fused) ? 3 : 1; }
 
 template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
@@ -1431,6 +2218,7 @@ int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
 
 int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
                      bool fused) {
+  if (use_pp(a, fused)) return launch_decode_tc_pp(a, ws, ws_bytes, sm_count, st);
   const TcPlan plan = plan_tc(a, sm_count, fused);
   if (ws_bytes < plan.bytes || (plan.bytes && !ws)) return DCPMLA_ERR_CAPACITY;
   TcParams* tp = new (std::nothrow) TcParams();
