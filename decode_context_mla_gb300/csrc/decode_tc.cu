@@ -76,6 +76,10 @@ struct TcParams {
   int32_t* ws_pre;
   int32_t* ws_bad;
   int32_t clusters, items;
+  CUtensorMap tm_q;                   // q as [B R, 576], box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_qr;                  // q as [B R, 576], box {32, 128}, 64-byte swizzle
+  CUtensorMap tm_o;                   // o_part as {512, R, shards x B} fp32, box {32, 32, 1}, 128-byte swizzle
+  CUtensorMap tm_ws;                  // workspace partials as {512, 128, slots} fp32, the same box
 };
 
 template <bool kCluster>
@@ -90,6 +94,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
   }
 }
+
+// Tiled store of a shared-memory box to global memory; completion by bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                             int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Waits until every committed bulk store of this thread has read its shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// Waits until at most the newest committed bulk store of this thread may still be reading.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half)
@@ -741,15 +759,19 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
 
 // ------------------------------------------------------------ bf16 KV, persistent grid
 // The same tile pipeline as decode_tc_bf16_body, run by a persistent grid: the 64-token
-// tiles of all items (item = request, shard, 128-row tile) form one sequence of T tiles
-// and cluster k takes the contiguous share [T k / G, T (k + 1) / G).  The stage ring, the
-// S/P slots and the score exchange run on across item boundaries; at a boundary the
-// softmax warpgroups write the finished unit's O (after its last PV) and load the next
-// unit's Q, and the next unit's first PV waits until O has been read.  A unit that covers
-// its whole item writes o_part and lse_part; an item cut by share boundaries leaves one
-// partial per unit in workspace slot item + k (unique: a later cluster starts at the same
-// or a later item), merged by tc_unit_combine_kernel, which also writes the empty output
-// of items with no tiles.  The tile prefix sums come from tc_prefix_kernel.
+// tiles of all items (item = request, 128-row tile, shard; shards innermost) form one
+// sequence of T tiles and cluster k takes the contiguous share [T k / G, T (k + 1) / G).
+// The stage ring, the S/P slots and the score exchange run on across item boundaries.  At
+// a boundary the warpgroup that had no share in the unit's last tile readies the next
+// unit's Q once that tile's QK has completed (nothing to load when the next item is
+// another shard of the same request), so the next unit's QKs run while the finished
+// unit's O leaves: both warpgroups read O from TMEM (the next unit's first PV waits for
+// that), stage it in their exchange buffers and store it by TMA; the relay holds back the
+// buffers of the unit's last two tiles from the peer until then.  A unit that covers its
+// whole item writes o_part and lse_part; an item cut by share boundaries leaves one partial
+// per unit in workspace slot item + k (unique: a later cluster starts at the same or a
+// later item), merged by tc_unit_combine_kernel, which also writes the empty output of
+// items with no tiles.  The tile prefix sums come from tc_prefix_kernel.
 namespace pp {
 constexpr int kUnitFlags = 8;                       // ring of per-unit bad-page flags
 
@@ -766,6 +788,16 @@ __device__ __forceinline__ int cluster_of(int T, int t, int G) {
   return k;
 }
 
+// Item `it` is (request b, 128-row tile rt, shard sr), shards innermost: the items that
+// use the same query rows are adjacent.
+struct ItemIdx {
+  int b, rt, sr;
+};
+__host__ __device__ __forceinline__ ItemIdx item_idx(int it, int row_tiles, int shard_count) {
+  const int brt = it / shard_count;
+  return ItemIdx{brt / row_tiles, brt % row_tiles, it % shard_count};
+}
+
 struct Unit {
   int it, b, sr, r, rt, L, j0, j1, ntiles, slot;
   bool whole;                                       // the unit covers its whole item
@@ -777,11 +809,11 @@ __device__ __forceinline__ bool unit_of(const TcParams& p, int it, int t_lo, int
   const int s = max(s0, t_lo), e = min(s1, t_hi);
   if (e <= s) return false;
   const DecodeArgs& a = p.a;
-  const int bz = it / p.row_tiles;
+  const ItemIdx x = item_idx(it, p.row_tiles, a.shard_count);
   u.it = it;
-  u.rt = it % p.row_tiles;
-  u.b = bz / a.shard_count;
-  u.sr = bz % a.shard_count;
+  u.rt = x.rt;
+  u.b = x.b;
+  u.sr = x.sr;
   u.r = a.shard_begin + u.sr;
   u.L = __ldg(a.seq_lens + u.b);
   const int n = shard_len(u.L, u.r, a.c, a.I);
@@ -817,10 +849,11 @@ __global__ void __launch_bounds__(1024) tc_prefix_kernel(const DecodeArgs a, int
     const int it = base + t;
     int v = 0;
     if (it < items) {
-      const int bz = it / row_tiles, b = bz / a.shard_count, r = a.shard_begin + bz % a.shard_count;
+      const pp::ItemIdx x = pp::item_idx(it, row_tiles, a.shard_count);
+      const int b = x.b, r = a.shard_begin + x.sr;
       const int L = a.seq_lens[b];
       if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) {
-        if (bz % a.shard_count == 0 && it % row_tiles == 0) set_err(a.err, DCPMLA_DERR_LENGTH);
+        if (x.sr == 0 && x.rt == 0) set_err(a.err, DCPMLA_DERR_LENGTH);
       } else {
         v = (shard_len(L, r, a.c, a.I) + kTileTok - 1) / kTileTok;
       }
@@ -864,8 +897,8 @@ constexpr int kCombineRows = 16;
 __global__ void __launch_bounds__(256) tc_unit_combine_kernel(const TcParams p) {
   const DecodeArgs& a = p.a;
   const int item = blockIdx.x, r0 = blockIdx.y * pp::kCombineRows, t = threadIdx.x;
-  const int bz = item / p.row_tiles, rt = item % p.row_tiles;
-  const int b = bz / a.shard_count, sr = bz % a.shard_count;
+  const pp::ItemIdx x = pp::item_idx(item, p.row_tiles, a.shard_count);
+  const int b = x.b, rt = x.rt, sr = x.sr;
   const int64_t R = a.R;
   const int G = p.clusters;
   __shared__ int k0_s, k1_s, bad_s;
@@ -941,7 +974,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
   uint8_t* sX = sKV + kStages * kStage;                  // the peer's partial scores, per warpgroup
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full[kStages], bar_p_full[kStages];
   __shared__ uint64_t bar_o_par[2], bar_mref[2], bar_x_full[2], bar_x_empty[2], bar_x_read[2];
-  __shared__ uint64_t bar_q_full, bar_o_full, bar_o_free, bar_drain_qk, bar_drain_pv, bar_l;
+  __shared__ uint64_t bar_q_full, bar_o_full, bar_o_free, bar_drain_qk, bar_drain_pv, bar_l, bar_stg;
   __shared__ float mref_s[2][kRows];                     // a warpgroup's reference max after its tile
   __shared__ float l_s[2][kRows], m_s[2][kRows];
   __shared__ int unit_bad_s[pp::kUnitFlags];             // unit u met a bad page: entry u % 8
@@ -968,12 +1001,13 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       mbar_init(smem_u32(&bar_x_empty[s]), 1);                 // the peer's relay thread
       mbar_init(smem_u32(&bar_x_read[s]), kWgThreads);
     }
-    mbar_init(smem_u32(&bar_q_full), kSoftmaxThreads);         // once per unit
+    mbar_init(smem_u32(&bar_q_full), kWgThreads + 1);          // once per unit: TMEM part + TMA
     mbar_init(smem_u32(&bar_o_full), 1);                        // once per unit
     mbar_init(smem_u32(&bar_o_free), kSoftmaxThreads);         // once per unit
     mbar_init(smem_u32(&bar_drain_qk), 1);
     mbar_init(smem_u32(&bar_drain_pv), 1);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);              // once per unit
+    mbar_init(smem_u32(&bar_stg), kSoftmaxThreads);            // once per unit: O has left sX
     abort_s = 0;
     fence_barrier_init();
   }
@@ -1180,24 +1214,87 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     }
   } else if (warp == 11) {
     // ---------------------------------------------------------------- relay
+    // Tells the peer that an exchange buffer was read.  A unit's O leaves through the
+    // exchange buffers, so the peer must write no later tile into them until it has: the
+    // buffers of the unit's last two tiles are released once the unit's O is out (and the
+    // last tile of a unit followed by a one-tile unit waits for that unit's O too).
     if (lane == 0) {
-      for (int gi = 0; gi < t_hi - t_lo; ++gi) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read[gi & 1]), (gi >> 1) & 1, abort_flag)) break;
-        mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[gi & 1]), peer));
+      int gi = 0, ui = 0;
+      bool okr = true;
+      // the buffers start empty: virtual tiles -2 and -1 are released first; tile -1's
+      // release (the peer may send tile 1) waits for unit 0's O when unit 0 has one tile
+      mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[0]), peer));
+      if (it0 < p.items && min(__ldg(p.ws_pre + it0 + 1), t_hi) - t_lo == 1)
+        okr = wait_bar<false>(smem_u32(&bar_stg), 0, abort_flag);
+      if (okr) mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[1]), peer));
+      for (int it = it0; okr && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
+        pp::Unit u;
+        if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
+        int itn = it + 1;                                  // the next item with tiles
+        while (itn < p.items && __ldg(p.ws_pre + itn) < t_hi && __ldg(p.ws_pre + itn + 1) == __ldg(p.ws_pre + itn))
+          ++itn;
+        const int nnext = itn < p.items ? max(0, min(__ldg(p.ws_pre + itn + 1), t_hi) - __ldg(p.ws_pre + itn)) : 0;
+        for (int i = 0; i < u.ntiles; ++i, ++gi) {
+          if (!wait_bar<false>(smem_u32(&bar_x_read[gi & 1]), (gi >> 1) & 1, abort_flag)) {
+            okr = false;
+            break;
+          }
+          const int wait_unit = (i == u.ntiles - 1 && nnext == 1) ? ui + 1 : (i >= u.ntiles - 2 ? ui : -1);
+          if (wait_unit >= 0 && !wait_bar<false>(smem_u32(&bar_stg), wait_unit & 1, abort_flag)) {
+            okr = false;
+            break;
+          }
+          mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[gi & 1]), peer));
+        }
+        ++ui;
       }
     }
   } else {
     // -------------------------------------------------------------- softmax
-    // Per unit: load the unit's Q, take the unit's tiles with gi % 2 == g (each thread one
-    // query row over a tile's 64 columns), then write the unit's O and LSE.
+    // Per unit: take the unit's tiles with gi % 2 == g (each thread one query row over a
+    // tile's 64 columns), ready the next unit's Q if this warpgroup had no share in the last
+    // tile, then write the unit's O and LSE.
     const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
     const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
-    int gi = 0, ui = 0;
+    int gi = 0, ui = 0, q_last = -1;
     bool ok = true;
+    // the query dims a CTA keeps in TMEM, one row per thread (zero past R)
+    auto load_q_tmem = [&](const pp::Unit& un) {
+      const int64_t gr = (int64_t)un.rt * kRows + row;
+      const bool rl = gr < R;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + ((int64_t)un.b * R + gr) * kDK + h * 256);
+      uint4 v[16];
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) v[kk] = rl ? __ldg(qsrc + kk) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c16 = 0; c16 < 4; ++c16) {
+        uint32_t rr[16];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 w4 = v[c16 * 4 + kk];
+          rr[kk * 4 + 0] = w4.x; rr[kk * 4 + 1] = w4.y; rr[kk * 4 + 2] = w4.z; rr[kk * 4 + 3] = w4.w;
+        }
+        tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_q_full));
+    };
+    // the query dims a CTA keeps in shared memory, by TMA (one thread); rows past R take
+    // the next request's rows (or the zero fill past the tensor's end): their scores stay
+    // finite and only their own rows, which are not written
+    auto issue_q_tma = [&](const pp::Unit& un) {
+      const uint32_t qf = smem_u32(&bar_q_full);
+      const int y = (int)((int64_t)un.b * R + (int64_t)un.rt * kRows);
+      mbar_arrive_expect_tx(qf, (uint32_t)kQBytes);
+      tma_load_2d(smem_u32(sQ), &p.tm_q, (int)(256 * h + 128), y, qf);
+      tma_load_2d(smem_u32(sQ + kQChunk), &p.tm_q, (int)(256 * h + 192), y, qf);
+      tma_load_2d(smem_u32(sQ + kQRopeOff), &p.tm_qr, (int)(512 + 32 * h), y, qf);
+    };
     for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
       pp::Unit u;
       if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
@@ -1206,45 +1303,15 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       // the keys a query sees form a prefix of the shard's tokens (positions <= qpos)
       const int jvis = min(u.j1, shard_len(u.L - a.Tq + (int)(grow / a.H) + 1, u.r, a.c, a.I));
       const int jvis_min = min(u.j1, shard_len(u.L - a.Tq + 1, u.r, a.c, a.I));
-      {
-        // the unit's Q (every QK of the previous unit has completed: its O was read)
-        const __nv_bfloat16* qrow = a.q + ((int64_t)u.b * R + grow) * kDK;
-        if (g == 0) {
-          const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256);
-          uint4 v[16];
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) v[kk] = real ? __ldg(qsrc + kk) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int c16 = 0; c16 < 4; ++c16) {
-            uint32_t rr[16];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint4 w4 = v[c16 * 4 + kk];
-              rr[kk * 4 + 0] = w4.x; rr[kk * 4 + 1] = w4.y; rr[kk * 4 + 2] = w4.z; rr[kk * 4 + 3] = w4.w;
-            }
-            tmem_st16(tmem + lane_off + kColQ + c16 * 16, rr);
-          }
-          tmem_st_wait();
-        } else {
-          const uint4* qsrc = reinterpret_cast<const uint4*>(qrow + h * 256 + 128);
-          const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + 512 + 32 * h);
-          uint4 v[20];
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) v[kk] = real ? __ldg(qsrc + kk) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) v[16 + kk] = real ? __ldg(rsrc + kk) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int cl = 0; cl < 2; ++cl)
-#pragma unroll
-            for (int uu = 0; uu < 8; ++uu)
-              *reinterpret_cast<uint4*>(sQ + cl * kQChunk + row * 128 + ((uu ^ (row & 7)) << 4)) = v[cl * 8 + uu];
-#pragma unroll
-          for (int uu = 0; uu < 4; ++uu)
-            *reinterpret_cast<uint4*>(sQ + kQRopeOff + row * 64 + ((uu ^ ((row >> 1) & 3)) << 4)) = v[16 + uu];
-          fence_proxy_async();
+      if (ui == 0 && g == 0) {
+        // the first unit's Q (later units': the warpgroup idle during the previous unit's
+        // last tile, below)
+        if (warp == 2 && lane == 0) {
+          issue_q_tma(u);
+          q_last = 0;
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_q_full));
+        __syncwarp();
+        load_q_tmem(u);
       }
       float m_own = -INFINITY, l = 0.f;
       const int gs = gi;                                     // the unit's first tile
@@ -1257,12 +1324,10 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (gt / kStages) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        // send this CTA's partial into the peer's buffer g, once the peer has read what
-        // this warpgroup sent two tiles ago
-        if (gt >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((gt >> 1) - 1) & 1, abort_flag));
-          if (!ok) break;
-        }
+        // send this CTA's partial into the peer's buffer g, once the peer has released it
+        // (read what this warpgroup sent two tiles ago, and let a unit's O out through it)
+        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), (gt >> 1) & 1, abort_flag));
+        if (!ok) break;
         const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
         float x[64];
         uint32_t* xb = reinterpret_cast<uint32_t*>(x);
@@ -1368,6 +1433,37 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         mbar_arrive(smem_u32(&bar_p_full[st]));
       }
       gi = gs + u.ntiles;
+      // the warpgroup without the unit's last tile readies the next unit's Q: nothing to
+      // load for the same query rows; else, once the unit's last QK has completed (it read
+      // Q), one thread loads the shared-memory part and the warpgroup writes the TMEM part
+      if (ok && ((gi - 1) & 1) != g) {
+        int itn = it + 1;
+        while (itn < p.items && __ldg(p.ws_pre + itn) < t_hi && __ldg(p.ws_pre + itn + 1) == __ldg(p.ws_pre + itn))
+          ++itn;                                             // items without tiles
+        pp::Unit un;
+        if (itn < p.items && pp::unit_of(p, itn, t_lo, t_hi, k, un)) {
+          // the arrivals for the next unit follow the unit's last QK, which followed the
+          // completion of this unit's q_full phase: no arrival can reach that phase, and the
+          // QK issuer has seen it before the next one can complete
+          const int gl = gi - 1;
+          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[gl % kStages]), (gl / kStages) & 1, abort_flag));
+          if (ok) {
+            tc_fence_after();
+            const bool tma_thread = warp == 2 + 4 * g && lane == 0;
+            if (un.b == u.b && un.rt == u.rt) {
+              mbar_arrive(smem_u32(&bar_q_full));
+              if (tma_thread) mbar_arrive(smem_u32(&bar_q_full));
+            } else {
+              if (tma_thread) {
+                issue_q_tma(un);
+                q_last = ui + 1;
+              }
+              __syncwarp();
+              load_q_tmem(un);
+            }
+          }
+        }
+      }
       // ---- the unit's epilogue ----
       if (ok) ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), ui & 1, abort_flag));
       l_s[g][row] = l;
@@ -1384,20 +1480,49 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       const float inv = live ? 1.f / l_tot : 0.f;
       const int64_t orow = ((int64_t)u.sr * a.B + u.b) * R + grow;
       const int64_t wrow = (int64_t)u.slot * kRows + row;
-      float* dst = (u.whole ? a.o_part + orow * kDL : p.ws_o + wrow * kDL) + h * 256 + g * 128;
-      for (int q = 0; q < 8; ++q) {
-        uint32_t w16[16];
-        if (ok) {
-          tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 16, w16);
-          tmem_ld_wait();
+      // O leaves through this warp's 8 KB of its warpgroup's exchange buffer (every tile's
+      // scores in it were read, and the relay lets the peer write the next tiles' only
+      // after this) in 32-column rounds, two 4 KB boxes alternating: each thread writes its
+      // row's 32 normalised values as 16-byte units, unit v at v ^ (row % 8) (the 128-byte
+      // swizzle), and one lane stores the warp's 32 x 32 box by TMA (rows past R fall
+      // outside the tensor).  Once the last round has read TMEM the next unit's PV may start.
+      uint8_t* stg = sX + (warp - 2) * 8192;
+      const CUtensorMap* omap = u.whole ? &p.tm_o : &p.tm_ws;
+      const int oy = (u.whole ? u.rt * kRows : 0) + quarter * 32;
+      const int oz = u.whole ? u.sr * a.B + u.b : u.slot;
+      const bool store = !u.whole || (int64_t)u.rt * kRows + quarter * 32 < R;   // a row below R
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint8_t* buf = stg + (q & 1) * 4096;
+        if (q >= 2) {
+          if (lane == 0) bulk_wait_read_1();                 // the box two rounds back is read out
+          __syncwarp();
         }
-        if (!real) continue;
-        float4* d4 = reinterpret_cast<float4*>(dst + q * 16);
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          d4[v] = live ? make_float4(__uint_as_float(w16[4 * v]) * inv, __uint_as_float(w16[4 * v + 1]) * inv,
-                                     __uint_as_float(w16[4 * v + 2]) * inv, __uint_as_float(w16[4 * v + 3]) * inv)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t w16[16];
+          if (ok) {
+            tmem_ld16(tmem + lane_off + kColO + g * 128 + q * 32 + hh * 16, w16);
+            tmem_ld_wait();
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float4 f = live ? make_float4(__uint_as_float(w16[4 * v]) * inv, __uint_as_float(w16[4 * v + 1]) * inv,
+                                                __uint_as_float(w16[4 * v + 2]) * inv, __uint_as_float(w16[4 * v + 3]) * inv)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(buf + lane * 128 + (((hh * 4 + v) ^ (lane & 7)) << 4)) = f;
+          }
+        }
+        if (q == 3) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_o_free));
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0 && store) {
+          tma_store_3d(omap, smem_u32(buf), (int)h * 256 + g * 128 + q * 32, oy, oz);
+          bulk_commit_group();
+        }
       }
       if (h == 0 && g == 0 && real) {
         const float lse2 = live ? m_tot + log2f(l_tot) : -INFINITY;
@@ -1407,9 +1532,16 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           p.ws_lse[wrow] = lse2;
       }
       if (!u.whole && h == 0 && g == 0 && row == 0) p.ws_bad[u.slot] = bad ? 1 : 0;
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_o_free));
+      if (lane == 0) bulk_wait_read_all();                   // every box is read out
+      __syncwarp();
+      mbar_arrive(smem_u32(&bar_stg));
       ++ui;
+    }
+    if (q_last >= 0 && *abort_flag) {
+      // let the last Q copy land before the CTA's shared memory goes away
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_q_full), q_last & 1) && clock64() - t0 < kWaitCycles / 8) {
+      }
     }
   }
 
@@ -2023,6 +2155,21 @@ int encode_rows_576(CUtensorMap* m, const void* base, uint64_t rows, uint32_t bo
   return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
 }
 
+// fp32 output rows as {512, rows, blocks}: one box {32 columns, 32 rows, 1} with the
+// 128-byte swizzle; rows past `rows` of a block are outside the tensor.
+int encode_out_f32(CUtensorMap* m, void* base, uint64_t rows, uint64_t blocks) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return DCPMLA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)kDL, (cuuint64_t)rows, (cuuint64_t)blocks};
+  cuuint64_t strides[2] = {(cuuint64_t)kDL * 4, (cuuint64_t)rows * kDL * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
 struct TcPlan {
   int32_t splits, chunk, row_tiles;
   size_t cnt_off, lse_off, o_off, bytes;
@@ -2176,6 +2323,10 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
   p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
   p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
   int rc = encode_bf16_maps(p, a);
+  if (rc == DCPMLA_OK) rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
+  if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_qr, a.q, (uint64_t)a.B * a.R, kRows);
+  if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_o, a.o_part, (uint64_t)a.R, (uint64_t)a.shard_count * a.B);
+  if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_ws, p.ws_o, kRows, (uint64_t)plan.slots);
   if (rc == DCPMLA_OK) {
     tc_prefix_kernel<<<1, 1024, 0, st>>>(a, plan.row_tiles, plan.items, p.ws_pre);
     rc = launch_status();
