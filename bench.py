@@ -6,11 +6,14 @@ merge.  Inputs are resident in HBM when the timed region starts; the KV cache
 of every workload except "tiny" is larger than L2, and for "tiny" L2 is
 flushed between timed steps.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config dsv3] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config bimodal] [--impl reference]
 
-Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
-independent replica on its own GPU: requests are independent and the path
-has no exchange step, so there is no collective on the data path.
+Prints one JSON line (rank 0).  The headline is the bimodal agentic batch, the
+workload with the most KV bytes per step; at N = 1 the other four workloads
+are timed after it the same way and reported under "per_workload".  With
+N > 1 (torchrun) every rank runs an independent replica on its own GPU:
+requests are independent and the path has no exchange step, so there is no
+collective on the data path.
 """
 from __future__ import annotations
 
@@ -303,15 +306,14 @@ def config_obj(w: W.Workload) -> dict:
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, w: W.Workload):
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    from __graft_entry__ import build
-    build()
+def measure_step(args, w: W.Workload, ws: int, local: int, with_e2e: bool) -> dict:
+    """Build the workload, capture its step as graphs and time `args.steps` replays.
+
+    Returns the step and decode-launch times (max over ranks for the step), the roofline
+    and tensor figures of the decode launch, the clocks seen during the timed region and,
+    when asked, the end-to-end figure from pinned host buffers."""
     import dcp_harness as Hn
+    from decode_context_mla_gb300 import binding as B
 
     dw = Hn.build(w, fused=args.fused)
     step = dw.step
@@ -335,7 +337,6 @@ def run_ours(args, w: W.Workload):
         graphs.append(g)
     g_pre, g_dec, g_post = graphs
     c = dw.cache
-    from decode_context_mla_gb300 import binding as B
     path, dec_launches = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, c.kv_dtype,
                                               step.page_table.shape[1])
     torch.cuda.synchronize()
@@ -395,10 +396,9 @@ def run_ours(args, w: W.Workload):
     clocks = sampler.summary(t_wall0, t_wall1)
     err = c.check_errors()
     if err:
-        raise RuntimeError(f"device error bits {err}")
+        raise RuntimeError(f"device error bits {err} ({w.name})")
 
     ms_step = max_over_ranks(ms_total / args.steps, ws)
-    value = whole_job_gbs(acc["kv_bytes"], ms_step, ws)
     peaks = measured_peaks()
     achieved = acc["decode_bytes"] / (ms_dec * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
@@ -410,10 +410,41 @@ def run_ours(args, w: W.Workload):
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"}
     tflops = acc["flops"] / (ms_dec * 1e-3) / 1e12
     tensor_info = {"achieved_tflops": round(tflops, 2), "peak_tflops": peaks["bf16_tflops"],
-                   "frac": round(tflops / peaks["bf16_tflops"], 4)}
+                   "frac": round(tflops / peaks["bf16_tflops"], 4),
+                   "algorithmic_flops": acc["flops"]}
+    e2e = run_e2e(args, w, dw, stream, acc, ws) if with_e2e else None
 
-    # end to end through the public API from pinned host buffers
-    e2e = run_e2e(args, w, dw, stream, acc, ws)
+    # slot map + append (when the step appends), the decode's kernels, the merge
+    # (fused: the decode's own merge kernel replaces the split merge and the LSE merge)
+    launches_per_step = (2 if step.do_append else 0) + (dec_launches if not args.fused else
+                                                         (2 if path == 1 else 1 if path == 2 else 2))
+    if not args.fused:
+        launches_per_step += 1
+    res = dict(acc=acc, lens=lens, ms_step=ms_step, ms_dec=ms_dec, roofline=roofline,
+               tensor=tensor_info, clocks=clocks, e2e=e2e, launches_per_step=launches_per_step,
+               value=whole_job_gbs(acc["kv_bytes"], ms_step, ws))
+    del graphs, g_pre, g_dec, g_post, dw, step, c, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+# The benchmark's headline workload: the one with the most KV bytes per step, on which the
+# KV-GB/s metric is largest (the bimodal agentic mix); the others are reported beside it.
+HEADLINE = "bimodal"
+
+
+def run_ours(args, w: W.Workload):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from __graft_entry__ import build
+    build()
+
+    head = measure_step(args, w, ws, local, with_e2e=True)
+    lens, acc, ms_step = head["lens"], head["acc"], head["ms_step"]
 
     # CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -424,15 +455,31 @@ def run_ours(args, w: W.Workload):
                "sample": f"fp64 oracle (striped decode + merge) on {n} whole request(s) of the "
                          f"{w.name} workload, {t:.1f} s of CPU work"}
 
-    # slot map + append (when the step appends), the decode's kernels, the merge
-    # (fused: the decode's own merge kernel replaces the split merge and the LSE merge)
-    launches_per_step = (2 if step.do_append else 0) + (dec_launches if not args.fused else
-                                                         (2 if path == 1 else 1 if path == 2 else 2))
-    if not args.fused:
-        launches_per_step += 1
+    # the other workloads of the benchmark, each timed the same way (N = 1 only: with more
+    # GPUs the run times the headline replicas alone)
+    per_workload = None
+    if ws == 1 and not args.no_per_workload and not args.batch and not args.interleave:
+        per_workload = {}
+        for name in W.WORKLOADS:
+            if name == w.name:
+                continue
+            r = measure_step(args, W.WORKLOADS[name], ws, local, with_e2e=False)
+            per_workload[name] = {
+                "value": round(r["value"], 2), "unit": "GB/s", "ms_per_step": round(r["ms_step"], 4),
+                "kernel_ms": r["roofline"]["kernel_ms"],
+                "hbm_frac": r["roofline"]["frac"], "tensor_frac": r["tensor"]["frac"],
+                "achieved_gbs": r["roofline"]["achieved"],
+                "achieved_tflops": r["tensor"]["achieved_tflops"],
+                "kernel": r["roofline"]["kernel"], "traffic": r["roofline"]["traffic"],
+                "attended_tokens_per_s": round(sum(r["lens"]) * W.WORKLOADS[name].Tq
+                                               / (r["ms_step"] * 1e-3), 1),
+                "clocks": r["clocks"], "gpu_launches": r["launches_per_step"] * args.steps,
+            }
+
     if rank == 0:
+        peaks = measured_peaks()
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "metric": METRIC, "value": round(head["value"], 2), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3", "data": "synthetic",
@@ -440,9 +487,12 @@ def run_ours(args, w: W.Workload):
             "attended_tokens_per_s": round(sum(lens) * w.Tq * ws / (ms_step * 1e-3), 1),
             "decode_tokens_per_s": round(w.B * w.Tq * ws / (ms_step * 1e-3), 1),
             "step_hbm_frac": round(acc["step_bytes"] / (ms_step * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "roofline": roofline, "tensor": tensor_info, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            "roofline": head["roofline"], "tensor": head["tensor"], "cpu_baseline": cpu,
+            "e2e": head["e2e"], "gpu_launches": head["launches_per_step"] * args.steps,
+            "clocks": head["clocks"],
         }
+        if per_workload is not None:
+            line["per_workload"] = per_workload
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -621,9 +671,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="dsv3", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--config", default=HEADLINE, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --config (by default the other workloads are timed after it "
+                         "and reported under per_workload)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--op", default="step", choices=["step", "relayout", "gather", "append_e4m3", "hicache"],
                     help="what to time: the decode step (default) or one of the layout calls")

@@ -341,6 +341,13 @@ size_t fma_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_fma(
 int launch_decode_fma(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
   const FmaPlan plan = plan_fma(a, sm_count);
   if (ws_bytes < plan.bytes || (plan.bytes && !ws)) return DCPMLA_ERR_CAPACITY;
+  // every refusal comes before the first enqueue: a refused call leaves the workspace alone
+  const int64_t z = (int64_t)a.B * a.shard_count;
+  if (z > 65535 || plan.row_groups > 65535) return DCPMLA_ERR_UNSUPPORTED;
+  const size_t smem = smem_bytes(a.fp8);
+  const auto kern = a.fp8 ? decode_fma_kernel<true> : decode_fma_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return DCPMLA_ERR_CUDA;
   FmaParams fp{};
   fp.a = a;
   fp.num_splits = plan.splits;
@@ -354,21 +361,8 @@ int launch_decode_fma(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_cou
     const size_t cnt_bytes = (size_t)a.B * a.shard_count * plan.row_groups * 4;
     if (cudaMemsetAsync(fp.ws_cnt, 0, cnt_bytes, st) != cudaSuccess) return DCPMLA_ERR_CUDA;
   }
-  const int64_t z = (int64_t)a.B * a.shard_count;
-  if (z > 65535 || plan.row_groups > 65535) return DCPMLA_ERR_UNSUPPORTED;
   const dim3 grid((unsigned)plan.splits, (unsigned)plan.row_groups, (unsigned)z);
-  const size_t smem = smem_bytes(a.fp8);
-  if (a.fp8) {
-    if (cudaFuncSetAttribute(decode_fma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return DCPMLA_ERR_CUDA;
-    decode_fma_kernel<true><<<grid, kThreads, smem, st>>>(fp);
-  } else {
-    if (cudaFuncSetAttribute(decode_fma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return DCPMLA_ERR_CUDA;
-    decode_fma_kernel<false><<<grid, kThreads, smem, st>>>(fp);
-  }
+  kern<<<grid, kThreads, smem, st>>>(fp);
   return launch_status();
 }
 

@@ -2355,12 +2355,18 @@ size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
 int tc_kernel_launches(const DecodeArgs& a, bool fused) { return use_pp(a, fused) ? 3 : 1; }
 
 template <bool kFp8>
+int set_tc_smem() {
+  auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
+  const size_t smem = kFp8 ? e4::kSmemBytes : b16::kSmemBytes;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess
+             ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+}
+
+template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
   auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
   const int threads = kFp8 ? e4::kThreads : b16::kThreads;
   const size_t smem = kFp8 ? e4::kSmemBytes : b16::kSmemBytes;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return DCPMLA_ERR_CUDA;
   const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
                   (unsigned)(p.a.B * p.a.shard_count));
   kern<<<grid, threads, smem, st>>>(p);
@@ -2372,6 +2378,9 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   if (use_pp(a, fused)) return launch_decode_tc_pp(a, ws, ws_bytes, sm_count, st);
   const TcPlan plan = plan_tc(a, sm_count, fused);
   if (ws_bytes < plan.bytes || (plan.bytes && !ws)) return DCPMLA_ERR_CAPACITY;
+  // every refusal comes before the first enqueue: a refused call leaves the workspace alone
+  if ((int64_t)a.B * a.shard_count > 65535 || plan.row_tiles > 65535 || 2LL * plan.splits > INT32_MAX)
+    return DCPMLA_ERR_UNSUPPORTED;
   TcParams* tp = new (std::nothrow) TcParams();
   if (!tp) return DCPMLA_ERR_CAPACITY;
   TcParams& p = *tp;
@@ -2394,6 +2403,7 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
     if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
       p.use3d = 0;   // fall back to one 2-D box per chunk
+  if (rc == DCPMLA_OK) rc = a.fp8 ? set_tc_smem<true>() : set_tc_smem<false>();
   if (rc == DCPMLA_OK && (plan.splits > 1 || fused)) {
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
@@ -2401,10 +2411,6 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
     if (cudaMemsetAsync(p.ws_cnt, 0, (size_t)a.B * a.shard_count * plan.row_tiles * 4, st) != cudaSuccess)
       rc = DCPMLA_ERR_CUDA;
-  }
-  if (rc == DCPMLA_OK) {
-    const int64_t z = (int64_t)a.B * a.shard_count;
-    if (z > 65535 || plan.row_tiles > 65535 || 2LL * plan.splits > INT32_MAX) rc = DCPMLA_ERR_UNSUPPORTED;
   }
   if (rc == DCPMLA_OK) rc = a.fp8 ? launch_tc<true>(p, plan, st) : launch_tc<false>(p, plan, st);
   delete tp;

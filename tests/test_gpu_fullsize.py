@@ -2,8 +2,8 @@
 
 The whole step (slot map, append, decode over all c shards, merge) runs at
 full size; the oracle then recomputes sampled requests one by one from the
-same seeded generator (every shard's partial and the merged result), and
-the sampled requests' rows in the shard pools are compared bit for bit.
+same seeded generator (every shard's partial and the merged result; every
+request of dsv3), and the sampled requests' rows in the shard pools are compared bit for bit.
 """
 import numpy as np
 import pytest
@@ -23,9 +23,20 @@ def built_library():
 
 
 def _samples(w, lens):
+    """Requests the oracle recomputes at full size.
+
+    dsv3: all 32 (the persistent 128-row grid cuts items at its clusters' share
+    boundaries, which fall inside different requests' shards).  fp8: eight requests
+    spread over the batch, each covering all four 128-row tiles and the split merge of
+    every shard (the oracle takes a few seconds per request there).  bimodal: the
+    shortest, the median and the longest context.  Otherwise the first and last."""
     order = sorted(range(w.B), key=lambda b: lens[b])
+    if w.name == "dsv3":
+        return list(range(w.B))
+    if w.name == "fp8":
+        return sorted({round(i * (w.B - 1) / 7) for i in range(8)})
     if w.name == "bimodal":
-        return [order[0], order[-1]]
+        return [order[0], order[len(order) // 2], order[-1]]
     if w.B > 1:
         return [0, w.B - 1]
     return [0]

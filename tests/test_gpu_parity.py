@@ -86,7 +86,22 @@ SMALL = {
                               lse_base="2", seed=27, L=3001),
     "tc_e4m3_p8": W.Workload("tce8", B=2, H=128, Tq=1, c=2, P=8, kv_dtype="e4m3", lse_base="e",
                              seed=28, L=999),
+    # E4M3 on the CUDA cores: more shards than the tensor-core kernels take in one launch
+    # (causal four-token verify, split-KV with last-arriver merge, contexts shorter than c),
+    # and page sizes the TMA kernels reject (P = 5, P = 12)
+    "fma_e4m3_c16_tq4": W.Workload("fe16", B=3, H=16, Tq=4, c=16, P=4, kv_dtype="e4m3",
+                                   lse_base="2", seed=29, lengths_mix=(1, 2000, 3000, 4, 15)),
+    "fma_e4m3_c3_p5": W.Workload("fe3", B=4, H=8, Tq=1, c=3, P=5, kv_dtype="e4m3", lse_base="e",
+                                 seed=30, lengths_mix=(2, 700, 1500, 1, 2)),
+    "fma_e4m3_h128_c12": W.Workload("fe12", B=2, H=128, Tq=2, c=12, P=16, kv_dtype="e4m3",
+                                    lse_base="2", seed=31, L=2500),
+    "fma_e4m3_p12_tq3": W.Workload("fe12p", B=2, H=32, Tq=3, c=2, P=12, kv_dtype="e4m3",
+                                   lse_base="e", seed=32, L=4100),
 }
+
+# cases that must run on the CUDA-core decode (asserted by test_decode_path_per_workload)
+FMA_CASES = ["c16_short", "c3_p5_tq2", "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5", "fma_e4m3_h128_c12",
+             "fma_e4m3_p12_tq3"]
 
 SENTINEL = 0xA5
 
@@ -278,13 +293,16 @@ def test_decode_path_per_workload():
         # merge; 128-row E4M3: one launch
         launches = {B.PATH_TC_FEWHEAD: 2, B.PATH_TC_ROWS: 3 if kv == B.KV_BF16 else 1}[path]
         assert got == (path, launches), name
-    w = SMALL["c16_short"]
-    got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
-    assert got == (B.PATH_CUDA_CORE, 1)
+    for name in FMA_CASES:
+        w = SMALL[name]
+        kv = B.KV_BF16 if w.kv_dtype == "bf16" else B.KV_E4M3
+        got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, kv, max(w.pages_per_request()))
+        assert got == (B.PATH_CUDA_CORE, 1), name
 
 
 
 FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
+               "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5",
                "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
                "ilv2_c16", "tc_p8_c3", "tc_p256_tq4"]
 

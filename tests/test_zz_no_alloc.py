@@ -4,9 +4,11 @@ dcpmla_decode_noalloc serves callers that cannot give the decode a device
 workspace (a plugin whose host framework owns all device memory, a process
 whose memory is fully reserved by a caching allocator, a latency-critical
 loop where cudaMalloc would synchronise the device).  Its scratch is a static
-device array inside the library.  These checks compare it with the regular
-dcpmla_decode on the same inputs, two calls in a row, within the parity
-tolerance, and check that oversized shapes are refused before any launch.
+device array inside the library.  These checks compare it, two calls in a row,
+with the fp64 oracle on the same seeded inputs (every shard's partial output and
+LSE, within the parity tolerance: 2e-3 for bf16 KV, 1e-2 for E4M3 KV against the
+dequantised oracle) and with the regular dcpmla_decode, and check that oversized
+shapes are refused before any launch.
 
 This file is collected last on purpose; it also passes when run alone.
 """
@@ -16,7 +18,7 @@ import torch
 import dcp_harness as Hn
 import dcp_workloads as W
 from decode_context_mla_gb300 import binding as B
-from oracle_ref import TOL, lse_err, row_rel_err
+from oracle_ref import TOL, OracleWorkload, lse_err, row_rel_err
 
 pytestmark = pytest.mark.gpu
 needs_cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
@@ -43,17 +45,21 @@ def _args(dw):
 
 @needs_cuda
 @pytest.mark.parametrize("name", list(CASES))
-def test_noalloc_matches_regular_decode_two_calls(name):
+def test_noalloc_matches_oracle_and_regular_decode_two_calls(name):
     w = CASES[name]
     dw = Hn.build(w)
     dw.step.run()                                   # append the step's new tokens
     torch.cuda.synchronize()
     st = dw.step
+    R = w.Tq * w.H
+    tol = TOL[w.kv_dtype]
+    ow = OracleWorkload(w)
+    want = {b: ow.decode(b)[:2] for b in range(w.B)}   # (o_parts (c,R,512), lse_parts (c,R))
     ref_o = torch.empty_like(st.o_part)
     ref_l = torch.empty_like(st.lse_part)
     B.dcpmla_decode(*_args(dw), ref_o, ref_l, st.workspace, dw.cache.err)
     torch.cuda.synchronize()
-    tol = TOL[w.kv_dtype]
+    ref_o, ref_l = ref_o.cpu().numpy(), ref_l.cpu().numpy()
     free_after_first = None
     o = torch.empty_like(st.o_part)
     lse = torch.empty_like(st.lse_part)
@@ -63,13 +69,21 @@ def test_noalloc_matches_regular_decode_two_calls(name):
         B.dcpmla_decode_noalloc(*_args(dw), o, lse, dw.cache.err)
         torch.cuda.synchronize()
         assert dw.cache.check_errors() == 0
-        assert row_rel_err(o.cpu().numpy(), ref_o.cpu().numpy()) < tol, (name, call)
-        assert lse_err(lse.cpu().numpy(), ref_l.cpu().numpy()) < tol, (name, call)
+        go, gl = o.cpu().numpy(), lse.cpu().numpy()
+        for b in range(w.B):
+            op, lp = want[b]
+            assert row_rel_err(go[:, b].reshape(w.c, R, 512), op) < tol, (name, call, b, "o")
+            assert lse_err(gl[:, b].reshape(w.c, R), lp) < tol, (name, call, b, "lse")
+        assert row_rel_err(go, ref_o) < tol, (name, call)
+        assert lse_err(gl, ref_l) < tol, (name, call)
+        # A weak check that the call allocates nothing: device-wide free memory must not
+        # drop by a cudaMalloc granule (2 MiB) between the first and the second call.  The
+        # first call may load the library's module, which maps the static scratch array.
         free_now = torch.cuda.mem_get_info()[0]
         if call == 0:
             free_after_first = free_now
         else:
-            assert free_now == free_after_first      # the second call took no device memory
+            assert free_after_first - free_now < (2 << 20)
 
 
 @needs_cuda
