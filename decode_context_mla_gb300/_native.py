@@ -47,6 +47,7 @@ SIGNATURES = {
     "dcpmla_decode_merged": (C.c_int, [vp, vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                        f32, i32, vp, vp, vp, sz, vp, vp]),
     "dcpmla_lse_merge": (C.c_int, [vp, vp, i32, i64, i32, vp, vp, vp, vp]),
+    "dcpmla_testing_set_wait_limit": (C.c_int, [i64]),
     "dcpmla_relayout_dense_to_striped": (C.c_int, [vp, vp, i64, vp, i32, vp, vp, i32, i64, vp, i32,
                                                    vp, i32, i32, i32, i32, vp, vp]),
     "dcpmla_gather_unstriped": (C.c_int, [vp, vp, i32, i64, vp, i32, vp, i32, i32, i32, i32, vp, vp,

@@ -273,6 +273,12 @@ def dcpmla_decode_noalloc(q: torch.Tensor, pools: Sequence[torch.Tensor],
         _stream(stream)), "dcpmla_decode_noalloc")
 
 
+def dcpmla_testing_set_wait_limit(cycles: int) -> None:
+    """Testing only: pipeline-wait limit (clock64 cycles) of later decode launches; <= 0 restores
+    the default of about one second."""
+    _check(lib().dcpmla_testing_set_wait_limit(int(cycles)), "dcpmla_testing_set_wait_limit")
+
+
 def dcpmla_lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, c: int, rows: int,
                      lse_base: int, o: torch.Tensor, lse: Optional[torch.Tensor],
                      err: Optional[torch.Tensor] = None, stream=None) -> None:

@@ -4,7 +4,12 @@
 // speculative decoding: each shard's kernel gets the rank-local page table,
 // cp_world (c), cp_rank (r) and the global KV length, and returns the
 // rank-local (output, LSE).
+#include <algorithm>
+#include <atomic>
+#include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "decode.cuh"
 
@@ -57,6 +62,68 @@ int fill_args(DecodeArgs& a, const void* d_q, void* const* pools, float* const* 
   return DCPMLA_OK;
 }
 
+}  // namespace
+
+namespace dcpmla {
+
+LaunchKey launch_key(const DecodeArgs& a, const void* ws, size_t ws_bytes, int tag) {
+  LaunchKey k;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  auto u = [](const void* ptr) { return (uint64_t)reinterpret_cast<uintptr_t>(ptr); };
+  k.add((uint64_t)(uint32_t)tag);
+  k.add((uint64_t)(uint32_t)dev);
+  k.add(u(ws));
+  k.add((uint64_t)ws_bytes);
+  k.add(u(a.q));
+  for (int r = a.shard_begin; r < a.shard_begin + a.shard_count; ++r) {
+    k.add(u(a.kv.pool[r]));
+    k.add(u(a.kv.scale[r]));
+  }
+  k.add((uint64_t)a.fp8);
+  k.add((uint64_t)a.pool_rows);
+  k.add((uint64_t)a.num_pages);
+  k.add(u(a.pt));
+  k.add(u(a.seq_lens));
+  k.add((uint64_t)(uint32_t)a.max_pages);
+  k.add(((uint64_t)(uint32_t)a.B << 32) | (uint32_t)a.Tq);
+  k.add(((uint64_t)(uint32_t)a.H << 32) | (uint32_t)a.R);
+  k.add(((uint64_t)(uint32_t)a.P << 32) | (uint32_t)a.c);
+  k.add(((uint64_t)(uint32_t)a.shard_begin << 32) | (uint32_t)a.shard_count);
+  uint32_t sc = 0;
+  memcpy(&sc, &a.sm_scale, 4);
+  k.add(((uint64_t)(uint32_t)a.I << 32) | sc);
+  k.add((uint64_t)a.base2);
+  k.add(u(a.o_part));
+  k.add(u(a.lse_part));
+  k.add(u(a.err));
+  return k;
+}
+
+namespace {
+std::atomic<int32_t> g_wait_kcycles{kDefaultWaitKcycles};
+}
+
+int32_t pipeline_wait_kcycles() { return g_wait_kcycles.load(std::memory_order_relaxed); }
+
+int ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;   // (function, device)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DCPMLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& d : done)
+    if (d.first == func && d.second == dev) return DCPMLA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return DCPMLA_ERR_CUDA;
+  done.emplace_back(func, dev);
+  return DCPMLA_OK;
+}
+
+}  // namespace dcpmla
+
+namespace {
+
 // Few query rows (<= 16, bf16 KV) run on the token-major tensor-core kernel;
 // other shapes the tensor cores take run on the 128-row-tile kernel; the rest
 // on the CUDA-core kernel.
@@ -68,6 +135,13 @@ size_t workspace_for(const DecodeArgs& a, int sm) {
 }  // namespace
 
 extern "C" {
+
+int dcpmla_testing_set_wait_limit(int64_t cycles) {
+  // in units of 1024 cycles, rounded down (0: the first failed try gives up), capped at 2^31 units
+  const int64_t k = cycles > 0 ? std::min<int64_t>(cycles >> 10, INT32_MAX) : (int64_t)kDefaultWaitKcycles;
+  g_wait_kcycles.store((int32_t)k, std::memory_order_relaxed);
+  return DCPMLA_OK;
+}
 
 int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c,
                                  int32_t shard_count, int32_t kv_dtype, int32_t max_pages,

@@ -3,6 +3,9 @@
 #pragma once
 #include <cuda.h>
 
+#include <mutex>
+#include <new>
+
 #include "common.cuh"
 
 namespace dcpmla {
@@ -24,6 +27,81 @@ struct DecodeArgs {
   float* lse_part;          // [shard_count, B, R]
   int32_t* err;
 };
+
+// ---------------------------------------------------------------------------
+// Host-side reuse of prepared launches.  A decode call's kernel parameters (the
+// encoded tensor maps among them) depend only on its arguments, so a call that
+// repeats an earlier one (same pointers, shapes, workspace and device) reuses the
+// block prepared then instead of encoding it again.
+// ---------------------------------------------------------------------------
+struct LaunchKey {
+  uint64_t w[80];
+  int n = 0;
+  void add(uint64_t v) {
+    if (n < 80) w[n] = v;
+    ++n;
+  }
+  bool operator==(const LaunchKey& o) const {
+    if (n != o.n || n > 80) return false;
+    for (int i = 0; i < n; ++i)
+      if (w[i] != o.w[i]) return false;
+    return true;
+  }
+};
+
+// Every argument the preparation reads, plus the workspace, a kernel tag and the device.
+LaunchKey launch_key(const DecodeArgs& a, const void* ws, size_t ws_bytes, int tag);
+
+// A few prepared parameter blocks of one kind, least recently used evicted.  The caller
+// holds `mu` from get() until its launches have been enqueued.
+template <class Params, int kSlots = 8>
+struct ParamCache {
+  std::mutex mu;
+  struct Slot {
+    LaunchKey key;
+    Params* p = nullptr;
+    uint64_t used = 0;
+  };
+  Slot slots[kSlots];
+  uint64_t tick = 0;
+  // The block for `key`; `fresh` is set when it was (re)zeroed and must be filled.
+  // nullptr when no memory could be had.
+  Params* get(const LaunchKey& key, bool& fresh) {
+    if (key.n > 80) {
+      fresh = true;
+      return nullptr;
+    }
+    Slot* victim = &slots[0];
+    for (Slot& s : slots) {
+      if (s.p && s.key == key) {
+        s.used = ++tick;
+        fresh = false;
+        return s.p;
+      }
+      if (!s.p || s.used < victim->used) victim = &s;
+    }
+    if (!victim->p) victim->p = new (std::nothrow) Params();
+    if (!victim->p) return nullptr;
+    *victim->p = Params{};
+    victim->key = key;
+    victim->used = ++tick;
+    fresh = true;
+    return victim->p;
+  }
+  // Forget a block whose preparation failed.
+  void drop(const Params* p) {
+    for (Slot& s : slots)
+      if (s.p == p) s.key.n = -1;
+  }
+};
+
+// Limit after which a decode pipeline wait gives up, in units of 1024 clock64 cycles: about
+// one second unless a test has lowered it (dcpmla_testing_set_wait_limit).
+constexpr int32_t kDefaultWaitKcycles = 2000000000 / 1024;
+int32_t pipeline_wait_kcycles();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (function, device).
+int ensure_smem_attr(const void* func, int bytes);
 
 // 2-D tensor map over a row-major bf16 matrix [rows, cols] with 128-byte swizzle.
 int tma_encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,

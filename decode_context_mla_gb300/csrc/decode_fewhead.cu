@@ -74,7 +74,6 @@ constexpr int kRelayWarp = 10;
 constexpr int kPvWarp = 11;
 constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kColS = 0, kColO = 64, kTmemCols = 256;
-constexpr long long kWaitCycles = 2000000000LL;   // about one second
 
 constexpr int kOffKV = 0;
 constexpr int kOffQ = kOffKV + kStages * kStage;
@@ -94,21 +93,10 @@ struct FhParams {
   int32_t* ws_bad;                   // [slots]: the unit needed a page outside the pools
   int32_t* ws_pre;                   // [B * shard_count + 1]: first tile of each (request, shard)
   int32_t fused;                     // 1: every unit to the workspace, merged over shards into o, lse
+  int32_t wait_kcycles;              // a pipeline wait gives up after 1024 x this many clock64 cycles
 };
 static_assert(sizeof(FhParams) <= 4096, "kernel parameter space");
 
-template <bool kCluster>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const long long t0 = clock64();
-  while (true) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
 
 // Tokens of request b on shard r (0 for a length the launch rejects).
 __device__ __forceinline__ int shard_tokens(const DecodeArgs& a, int L, int r) {
@@ -167,6 +155,8 @@ __device__ __forceinline__ int fh_cluster_of(int T, int t, int G) {
   return k;
 }
 
+// kRL: waits give up after the launch's wait_kcycles instead of the fixed limit (tests only)
+template <bool kRL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_fh_bf16_kernel(const __grid_constant__ FhParams p) {
   const DecodeArgs& a = p.a;
@@ -187,7 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float lsum_s[2][2][4][8];   // [unit parity][warpgroup][quarter][row]
   __shared__ int seg_s[kThreads];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, ubad_s[2];
+  __shared__ int ubad_s[2], issued_s, q_issued_s;
+  __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t h = cluster_ctarank();
@@ -217,7 +208,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads / 32);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 2);                  // both MMA issuers
-    abort_s = 0;
+    wctl_s.abort = 0;
+    wctl_s.limit_kcycles = p.wait_kcycles;
+    issued_s = 0;
+    q_issued_s = 0;
     ubad_s[0] = ubad_s[1] = 0;
     fence_barrier_init();
   }
@@ -302,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_wait();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  volatile int* abort_flag = &abort_s;
+  volatile WaitCtl* abort_flag = &wctl_s;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -311,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[h][i]);
     }
     bool ok = true;
-    int gi = 0, kk = 0, issued = 0;
+    int gi = 0, kk = 0, issued = 0, q_issued = 0;
     const int box = p.box_rows;
     // Page ids run kLook tiles ahead of the loads (across unit boundaries) through a
     // per-lane FIFO: entry k holds, for lane l, box l of the tile k places ahead
@@ -355,8 +349,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const CUtensorMap* kvmap = &p.tm_kv[h][x.sr];
       bool okq = true;
       if (lane == 0) {
-        if (kk >= 2) okq = wait_bar<false>(smem_u32(&bar_q_free[qb]), ((kk >> 1) - 1) & 1, abort_flag);
+        if (kk >= 2) okq = wait_bar<false, kRL>(smem_u32(&bar_q_free[qb]), ((kk >> 1) - 1) & 1, abort_flag);
         if (okq) {
+          q_issued = kk + 1;
           const uint32_t qf = smem_u32(&bar_q_full[qb]);
           mbar_arrive_expect_tx(qf, (uint32_t)(nck * kQChunk));
           for (int c = 0; c < nck; ++c)
@@ -383,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         bool okw = true;
         if (lane == 0 && gi >= kStages)
-          okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((gi >> 1) - 1) & 1, abort_flag);
+          okw = wait_bar<false, kRL>(smem_u32(&bar_kv_empty[st]), ((gi >> 1) - 1) & 1, abort_flag);
         ok = __shfl_sync(0xffffffffu, (int)okw, 0) != 0;
         if (!ok) break;
         const uint32_t full = smem_u32(&bar_kv_full[st]);
@@ -417,20 +412,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       ++kk;
     }
-    if (lane == 0 && *abort_flag) {
-      // let copies already in flight land before the CTA's shared memory goes away
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(smem_u32(&bar_kv_full[i & 1]), (i >> 1) & 1) && clock64() - t0 < kWaitCycles / 8) {
-        }
-      }
-      for (int q = 0; q < 2; ++q) {
-        const int k = kk - 1 - q;   // the last two Q loads
-        if (k < 0) break;
-        const long long t0 = clock64();
-        while (!mbar_try_wait(smem_u32(&bar_q_full[k & 1]), (k >> 1) & 1) && clock64() - t0 < kWaitCycles / 8) {
-        }
-      }
+    if (lane == 0) {                                   // drained at the teardown
+      issued_s = issued;
+      q_issued_s = q_issued;
     }
   } else if (warp == 1 || warp == kPvWarp) {
     if (lane == 0) {
@@ -457,11 +441,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int ntiles = x.ntiles;
         const int qb = kk & 1, ob = kk & 1;
         if (qk_role) {
-          ok = wait_bar<false>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag);
+          ok = wait_bar<false, kRL>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag);
           for (int i = 0; ok && i < ntiles; ++i, ++gt) {
             const int sb = gt & 1;
-            if (gt >= 2) ok = wait_bar<false>(smem_u32(&bar_s_free[sb]), ((gt >> 1) - 1) & 1, abort_flag);
-            if (ok) ok = wait_bar<false>(smem_u32(&bar_kv_full[sb]), (gt >> 1) & 1, abort_flag);
+            if (gt >= 2) ok = wait_bar<false, kRL>(smem_u32(&bar_s_free[sb]), ((gt >> 1) - 1) & 1, abort_flag);
+            if (ok) ok = wait_bar<false, kRL>(smem_u32(&bar_kv_full[sb]), (gt >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
@@ -479,9 +463,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
           for (int i = 0; ok && i < ntiles; ++i, ++gt) {
             const int sb = gt & 1;
-            ok = wait_bar<false>(smem_u32(&bar_p_full[sb]), (gt >> 1) & 1, abort_flag);
+            ok = wait_bar<false, kRL>(smem_u32(&bar_p_full[sb]), (gt >> 1) & 1, abort_flag);
             if (ok && i == 0 && kk >= 2)
-              ok = wait_bar<false>(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1, abort_flag);
+              ok = wait_bar<false, kRL>(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -507,7 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // arrival per issuing thread)
       mma_commit(smem_u32(&bar_drain));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
   } else if (warp == kRelayWarp) {
@@ -517,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int total = t_hi - t_lo;   // the cluster's share of tiles
       const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
       for (int gi = 0; gi < total; ++gi) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read), gi & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_x_read), gi & 1, abort_flag)) break;
         mbar_arrive_remote(xe_peer);
       }
     }
@@ -565,7 +549,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this thread's page id, checked at the end of the tile (its load is in
         // flight meanwhile)
         const int gpg = tok < ntok ? __ldg(pt_row + (t0 + tok) / a.P) : 0;
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         uint32_t own[8];
@@ -577,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
         // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
         if (gi >= 1) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
           if (!ok) break;
         }
 #pragma unroll
@@ -585,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           st_async_v4(x_remote + (uint32_t)(((2 * g + v) * kTok + tok) * 16),
                       make_uint4(own[4 * v], own[4 * v + 1], own[4 * v + 2], own[4 * v + 3]), xfull_remote);
         if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), gi & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), gi & 1, abort_flag));
         if (!ok) break;
         float s[8];
 #pragma unroll
@@ -657,10 +641,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // phase before.
             if (gi >= 2) {
               ok = __all_sync(0xffffffffu,
-                              wait_bar<false>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
+                              wait_bar<false, kRL>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
               if (!ok) break;
             }
-            ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -685,7 +669,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // P^T as bf16 hi (rows 0-15) + lo (rows 16-31); one bf16 rounding of the
         // weights alone would cost ~1e-3 relative error in O
         if (gi >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
           if (!ok) break;
         }
         // P^T is MN-major with a 64-byte swizzle: a token's 32 rows (hi 0-15, lo 16-31) are
@@ -731,7 +715,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Not bar_o: when the last tile's softmax ends, the PV two tiles back may
         // still be running, and a parity wait on bar_o would then match an older
         // phase.  bar_o_full[ob] completes once per unit on this buffer.
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full[ob]), (kk >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_full[ob]), (kk >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
       }
@@ -806,6 +790,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Every role has left its loop.  After an abort, the KV and Q loads issued before it may
+  // still be in flight (their consumers gave up): they land before this CTA's shared memory
+  // goes away.
+  if (tid == 0 && wctl_s.abort) {
+    drain_ring(bar_kv_full, kStages, issued_s);
+    drain_ring(bar_q_full, 2, q_issued_s);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -813,7 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // the peer may still be writing into this CTA's exchange buffer or barriers
   cluster_arrive();
   cluster_wait();
-  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (wctl_s.abort && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
 }
 
 // Merge of the (request, shard) items split between clusters: one block per (item,
@@ -963,28 +954,38 @@ size_t fh_workspace_bytes(const DecodeArgs& a, int sm_count) { return plan_fh(a,
 int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st, bool fused) {
   const FhPlan plan = plan_fh(a, sm_count);
   if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
-  FhParams* fp = new (std::nothrow) FhParams();
+  static ParamCache<FhParams> cache;
+  const LaunchKey key = launch_key(a, ws, ws_bytes, fused ? 5 : 4);
+  std::lock_guard<std::mutex> lk(cache.mu);
+  bool fresh = false;
+  FhParams* fp = cache.get(key, fresh);
   if (!fp) return DCPMLA_ERR_CAPACITY;
   FhParams& p = *fp;
-  p.a = a;
-  p.box_rows = std::min(a.P, kTok);
-  p.fused = fused ? 1 : 0;
-  int rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
-  for (int hh = 0; hh < 2; ++hh)
-    for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
-      rc = tma_encode_kv_rowgroups(&p.tm_kv[hh][i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
-                                   hh ? 5u : 4u, (uint32_t)p.box_rows / 8);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
-  p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
-  p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
-  p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
-  if (rc == DCPMLA_OK &&
-      cudaFuncSetAttribute(decode_fh_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-          cudaSuccess)
-    rc = DCPMLA_ERR_CUDA;
+  int rc = DCPMLA_OK;
+  if (fresh) {
+    p.a = a;
+    p.box_rows = std::min(a.P, kTok);
+    p.fused = fused ? 1 : 0;
+    rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
+    for (int hh = 0; hh < 2; ++hh)
+      for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
+        rc = tma_encode_kv_rowgroups(&p.tm_kv[hh][i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
+                                     hh ? 5u : 4u, (uint32_t)p.box_rows / 8);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
+    p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
+    p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
+    p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
+    if (rc != DCPMLA_OK) {
+      cache.drop(fp);
+      return rc;
+    }
+  }
+  p.wait_kcycles = pipeline_wait_kcycles();
+  const auto kern = p.wait_kcycles == kDefaultWaitKcycles ? decode_fh_bf16_kernel<false> : decode_fh_bf16_kernel<true>;
+  rc = ensure_smem_attr((const void*)kern, (int)kSmemBytes);
   if (rc == DCPMLA_OK) {
-    decode_fh_bf16_kernel<<<2 * plan.clusters, kThreads, kSmemBytes, st>>>(p);
+    kern<<<2 * plan.clusters, kThreads, kSmemBytes, st>>>(p);
     rc = launch_status();
   }
   if (rc == DCPMLA_OK && fused) {
@@ -996,7 +997,6 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o, p.ws_lse, p.ws_bad);
     rc = launch_status();
   }
-  delete fp;
   return rc;
 }
 

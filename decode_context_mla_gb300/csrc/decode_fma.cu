@@ -346,8 +346,7 @@ int launch_decode_fma(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_cou
   if (z > 65535 || plan.row_groups > 65535) return DCPMLA_ERR_UNSUPPORTED;
   const size_t smem = smem_bytes(a.fp8);
   const auto kern = a.fp8 ? decode_fma_kernel<true> : decode_fma_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return DCPMLA_ERR_CUDA;
+  if (ensure_smem_attr((const void*)kern, (int)smem) != DCPMLA_OK) return DCPMLA_ERR_CUDA;
   FmaParams fp{};
   fp.a = a;
   fp.num_splits = plan.splits;

@@ -56,7 +56,6 @@ constexpr int kXBytes = kRows * kTileTok * 4;        // one fp32 partial score t
 constexpr int kSoftmaxThreads = 256;
 constexpr int kWgThreads = 128;                     // one softmax warpgroup
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitCycles = 2000000000LL;     // about one second
 constexpr int kMaxCombineParts = 80;                // clusters one item may span (<= SM pairs)
 
 struct TcParams {
@@ -80,20 +79,8 @@ struct TcParams {
   CUtensorMap tm_qr;                  // q as [B R, 576], box {32, 128}, 64-byte swizzle
   CUtensorMap tm_o;                   // o_part as {512, R, shards x B} fp32, box {32, 32, 1}, 128-byte swizzle
   CUtensorMap tm_ws;                  // workspace partials as {512, 128, slots} fp32, the same box
+  int32_t wait_kcycles;               // a pipeline wait gives up after 1024 x this many clock64 cycles
 };
-
-template <bool kCluster>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const long long t0 = clock64();
-  while (true) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
 
 // Tiled store of a shared-memory box to global memory; completion by bulk group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
@@ -254,6 +241,7 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQ = 448;
 static_assert(kSmemBytes <= 227 * 1024 - 4096, "stages, Q and exchange buffers exceed shared memory");
 }  // namespace b16
 
+template <bool kRL>
 __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
   using namespace b16;
   const DecodeArgs& a = p.a;
@@ -269,7 +257,8 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
   __shared__ float mref_s[2][kRows];                     // a warpgroup's reference max after its tile
   __shared__ float l_s[2][kRows], m_s[2][kRows];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, bad_s, last_s;
+  __shared__ int bad_s, last_s, issued_s;
+  __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
@@ -299,7 +288,9 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     mbar_init(smem_u32(&bar_drain_qk), 1);
     mbar_init(smem_u32(&bar_drain_pv), 1);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);
-    abort_s = 0;
+    wctl_s.abort = 0;
+    wctl_s.limit_kcycles = p.wait_kcycles;
+    issued_s = 0;
     bad_s = 0;
     last_s = 0;
     fence_barrier_init();
@@ -332,7 +323,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     j1 = j0;
   }
   const int ntiles = (j1 - j0 + kTileTok - 1) / kTileTok;
-  volatile int* abort_flag = &abort_s;
+  volatile WaitCtl* abort_flag = &wctl_s;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -385,7 +376,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         }
         if (i >= kStages) {
           bool okw = true;
-          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
+          if (lane == 0) okw = wait_bar<false, kRL>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
         }
         int tok;
@@ -409,15 +400,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         issued = i + 1;
         if (ip < ntiles) prefetch_tile(ip);
       }
-      if (lane == 0 && *abort_flag) {
-        // let copies already in flight land before the CTA's shared memory goes away
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
-          const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
-                 clock64() - t0 < kWaitCycles / 8) {
-          }
-        }
-      }
+      if (lane == 0) issued_s = issued;                   // drained at the teardown
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
@@ -431,11 +414,11 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
       const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
       const uint32_t tq = tmem + kColQ;
-      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
+      bool ok = wait_bar<false, kRL>(smem_u32(&bar_q_full), 0, abort_flag);
       tc_fence_after();
       for (int i = 0; ok && i < ntiles; ++i) {
         const int st = i % kStages;
-        if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + kColS + st * kTileTok;
         const uint64_t so = (uint64_t)((st * kStage) >> 4);
@@ -457,7 +440,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       // drain: every MMA issued above completes before TMEM is released
       mma_commit(smem_u32(&bar_drain_qk));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
   } else if (warp == 10) {
@@ -470,7 +453,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const uint32_t to = tmem + kColO;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (!wait_bar<false>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag)) break;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
         const uint32_t pa = tmem + kColS + st * kTileTok;
@@ -483,7 +466,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       }
       mma_commit(smem_u32(&bar_drain_pv));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
   } else if (warp == 11) {
@@ -492,7 +475,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // the peer its next partial may overwrite that exchange buffer
     if (lane == 0) {
       for (int i = 0; i < ntiles; ++i) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read[i & 1]), (i >> 1) & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_x_read[i & 1]), (i >> 1) & 1, abort_flag)) break;
         mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[i & 1]), peer));
       }
     }
@@ -566,13 +549,13 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const int t0 = j0 + i * kTileTok;
       const int ntok = min(kTileTok, j1 - t0);
       const uint32_t scol = tmem + lane_off + kColS + st * kTileTok;
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (i / kStages) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[st]), (i / kStages) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       // send this CTA's partial into the peer's buffer g ([16 column groups][128 rows]
       // of float4), once the peer has read what this warpgroup sent two tiles ago
       if (i >= 2) {
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), ((i >> 1) - 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty[g]), ((i >> 1) - 1) & 1, abort_flag));
         if (!ok) break;
       }
       const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
@@ -587,7 +570,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         st_async_v4(x_remote + g * kXBytes + (c * kRows + row) * 16,
                     make_uint4(xb[4 * c], xb[4 * c + 1], xb[4 * c + 2], xb[4 * c + 3]), xfull_remote);
       if (row == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
-      ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (i >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full[g]), (i >> 1) & 1, abort_flag));
       if (!ok) break;
       const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
 #pragma unroll
@@ -614,7 +597,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       // the reference max as the previous tile (the other warpgroup's) left it
       float m_ref = -INFINITY;
       if (i >= 1) {
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[g ^ 1]), ((i - 1) >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_mref[g ^ 1]), ((i - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
         m_ref = mref_s[g ^ 1][row];
       }
@@ -626,7 +609,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       const bool rescale_me = move && m_ref != -INFINITY;
       if (__any_sync(0xffffffffu, rescale_me)) {
         ok = __all_sync(0xffffffffu,
-                        wait_bar<false>(smem_u32(&bar_o_par[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag));
+                        wait_bar<false, kRL>(smem_u32(&bar_o_par[(i - 1) & 1]), ((i - 1) >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
@@ -686,11 +669,11 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
       mbar_arrive(smem_u32(&bar_p_full[st]));
     }
     // ---- epilogue ----
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
+    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_full), 0, abort_flag));
     l_s[g][row] = l;
     m_s[g][row] = m_own;
     mbar_arrive(smem_u32(&bar_l));
-    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
+    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_l), 0, abort_flag));
     ok = ok && l_ok;
     // O follows the latest reference (the larger, since the reference only grows);
     // each warpgroup's sum is brought to it
@@ -745,6 +728,9 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
 
   tc_fence_before();
   __syncthreads();
+  // Every role has left its loop.  After an abort, loads issued before it may still be in
+  // flight (their consumer gave up): they land before this CTA's shared memory goes away.
+  if (tid == 0 && wctl_s.abort) drain_ring(bar_kv_full, kStages, issued_s);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -752,7 +738,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
   // the peer may still be writing into this CTA's exchange buffer or barriers
   cluster_arrive();
   cluster_wait();
-  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (wctl_s.abort && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
   if (p.num_splits == 1 && !p.fused) return;
   tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
 }
@@ -963,6 +949,7 @@ __global__ void __launch_bounds__(256) tc_unit_combine_kernel(const TcParams p) 
   }
 }
 
+template <bool kRL>
 __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
   using namespace b16;
   const DecodeArgs& a = p.a;
@@ -979,7 +966,8 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
   __shared__ float l_s[2][kRows], m_s[2][kRows];
   __shared__ int unit_bad_s[pp::kUnitFlags];             // unit u met a bad page: entry u % 8
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s;
+  __shared__ int issued_s, q_last_s;
+  __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
@@ -1008,7 +996,10 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     mbar_init(smem_u32(&bar_drain_pv), 1);
     mbar_init(smem_u32(&bar_l), kSoftmaxThreads);              // once per unit
     mbar_init(smem_u32(&bar_stg), kSoftmaxThreads);            // once per unit: O has left sX
-    abort_s = 0;
+    wctl_s.abort = 0;
+    wctl_s.limit_kcycles = p.wait_kcycles;
+    issued_s = 0;
+    q_last_s = -1;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -1024,7 +1015,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
   cluster_wait();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  volatile int* abort_flag = &abort_s;
+  volatile WaitCtl* abort_flag = &wctl_s;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -1080,7 +1071,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         }
         if (gi >= kStages) {
           bool okw = true;
-          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((gi / kStages) - 1) & 1, abort_flag);
+          if (lane == 0) okw = wait_bar<false, kRL>(smem_u32(&bar_kv_empty[st]), ((gi / kStages) - 1) & 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, (int)okw, 0)) {
             ok = false;
             break;
@@ -1117,15 +1108,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       }
       ++ui;
     }
-    if (lane == 0 && *abort_flag) {
-      // let copies already in flight land before the CTA's shared memory goes away
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(smem_u32(&bar_kv_full[i % kStages]), (i / kStages) & 1) &&
-               clock64() - t0 < kWaitCycles / 8) {
-        }
-      }
-    }
+    if (lane == 0) issued_s = issued;                     // drained at the teardown
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
     // S(gi) = Q_h K_h(gi)^T into slot gi % 3, once the unit's Q is loaded; the slot is
@@ -1142,11 +1125,11 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
         pp::Unit u;
         if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
-        if (!wait_bar<false>(smem_u32(&bar_q_full), ui & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_q_full), ui & 1, abort_flag)) break;
         tc_fence_after();
         for (int i = 0; i < u.ntiles; ++i, ++gi) {
           const int st = gi % kStages;
-          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (gi / kStages) & 1, abort_flag)) {
+          if (!wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (gi / kStages) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -1172,7 +1155,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       }
       mma_commit(smem_u32(&bar_drain_qk));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
   } else if (warp == 10) {
@@ -1190,8 +1173,8 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
         for (int i = 0; i < u.ntiles; ++i, ++gi) {
           const int st = gi % kStages;
-          if (!wait_bar<false>(smem_u32(&bar_p_full[st]), (gi / kStages) & 1, abort_flag) ||
-              (i == 0 && ui > 0 && !wait_bar<false>(smem_u32(&bar_o_free), (ui - 1) & 1, abort_flag))) {
+          if (!wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (gi / kStages) & 1, abort_flag) ||
+              (i == 0 && ui > 0 && !wait_bar<false, kRL>(smem_u32(&bar_o_free), (ui - 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -1209,7 +1192,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       }
       mma_commit(smem_u32(&bar_drain_pv));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
   } else if (warp == 11) {
@@ -1225,7 +1208,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       // release (the peer may send tile 1) waits for unit 0's O when unit 0 has one tile
       mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[0]), peer));
       if (it0 < p.items && min(__ldg(p.ws_pre + it0 + 1), t_hi) - t_lo == 1)
-        okr = wait_bar<false>(smem_u32(&bar_stg), 0, abort_flag);
+        okr = wait_bar<false, kRL>(smem_u32(&bar_stg), 0, abort_flag);
       if (okr) mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty[1]), peer));
       for (int it = it0; okr && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
         pp::Unit u;
@@ -1235,12 +1218,12 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           ++itn;
         const int nnext = itn < p.items ? max(0, min(__ldg(p.ws_pre + itn + 1), t_hi) - __ldg(p.ws_pre + itn)) : 0;
         for (int i = 0; i < u.ntiles; ++i, ++gi) {
-          if (!wait_bar<false>(smem_u32(&bar_x_read[gi & 1]), (gi >> 1) & 1, abort_flag)) {
+          if (!wait_bar<false, kRL>(smem_u32(&bar_x_read[gi & 1]), (gi >> 1) & 1, abort_flag)) {
             okr = false;
             break;
           }
           const int wait_unit = (i == u.ntiles - 1 && nnext == 1) ? ui + 1 : (i >= u.ntiles - 2 ? ui : -1);
-          if (wait_unit >= 0 && !wait_bar<false>(smem_u32(&bar_stg), wait_unit & 1, abort_flag)) {
+          if (wait_unit >= 0 && !wait_bar<false, kRL>(smem_u32(&bar_stg), wait_unit & 1, abort_flag)) {
             okr = false;
             break;
           }
@@ -1321,12 +1304,12 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         const int t0 = u.j0 + i * kTileTok;
         const int ntok = min(kTileTok, u.j1 - t0);
         const uint32_t scol = tmem + lane_off + kColS + st * kTileTok;
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[st]), (gt / kStages) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[st]), (gt / kStages) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         // send this CTA's partial into the peer's buffer g, once the peer has released it
         // (read what this warpgroup sent two tiles ago, and let a unit's O out through it)
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty[g]), (gt >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty[g]), (gt >> 1) & 1, abort_flag));
         if (!ok) break;
         const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full[g]), peer);
         float x[64];
@@ -1339,7 +1322,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           st_async_v4(x_remote + g * kXBytes + (c * kRows + row) * 16,
                       make_uint4(xb[4 * c], xb[4 * c + 1], xb[4 * c + 2], xb[4 * c + 3]), xfull_remote);
         if (row == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full[g]), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full[g]), (gt >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full[g]), (gt >> 1) & 1, abort_flag));
         if (!ok) break;
         const float4* xin = reinterpret_cast<const float4*>(sX + g * kXBytes);
 #pragma unroll
@@ -1365,7 +1348,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         // the reference max as the unit's previous tile (the other warpgroup's) left it
         float m_ref = -INFINITY;
         if (i >= 1) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_mref[g ^ 1]), ((gt - 1) >> 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_mref[g ^ 1]), ((gt - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
           m_ref = mref_s[g ^ 1][row];
         }
@@ -1375,7 +1358,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         const bool rescale_me = move && m_ref != -INFINITY;
         if (__any_sync(0xffffffffu, rescale_me)) {
           ok = __all_sync(0xffffffffu,
-                          wait_bar<false>(smem_u32(&bar_o_par[(gt - 1) & 1]), ((gt - 1) >> 1) & 1, abort_flag));
+                          wait_bar<false, kRL>(smem_u32(&bar_o_par[(gt - 1) & 1]), ((gt - 1) >> 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
           const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
@@ -1446,7 +1429,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           // completion of this unit's q_full phase: no arrival can reach that phase, and the
           // QK issuer has seen it before the next one can complete
           const int gl = gi - 1;
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[gl % kStages]), (gl / kStages) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[gl % kStages]), (gl / kStages) & 1, abort_flag));
           if (ok) {
             tc_fence_after();
             const bool tma_thread = warp == 2 + 4 * g && lane == 0;
@@ -1465,11 +1448,11 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         }
       }
       // ---- the unit's epilogue ----
-      if (ok) ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), ui & 1, abort_flag));
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_full), ui & 1, abort_flag));
       l_s[g][row] = l;
       m_s[g][row] = m_own;
       mbar_arrive(smem_u32(&bar_l));
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), ui & 1, abort_flag)) && ok;
+      ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_l), ui & 1, abort_flag)) && ok;
       const float m0 = m_s[0][row], m1 = m_s[1][row];
       const float m_tot = fmaxf(m0, m1);
       const float l_tot = (m0 == -INFINITY ? 0.f : l_s[0][row] * ex2_approx(m0 - m_tot)) +
@@ -1537,16 +1520,23 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       mbar_arrive(smem_u32(&bar_stg));
       ++ui;
     }
-    if (q_last >= 0 && *abort_flag) {
-      // let the last Q copy land before the CTA's shared memory goes away
-      const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_q_full), q_last & 1) && clock64() - t0 < kWaitCycles / 8) {
-      }
-    }
+    if (q_last >= 0) atomicMax(&q_last_s, q_last);         // drained at the teardown
   }
 
   tc_fence_before();
   __syncthreads();
+  // Every role has left its loop.  After an abort, the KV and Q copies issued before it may
+  // still be in flight (their consumers gave up): they land before this CTA's shared memory
+  // goes away.  (A Q phase also needs its TMEM-part arrivals; if the abort cut those, the
+  // wait runs to its limit, long after the copy itself has landed.)
+  if (tid == 0 && wctl_s.abort) {
+    drain_ring(bar_kv_full, kStages, issued_s);
+    if (q_last_s >= 0) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(&bar_q_full), q_last_s & 1) && clock64() - t0 < kDrainCycles) {
+      }
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -1554,12 +1544,14 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
   // the peer may still be writing into this CTA's exchange buffers or barriers
   cluster_arrive();
   cluster_wait();
-  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (wctl_s.abort && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
 }
 
+// kRL: waits give up after the launch's wait_kcycles instead of the fixed limit (tests only)
+template <bool kRL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
     decode_tc_bf16_persist_kernel(const __grid_constant__ TcParams p) {
-  decode_tc_bf16_persist_body(p);
+  decode_tc_bf16_persist_body<kRL>(p);
 }
 
 // ------------------------------------------------------------ E4M3 KV
@@ -1593,6 +1585,7 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 static_assert(kSmemBytes <= 227 * 1024 - 6144, "stages, Q and exchange buffer exceed shared memory");
 }  // namespace e4
 
+template <bool kRL>
 __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
   using namespace e4;
   const DecodeArgs& a = p.a;
@@ -1612,7 +1605,8 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
   __shared__ float l_s[2][kRows], m_s[2][kRows];
   __shared__ float kscale_s[kStages][kTileTok];          // the stage's per-token scales
   __shared__ uint32_t tmem_base_s;
-  __shared__ int abort_s, bad_s, last_s;
+  __shared__ int bad_s, last_s, issued_s;
+  __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t h = cluster_ctarank();                  // which key dims this CTA owns
@@ -1646,7 +1640,9 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_o_full), 1);
     mbar_init(smem_u32(&bar_drain), 1);
-    abort_s = 0;
+    wctl_s.abort = 0;
+    wctl_s.limit_kcycles = p.wait_kcycles;
+    issued_s = 0;
     bad_s = 0;
     last_s = 0;
     fence_barrier_init();
@@ -1679,7 +1675,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
     j1 = j0;
   }
   const int ntiles = (j1 - j0 + kTileTok - 1) / kTileTok;
-  volatile int* abort_flag = &abort_s;
+  volatile WaitCtl* abort_flag = &wctl_s;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
@@ -1692,7 +1688,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         const int st = i % kRawStages;
         if (i >= kRawStages) {
           bool okw = true;
-          if (lane == 0) okw = wait_bar<false>(smem_u32(&bar_raw_empty[st]), ((i / kRawStages) - 1) & 1, abort_flag);
+          if (lane == 0) okw = wait_bar<false, kRL>(smem_u32(&bar_raw_empty[st]), ((i / kRawStages) - 1) & 1, abort_flag);
           if (!__shfl_sync(0xffffffffu, (int)okw, 0)) break;
         }
         const int t0 = j0 + i * kTileTok;
@@ -1721,15 +1717,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         }
         issued = i + 1;
       }
-      if (lane == 0 && *abort_flag) {
-        // let copies already in flight land before the CTA's shared memory goes away
-        for (int i = max(0, issued - kRawStages); i < issued; ++i) {
-          const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&bar_raw_full[i % kRawStages]), (i / kRawStages) & 1) &&
-                 clock64() - t0 < kWaitCycles / 8) {
-          }
-        }
-      }
+      if (lane == 0) issued_s = issued;                   // drained at the teardown
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
@@ -1742,12 +1730,12 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
       const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);        // MN-major values
       const uint64_t qd0 = desc_sw128(smem_u32(sQr), 16, 1024);            // rope part of Q
       const uint32_t tq = tmem + kColQ, to = tmem + kColO;
-      bool ok = wait_bar<false>(smem_u32(&bar_q_full), 0, abort_flag);
+      bool ok = wait_bar<false, kRL>(smem_u32(&bar_q_full), 0, abort_flag);
       tc_fence_after();
       for (int i = 0; ok && i <= ntiles; ++i) {
         if (i < ntiles) {
           const int st = i % kStages, sb = i & 1;
-          if (!wait_bar<false>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
+          if (!wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
           tc_fence_after();
           const uint32_t d = tmem + kColS + sb * kTileTok;
           const uint64_t kd = kd0 + (uint64_t)((st * kStage) >> 4);
@@ -1764,7 +1752,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         }
         if (i >= 1) {
           const int pi = i - 1, st = pi % kStages, sb = pi & 1;
-          if (!wait_bar<false>(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
+          if (!wait_bar<false, kRL>(smem_u32(&bar_p_full[sb]), (pi >> 1) & 1, abort_flag)) break;
           tc_fence_after();
           const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
           const uint32_t pa = tmem + kColS + sb * kTileTok;
@@ -1779,7 +1767,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
       // drain: every MMA issued above completes before TMEM is released
       mma_commit(smem_u32(&bar_drain));
       const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kWaitCycles) {
+      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
     if (lane == 1) {
@@ -1787,7 +1775,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
       // tell the peer its next partial may overwrite our exchange buffer.  This
       // thread has no stores in flight, so its cluster-scope release is cheap.
       for (int i = 0; i < ntiles; ++i) {
-        if (!wait_bar<false>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
+        if (!wait_bar<false, kRL>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
         mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty), peer));
       }
     }
@@ -1802,10 +1790,10 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         const int rs = i % kRawStages, st = i % kStages;
         const int t0 = j0 + i * kTileTok;
         const int ntok = min(kTileTok, j1 - t0);
-        if (!__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_raw_full[rs]), (i / kRawStages) & 1, abort_flag)))
+        if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_raw_full[rs]), (i / kRawStages) & 1, abort_flag)))
           break;
         if (i >= kStages &&
-            !__all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag)))
+            !__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_kv_empty[st]), ((i / kStages) - 1) & 1, abort_flag)))
           break;
         const uint8_t* raw = sRaw + rs * kRawStage;
         uint8_t* dst = sKV + st * kStage;
@@ -1909,7 +1897,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
       for (int i = 0; ok && i < ntiles; ++i) {
         const int sb = i & 1, st = i % kStages;
         const int t0 = j0 + i * kTileTok;
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[sb]), (i >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         uint32_t own[32];
@@ -1920,7 +1908,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
         // float4), once the peer has read the previous one
         if (i >= 1) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
           if (!ok) break;
         }
 #pragma unroll
@@ -1928,7 +1916,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
           st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
                       make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
         if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(smem_u32(&bar_x_full), i & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), i & 1, abort_flag));
         if (!ok) break;
         float x[32];
         const float4* xin = reinterpret_cast<const float4*>(sX);
@@ -1962,7 +1950,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         xmax_s[i & 1][g][row] = tmax;
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_max[i & 1]));
-        ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_max[i & 1]), (i >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         tmax = fmaxf(tmax, xmax_s[i & 1][g ^ 1][row]) * qscale;
@@ -1972,7 +1960,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         const bool move = tmax > m_ref + 8.f;
         const bool rescale_me = move && m_ref != -INFINITY;
         if (__any_sync(0xffffffffu, rescale_me)) {
-          ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o), (i - 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
           const float alpha = rescale_me ? ex2_approx(m_ref - tmax) : 1.f;
@@ -2012,11 +2000,11 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
     if (ok && ntiles > 0)
       // Not bar_o: when the last tile's softmax ends, PV(ntiles - 2) may still be
       // running, and a parity wait on bar_o would then match an older phase.
-      ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_o_full), 0, abort_flag));
+      ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_full), 0, abort_flag));
     l_s[g][row] = l;
     m_s[g][row] = m_own;
     mbar_arrive(smem_u32(&bar_l));
-    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false>(smem_u32(&bar_l), 0, abort_flag));
+    const bool l_ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_l), 0, abort_flag));
     ok = ok && l_ok;
     // O follows the latest reference (the larger, since the reference only grows);
     // each warpgroup's sum is brought to it
@@ -2059,6 +2047,9 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
 
   tc_fence_before();
   __syncthreads();
+  // Every role has left its loop.  After an abort, raw loads issued before it may still be
+  // in flight (the converters gave up): they land before this CTA's shared memory goes away.
+  if (tid == 0 && wctl_s.abort) drain_ring(bar_raw_full, kRawStages, issued_s);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -2066,20 +2057,22 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
   // the peer may still be writing into this CTA's exchange buffer or barriers
   cluster_arrive();
   cluster_wait();
-  if (abort_s && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
+  if (wctl_s.abort && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
   if (p.num_splits == 1 && !p.fused) return;
 
   tc_combine_tail<kThreads>(p, b, bz, sr, rt, sKV, (size_t)kStages * kStage, &last_s);
 }
 
 
+template <bool kRL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
     decode_tc_bf16_kernel(const __grid_constant__ TcParams p) {
-  decode_tc_bf16_body(p);
+  decode_tc_bf16_body<kRL>(p);
 }
+template <bool kRL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(e4::kThreads, 1)
     decode_tc_e4m3_kernel(const __grid_constant__ TcParams p) {
-  decode_tc_e4m3_body(p);
+  decode_tc_e4m3_body<kRL>(p);
 }
 
 // ------------------------------------------------------------------ host side
@@ -2306,44 +2299,54 @@ int encode_bf16_maps(TcParams& p, const DecodeArgs& a) {
 int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
   const PpPlan plan = plan_pp(a, sm_count);
   if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
-  TcParams* tp = new (std::nothrow) TcParams();
+  static ParamCache<TcParams> cache;
+  const LaunchKey key = launch_key(a, ws, ws_bytes, 1);
+  std::lock_guard<std::mutex> lk(cache.mu);
+  bool fresh = false;
+  TcParams* tp = cache.get(key, fresh);
   if (!tp) return DCPMLA_ERR_CAPACITY;
   TcParams& p = *tp;
-  p.a = a;
-  p.box_rows = std::min(a.P, kTileTok);
-  p.num_splits = 1;
-  p.chunk = 0;
-  p.row_tiles = plan.row_tiles;
-  p.fused = 0;
-  p.clusters = plan.clusters;
-  p.items = plan.items;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
-  p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
-  p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
-  p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
-  int rc = encode_bf16_maps(p, a);
-  if (rc == DCPMLA_OK) rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
-  if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_qr, a.q, (uint64_t)a.B * a.R, kRows);
-  if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_o, a.o_part, (uint64_t)a.R, (uint64_t)a.shard_count * a.B);
-  if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_ws, p.ws_o, kRows, (uint64_t)plan.slots);
+  int rc = DCPMLA_OK;
+  if (fresh) {
+    p.a = a;
+    p.box_rows = std::min(a.P, kTileTok);
+    p.num_splits = 1;
+    p.chunk = 0;
+    p.row_tiles = plan.row_tiles;
+    p.fused = 0;
+    p.clusters = plan.clusters;
+    p.items = plan.items;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
+    p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
+    p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
+    p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
+    rc = encode_bf16_maps(p, a);
+    if (rc == DCPMLA_OK) rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
+    if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_qr, a.q, (uint64_t)a.B * a.R, kRows);
+    if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_o, a.o_part, (uint64_t)a.R, (uint64_t)a.shard_count * a.B);
+    if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_ws, p.ws_o, kRows, (uint64_t)plan.slots);
+    if (rc != DCPMLA_OK) {
+      cache.drop(tp);
+      return rc;
+    }
+  }
+  p.wait_kcycles = pipeline_wait_kcycles();
+  const auto kern = p.wait_kcycles == kDefaultWaitKcycles ? decode_tc_bf16_persist_kernel<false>
+                                                          : decode_tc_bf16_persist_kernel<true>;
+  rc = ensure_smem_attr((const void*)kern, (int)b16::kSmemBytes);
   if (rc == DCPMLA_OK) {
     tc_prefix_kernel<<<1, 1024, 0, st>>>(a, plan.row_tiles, plan.items, p.ws_pre);
     rc = launch_status();
   }
-  if (rc == DCPMLA_OK &&
-      cudaFuncSetAttribute(decode_tc_bf16_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)b16::kSmemBytes) != cudaSuccess)
-    rc = DCPMLA_ERR_CUDA;
   if (rc == DCPMLA_OK) {
-    decode_tc_bf16_persist_kernel<<<2 * plan.clusters, b16::kThreads, b16::kSmemBytes, st>>>(p);
+    kern<<<2 * plan.clusters, b16::kThreads, b16::kSmemBytes, st>>>(p);
     rc = launch_status();
   }
   if (rc == DCPMLA_OK) {
     tc_unit_combine_kernel<<<dim3((unsigned)plan.items, kRows / pp::kCombineRows), 256, 0, st>>>(p);
     rc = launch_status();
   }
-  delete tp;
   return rc;
 }
 }  // namespace
@@ -2355,16 +2358,14 @@ size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
 int tc_kernel_launches(const DecodeArgs& a, bool fused) { return use_pp(a, fused) ? 3 : 1; }
 
 template <bool kFp8>
-int set_tc_smem() {
-  auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
-  const size_t smem = kFp8 ? e4::kSmemBytes : b16::kSmemBytes;
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess
-             ? DCPMLA_OK : DCPMLA_ERR_CUDA;
+auto tc_kernel(bool runtime_limit) {
+  return kFp8 ? (runtime_limit ? decode_tc_e4m3_kernel<true> : decode_tc_e4m3_kernel<false>)
+              : (runtime_limit ? decode_tc_bf16_kernel<true> : decode_tc_bf16_kernel<false>);
 }
 
 template <bool kFp8>
 int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
-  auto kern = kFp8 ? decode_tc_e4m3_kernel : decode_tc_bf16_kernel;
+  auto kern = tc_kernel<kFp8>(p.wait_kcycles != kDefaultWaitKcycles);
   const int threads = kFp8 ? e4::kThreads : b16::kThreads;
   const size_t smem = kFp8 ? e4::kSmemBytes : b16::kSmemBytes;
   const dim3 grid((unsigned)(2 * plan.splits), (unsigned)plan.row_tiles,
@@ -2381,39 +2382,52 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   // every refusal comes before the first enqueue: a refused call leaves the workspace alone
   if ((int64_t)a.B * a.shard_count > 65535 || plan.row_tiles > 65535 || 2LL * plan.splits > INT32_MAX)
     return DCPMLA_ERR_UNSUPPORTED;
-  TcParams* tp = new (std::nothrow) TcParams();
+  static ParamCache<TcParams> cache;
+  const LaunchKey key = launch_key(a, ws, ws_bytes, fused ? 3 : 2);
+  std::lock_guard<std::mutex> lk(cache.mu);
+  bool fresh = false;
+  TcParams* tp = cache.get(key, fresh);
   if (!tp) return DCPMLA_ERR_CAPACITY;
   TcParams& p = *tp;
-  p.a = a;
-  p.box_rows = std::min(a.P, kTileTok);
-  p.num_splits = plan.splits;
-  p.chunk = plan.chunk;
-  p.row_tiles = plan.row_tiles;
-  p.fused = fused ? 1 : 0;
   int rc = DCPMLA_OK;
-  for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
-    const void* pool = a.kv.pool[a.shard_begin + i];
-    rc = a.fp8 ? encode_rows_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, 64, (uint32_t)p.box_rows)
-               : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+  if (fresh) {
+    p.a = a;
+    p.box_rows = std::min(a.P, kTileTok);
+    p.num_splits = plan.splits;
+    p.chunk = plan.chunk;
+    p.row_tiles = plan.row_tiles;
+    p.fused = fused ? 1 : 0;
+    for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
+      const void* pool = a.kv.pool[a.shard_begin + i];
+      rc = a.fp8 ? encode_rows_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, 64, (uint32_t)p.box_rows)
+                 : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+    }
+    for (int i = 0; rc == DCPMLA_OK && !a.fp8 && i < a.shard_count; ++i)
+      rc = encode_rows_rope(&p.tm_rope[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
+                            (uint32_t)p.box_rows);
+    p.use3d = !a.fp8 && p.box_rows == kTileTok;
+    for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
+      if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
+        p.use3d = 0;   // fall back to one 2-D box per chunk
+    if (plan.splits > 1 || fused) {
+      uint8_t* w = static_cast<uint8_t*>(ws);
+      p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
+      p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
+      p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
+    }
+    if (rc != DCPMLA_OK) {
+      cache.drop(tp);
+      return rc;
+    }
   }
-  for (int i = 0; rc == DCPMLA_OK && !a.fp8 && i < a.shard_count; ++i)
-    rc = encode_rows_rope(&p.tm_rope[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
-                          (uint32_t)p.box_rows);
-  p.use3d = !a.fp8 && p.box_rows == kTileTok;
-  for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
-    if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
-      p.use3d = 0;   // fall back to one 2-D box per chunk
-  if (rc == DCPMLA_OK) rc = a.fp8 ? set_tc_smem<true>() : set_tc_smem<false>();
-  if (rc == DCPMLA_OK && (plan.splits > 1 || fused)) {
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
-    p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
-    p.ws_o = reinterpret_cast<float*>(w + plan.o_off);
-    if (cudaMemsetAsync(p.ws_cnt, 0, (size_t)a.B * a.shard_count * plan.row_tiles * 4, st) != cudaSuccess)
-      rc = DCPMLA_ERR_CUDA;
-  }
+  p.wait_kcycles = pipeline_wait_kcycles();
+  const bool rl = p.wait_kcycles != kDefaultWaitKcycles;
+  rc = a.fp8 ? ensure_smem_attr((const void*)tc_kernel<true>(rl), (int)e4::kSmemBytes)
+             : ensure_smem_attr((const void*)tc_kernel<false>(rl), (int)b16::kSmemBytes);
+  if (rc == DCPMLA_OK && (plan.splits > 1 || fused) &&
+      cudaMemsetAsync(p.ws_cnt, 0, (size_t)a.B * a.shard_count * plan.row_tiles * 4, st) != cudaSuccess)
+    rc = DCPMLA_ERR_CUDA;
   if (rc == DCPMLA_OK) rc = a.fp8 ? launch_tc<true>(p, plan, st) : launch_tc<false>(p, plan, st);
-  delete tp;
   return rc;
 }
 

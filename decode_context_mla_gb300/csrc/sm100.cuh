@@ -73,6 +73,52 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// ---------------------------------------------------------------- bounded waits
+// Limit, in clock64 cycles, of the waits that let copies and MMAs already issued finish
+// (about an eighth of a second at 2 GHz; such work ends in microseconds).
+constexpr long long kDrainCycles = 250000000LL;
+
+// Per-CTA state of the pipeline's waits, in shared memory: the abort flag and, for kernels
+// built with a runtime limit, the limit in units of 1024 clock64 cycles.
+struct WaitCtl {
+  int abort;
+  int limit_kcycles;
+};
+
+// The fixed limit of the production kernels: about one second at 2 GHz.
+constexpr long long kWaitCycles = 2000000000LL;
+
+// Wait for the phase with `parity`.  Gives up (false) at once when the CTA has aborted, or
+// after the limit, which aborts the CTA: every later wait of the CTA that is not already
+// satisfied then gives up too, so every role leaves its loop in bounded time.  The limit is
+// kWaitCycles, or with kRuntimeLimit the CTA's limit_kcycles (the instantiation tests use to
+// make waits run out; kept apart because the production kernels run at their register
+// ceiling, where even this one comparison changes their code).
+template <bool kCluster, bool kRuntimeLimit = false>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile WaitCtl* w) {
+  const long long t0 = clock64();
+  while (true) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (w->abort) return false;
+    const bool out = kRuntimeLimit ? ((clock64() - t0) >> 10) >= w->limit_kcycles : clock64() - t0 > kWaitCycles;
+    if (out) {
+      w->abort = 1;
+      return false;
+    }
+  }
+}
+
+// After an abort: wait (up to kDrainCycles each) for the last min(issued, stages) loads of a
+// ring whose load i completes phase i / stages of full[i % stages].
+__device__ __forceinline__ void drain_ring(const uint64_t* full, int stages, int issued) {
+  for (int i = issued > stages ? issued - stages : 0; i < issued; ++i) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(smem_u32(&full[i % stages]), (uint32_t)((i / stages) & 1)) &&
+           clock64() - t0 < kDrainCycles) {
+    }
+  }
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");

@@ -378,6 +378,25 @@ int dcpmla_decode_noalloc(const void* d_q, void* const* pools, float* const* sca
                           float* d_lse_part, int32_t* d_err, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Testing only: the limit of the tensor-core decode kernels' pipeline waits.
+ * The pages have no counterpart to this call.
+ *
+ * Every wait inside the tensor-core decode kernels (a TMA tile landing, an MMA
+ * completing, the peer CTA's partial scores arriving) gives up after a limit
+ * of clock64 cycles, about one second by default.  A wait that gives up sets
+ * DCPMLA_DERR_TIMEOUT in *d_err and aborts its CTA: every role leaves its
+ * loop, the copies and MMAs already issued are waited for, TMEM is freed, and
+ * the kernel returns; that call's outputs are invalid (some may be left
+ * unwritten).  This call sets the limit for decode launches enqueued after it,
+ * rounded down to a multiple of 1024 cycles (so cycles < 1024 makes every wait
+ * that is not already satisfied give up at once; cycles <= 0 restores the
+ * default); it exists so that tests can make the
+ * waits run out on purpose and check that the error is reported and the
+ * context stays usable.  Process-wide; not for production use.
+ * ------------------------------------------------------------------------ */
+int dcpmla_testing_set_wait_limit(int64_t cycles);
+
+/* ------------------------------------------------------------------------
  * Exact LSE merge (SGLang DCP docs, MLA decode dataflow): for every row,
  *   lse = log_b sum_r b^{lse_r},   o = sum_r b^{lse_r - lse} * o_r,
  * with b = e or 2 (the decode's LSE base); the maximum is factored out so no

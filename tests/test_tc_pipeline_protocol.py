@@ -15,6 +15,11 @@ protocol is checked here, on the CPU, before any change to it runs:
 Shares are cut from item tile counts the way the kernel cuts them (contiguous balanced shares of
 the tile sequence, units of 1 tile upwards, runs of items with the same query rows), and two
 planted mistakes must be caught.
+
+A second, finer model (run_pair_abort: softmax warps one by one, transaction bytes per copy, the
+teardown) covers aborts: any wait may run out its limit, and the copies and MMAs left in flight
+must all be waited for before TMEM is freed and the CTA exits; the earlier teardown, which
+missed some of them, must be caught.
 """
 import random
 
@@ -242,4 +247,354 @@ def test_model_catches_unordered_same_q_arrivals():
 
 def test_model_catches_buffers_released_during_staging():
     caught = sum(bool(run_pair(units, seed, hold_buffers=False)[1]) for units, seed in _random_layouts(300, 9))
+    assert caught > 0
+
+
+# ---------------------------------------------------------------------------------------------
+# Aborts.  Every wait of the kernel gives up after a limit (the kernel parameter wait_cycles):
+# the waiting thread sets the CTA's abort flag and leaves its loop, and every other wait of that
+# CTA then returns at once unless its phase has already completed.  The peer CTA learns nothing
+# of it: its own waits on the aborted CTA run out in turn.  The model below follows the kernel's
+# code paths after a failed wait (which arrivals still happen, which copies and MMAs are left in
+# flight) down to the teardown, and checks that
+#   * no MMA is in flight when TMEM is freed,
+#   * no TMA copy lands in a CTA after it has exited (st.async writes into the peer are ordered
+#     before the issuing CTA's release arrival at the final cluster barrier),
+#   * no barrier receives more arrivals than a phase holds.
+# Drain waits (the ones that let copies and MMAs already issued finish) have a limit far above
+# any copy's or MMA's latency: in the model they give up only when nothing is left in flight.
+# ---------------------------------------------------------------------------------------------
+class W:
+    """A wait: bounded (gives up at the kernel's limit), a drain (gives up only when nothing is
+    in flight), or hard (the cluster barrier: never gives up)."""
+
+    def __init__(self, bar, parity, drain=False, hard=False):
+        self.bar, self.parity, self.drain, self.hard = bar, parity, drain, hard
+
+    def done(self):
+        return self.bar.done(self.parity)
+
+
+class Flag:
+    """A barrier stand-in whose wait completes once `value` is set."""
+
+    def __init__(self, value=False):
+        self.value = value
+
+    def done(self, parity):
+        return self.value
+
+
+def run_pair_abort(units, seed, abort_after=(None, None), teardown_drain=True):
+    """Both CTAs over one share; CTA c's waits may start to run out after abort_after[c] steps
+    (None: never).  teardown_drain=True is the kernel's teardown (copies drained after every
+    role has finished); False is the earlier one, where a role drained only the copies it saw
+    in flight when it left its loop."""
+    rng = random.Random(seed)
+    C = []
+    for c in range(2):
+        B = {}
+        for s in range(3):
+            for name, cnt in (("kv_full", 1), ("kv_empty", 1), ("s_full", 1), ("p_full", 128)):
+                B[f"{name}{s}"] = Bar(f"c{c}.{name}{s}", cnt)
+        for s in range(2):
+            for name, cnt in (("o_par", 1), ("mref", 128), ("x_full", 1), ("x_empty", 1), ("x_read", 128)):
+                B[f"{name}{s}"] = Bar(f"c{c}.{name}{s}", cnt)
+        for name, cnt in (("q_full", 129), ("o_full", 1), ("o_free", 256), ("l", 256), ("stg", 256),
+                          ("drain_qk", 1), ("drain_pv", 1)):
+            B[name] = Bar(f"c{c}.{name}", cnt)
+        C.append(B)
+    landing = []                       # (source CTA, target CTA, kind, apply)
+    mma = [[], []]                     # (issuer, barrier) commits in issue order
+    abort = [False, False]
+    issued = [0, 0]                    # stage loads issued
+    q_last = [-1, -1]                  # unit of the last Q copy issued
+    arrived = [False, False]
+    cluster = Flag()
+    errors = []
+    steps = [0]
+
+    def land(src, dst, kind, fn):
+        landing.append((src, dst, kind, fn))
+
+    def issue_q(c, u):
+        C[c]["q_full"].arrive(1, tx=40960)
+        land(c, c, "tma", lambda B=C[c]: B["q_full"].complete_tx(40960))
+        q_last[c] = max(q_last[c], u)
+
+    def producer(c):
+        B, gi, ok = C[c], 0, True
+        for n, _ in units:
+            if not ok:
+                break
+            for _ in range(n):
+                st = gi % 3
+                if gi >= 3:
+                    if not (yield W(B[f"kv_empty{st}"], ((gi // 3) - 1) & 1)):
+                        ok = False
+                        break
+                B[f"kv_full{st}"].arrive(1, tx=1)
+                land(c, c, "tma", lambda b=B[f"kv_full{st}"]: b.complete_tx(1))
+                issued[c] = gi + 1
+                gi += 1
+        if not teardown_drain and abort[c]:
+            for i in range(max(0, issued[c] - 3), issued[c]):
+                yield W(B[f"kv_full{i % 3}"], (i // 3) & 1, drain=True)
+
+    def qk_issuer(c):
+        B, gi, ok = C[c], 0, True
+        for ui, (n, _) in enumerate(units):
+            if not ok or not (yield W(B["q_full"], ui & 1)):
+                break
+            for _ in range(n):
+                st = gi % 3
+                if not (yield W(B[f"kv_full{st}"], (gi // 3) & 1)):
+                    ok = False
+                    break
+                mma[c].append(("qk", f"s_full{st}"))
+                gi += 1
+        mma[c].append(("qk", "drain_qk"))
+        yield W(B["drain_qk"], 0, drain=True)
+
+    def pv_issuer(c):
+        B, gi, ok = C[c], 0, True
+        for ui, (n, _) in enumerate(units):
+            if not ok:
+                break
+            for i in range(n):
+                st = gi % 3
+                good = yield W(B[f"p_full{st}"], (gi // 3) & 1)
+                if good and i == 0 and ui > 0:
+                    good = yield W(B["o_free"], (ui - 1) & 1)
+                if not good:
+                    ok = False
+                    break
+                mma[c] += [("pv", f"kv_empty{st}"), ("pv", f"o_par{gi & 1}")]
+                if i == n - 1:
+                    mma[c].append(("pv", "o_full"))
+                gi += 1
+        mma[c].append(("pv", "drain_pv"))
+        yield W(B["drain_pv"], 0, drain=True)
+
+    def relay(c):
+        B, P = C[c], C[1 - c]
+        P["x_empty0"].arrive(1)
+        okr = True
+        if units[0][0] == 1:
+            okr = yield W(B["stg"], 0)
+        if okr:
+            P["x_empty1"].arrive(1)
+        gi = 0
+        for ui, (n, _) in enumerate(units):
+            if not okr:
+                break
+            n_next = units[ui + 1][0] if ui + 1 < len(units) else 0
+            for i in range(n):
+                if not (yield W(B[f"x_read{gi & 1}"], (gi >> 1) & 1)):
+                    okr = False
+                    break
+                hold = ui + 1 if (i == n - 1 and n_next == 1) else (ui if i >= n - 2 else -1)
+                if hold >= 0 and not (yield W(B["stg"], hold & 1)):
+                    okr = False
+                    break
+                P[f"x_empty{gi & 1}"].arrive(1)
+                gi += 1
+
+    def softmax_warp(c, w):
+        # warps 2..9: warpgroup g = (w - 2) >> 2; row 0 (which arms x_full) in warp 4 + 4g;
+        # the Q copies are issued by warp 2 + 4g; every thread arrives, 32 per warp
+        B = C[c]
+        g = (w - 2) >> 2
+        row0 = w == 4 + 4 * g
+        tma_thread = w == 2 + 4 * g
+        gi, ok, my_q = 0, True, -1
+        for ui, (n, q) in enumerate(units):
+            if not ok:
+                break
+            if ui == 0 and g == 0:
+                if tma_thread:
+                    issue_q(c, 0)
+                    my_q = 0
+                B["q_full"].arrive(32)
+            gs = gi
+            i = (g - gs) & 1
+            while ok and i < n:
+                gt = gs + i
+                st = gt % 3
+                ok = yield W(B[f"s_full{st}"], (gt // 3) & 1)
+                if ok:
+                    ok = yield W(B[f"x_empty{g}"], (gt >> 1) & 1)
+                if not ok:
+                    break
+                land(c, 1 - c, "st.async", lambda P=C[1 - c], g=g: P[f"x_full{g}"].complete_tx(8192))
+                if row0:
+                    B[f"x_full{g}"].arrive(1, tx=32768)
+                ok = yield W(B[f"x_full{g}"], (gt >> 1) & 1)
+                if not ok:
+                    break
+                B[f"x_read{g}"].arrive(32)
+                if i >= 1:
+                    ok = yield W(B[f"mref{g ^ 1}"], ((gt - 1) >> 1) & 1)
+                    if not ok:
+                        break
+                    if rng.random() < 0.3:     # a row of this warp moved the reference: rescale O
+                        ok = yield W(B[f"o_par{(gt - 1) & 1}"], ((gt - 1) >> 1) & 1)
+                        if not ok:
+                            break
+                B[f"mref{g}"].arrive(32)
+                B[f"p_full{st}"].arrive(32)
+                i += 2
+            gi = gs + n
+            if ok and ((gi - 1) & 1) != g and ui + 1 < len(units):
+                gl = gi - 1
+                ok = yield W(B[f"s_full{gl % 3}"], (gl // 3) & 1)
+                if ok:
+                    if units[ui + 1][1] == q:
+                        B["q_full"].arrive(32)
+                        if tma_thread:
+                            B["q_full"].arrive(1)
+                    else:
+                        if tma_thread:
+                            issue_q(c, ui + 1)
+                            my_q = ui + 1
+                        B["q_full"].arrive(32)
+            # the unit's epilogue (also after a failed wait: its output is written empty)
+            if ok:
+                ok = yield W(B["o_full"], ui & 1)
+            B["l"].arrive(32)
+            okl = yield W(B["l"], ui & 1)
+            ok = okl and ok
+            yield W(Flag(True), 0)             # O is staged through exchange buffer g
+            B["o_free"].arrive(32)
+            B["stg"].arrive(32)
+        if not teardown_drain and my_q >= 0 and abort[c]:
+            yield W(B["q_full"], my_q & 1, drain=True)
+
+    def teardown(c):
+        B = C[c]
+        if teardown_drain and abort[c]:
+            for i in range(max(0, issued[c] - 3), issued[c]):
+                yield W(B[f"kv_full{i % 3}"], (i // 3) & 1, drain=True)
+            if q_last[c] >= 0:
+                yield W(B["q_full"], q_last[c] & 1, drain=True)
+        if mma[c]:
+            errors.append(f"c{c}: TMEM freed with {len(mma[c])} MMA commit(s) in flight")
+        # release arrival at the cluster barrier: this CTA's st.async writes are performed first
+        for x in [x for x in landing if x[0] == c and x[2] == "st.async"]:
+            landing.remove(x)
+            x[3]()
+        arrived[c] = True
+        if all(arrived):
+            cluster.value = True
+        yield W(cluster, 0, hard=True)
+        if any(x[1] == c for x in landing):
+            errors.append(f"c{c}: a copy lands after the CTA exited: "
+                          + ", ".join(f"{x[2]} from c{x[0]}" for x in landing if x[1] == c))
+
+    roles = {}
+    for c in range(2):
+        roles.update({f"c{c}.producer": producer(c), f"c{c}.qk": qk_issuer(c), f"c{c}.pv": pv_issuer(c),
+                      f"c{c}.relay": relay(c)})
+        for w in range(2, 10):
+            roles[f"c{c}.sm{w}"] = softmax_warp(c, w)
+    pending = {}
+    try:
+        for k, r in roles.items():
+            pending[k] = next(r, None)
+        started = [False, False]
+        while True:
+            steps[0] += 1
+            for c in range(2):
+                if not started[c] and all(pending[k] is None for k in roles if k.startswith(f"c{c}.")):
+                    started[c] = True
+                    roles[f"c{c}.teardown"] = teardown(c)
+                    pending[f"c{c}.teardown"] = next(roles[f"c{c}.teardown"], None)
+            moves = []
+            for k, wt in pending.items():
+                if wt is None:
+                    continue
+                c = int(k[1])
+                if wt.done():
+                    moves.append(("go", k, True))
+                elif wt.hard:
+                    pass
+                elif wt.drain:
+                    if not landing and not mma[c]:
+                        moves.append(("go", k, False))            # nothing left to wait for
+                elif abort[c]:
+                    moves.append(("go", k, False))
+                elif abort_after[c] is not None and steps[0] >= abort_after[c]:
+                    moves.append(("timeout", k, False))
+            if landing:
+                moves.append(("land", None, None))
+            for c in range(2):
+                if mma[c]:
+                    moves.append(("mma", c, None))
+            if not moves:
+                # nothing can move: every wait still blocked runs out its limit in the end
+                moves = [("timeout", k, False) for k, wt in pending.items()
+                         if wt is not None and not wt.drain and not wt.hard]
+            if not moves:
+                break
+            kind, k, val = rng.choice(moves)
+            if kind in ("go", "timeout"):
+                if kind == "timeout":
+                    abort[int(k[1])] = True
+                try:
+                    pending[k] = roles[k].send(val)
+                except StopIteration:
+                    pending[k] = None
+            elif kind == "land":
+                x = landing.pop(rng.randrange(len(landing)))
+                x[3]()
+            else:
+                C[k][mma[k].pop(0)[1]].arrive(1)
+    except AssertionError as e:
+        errors.append(str(e))
+    stuck = sorted(k for k in pending if pending[k] is not None)
+    return stuck, errors, abort
+
+
+def _abort_cases(n, seed):
+    rng = random.Random(seed)
+    for units, s in _random_layouts(n, seed):
+        total = sum(t for t, _ in units)
+        # when each CTA's waits may start to run out: early, mid-share or never
+        pick = lambda: rng.choice([None, rng.randint(0, 40 * total + 40)])
+        yield units, s, (pick(), pick())
+
+
+def test_aborts_at_any_wait_drain_everything():
+    n_abort = 0
+    for units, seed, after in _abort_cases(400, 11):
+        stuck, errors, aborted = run_pair_abort(units, seed, after)
+        assert not stuck and not errors, (units, seed, after, stuck, errors[:2])
+        n_abort += any(aborted)
+    assert n_abort > 200          # most cases do abort somewhere
+
+
+def test_aborts_with_an_immediate_limit_drain_everything():
+    # a wait limit of zero: every wait that is not already satisfied gives up at once
+    layouts = list(_random_layouts(200, 12)) + [(u, s) for u in ([(1, 0)], [(2, 0)], [(3, 0)], [(2, 0), (1, 1)])
+                                                for s in range(50)]
+    for units, seed in layouts:
+        stuck, errors, aborted = run_pair_abort(units, seed, (0, 0))
+        assert not stuck and not errors, (units, seed, stuck, errors[:2])
+        assert all(aborted)
+
+
+def test_abort_model_without_aborts_matches_the_protocol():
+    for units, seed in _random_layouts(200, 13):
+        stuck, errors, aborted = run_pair_abort(units, seed)
+        assert not stuck and not errors and not any(aborted), (units, seed, stuck, errors[:2])
+
+
+def test_abort_model_catches_copies_drained_only_by_their_role():
+    # the earlier teardown: a producer that had issued a short share's loads and left its loop
+    # before another role aborted did not wait for them, and they could land after the CTA exited
+    caught = 0
+    for units in ([(2, 0)], [(3, 0)], [(2, 0), (1, 1)]):
+        for seed in range(100):
+            stuck, errors, _ = run_pair_abort(units, seed, (0, 0), teardown_drain=False)
+            caught += bool(errors)
     assert caught > 0
