@@ -598,3 +598,134 @@ def test_abort_model_catches_copies_drained_only_by_their_role():
             stuck, errors, _ = run_pair_abort(units, seed, (0, 0), teardown_drain=False)
             caught += bool(errors)
     assert caught > 0
+
+
+# ---------------------------------------------------------------------------------------------
+# One exchange buffer for both softmax warpgroups.  The non-persistent 128-row kernel had a
+# four-stage variant (measured, not kept) in which the two warpgroups, taking alternate tiles,
+# shared one exchange buffer; it faulted the GPU twice and its source was not kept.  This
+# model rebuilds its exchange protocol from that description (one item per CTA pair: one unit
+# of n tiles, tiles alternating between the warpgroups, the peer's partial of tile t in the
+# single buffer, tile t + 1 sent once tile t has been read) and checks the buffer's contents
+# at every read.  With one set of exchange barriers for both warpgroups, the two warpgroups'
+# row-0 threads arm the same x_full phase (an over-arrival), parity waits alias across tiles,
+# and roles hang: on the GPU a hang ran into the bounded waits, whose abort path then let
+# loads still in flight land after the CTA exited (the teardown gap the abort model above
+# catches).  With the barriers indexed by tile parity (each warpgroup arms and waits only its
+# own) every read sees its own tile's partial.  The kept kernels give each warpgroup its own
+# buffer and barriers (run_pair above).
+# ---------------------------------------------------------------------------------------------
+def run_pair_one_buffer(n, seed, stages=4, per_parity_barriers=True):
+    rng = random.Random(seed)
+    C = []
+    for c in range(2):
+        B = {}
+        for s in range(stages):
+            for name, cnt in (("kv_full", 1), ("kv_empty", 1), ("s_full", 1), ("p_full", 128)):
+                B[f"{name}{s}"] = Bar(f"c{c}.{name}{s}", cnt)
+        for s in range(2):
+            for name, cnt in (("mref", 128), ("x_full", 1), ("x_empty", 1), ("x_read", 128)):
+                B[f"{name}{s}"] = Bar(f"c{c}.{name}{s}", cnt)
+        C.append(B)
+    landing, mma, errors = [], [[], []], []
+    buf = [None, None]                 # the tile whose partial CTA c's buffer holds
+    writing = [None, None]             # a partial landing in CTA c's buffer
+
+    def xb(t):                         # exchange barrier index of tile t
+        return t & 1 if per_parity_barriers else 0
+
+    def xpar(t):                       # parity of tile t's phase on its exchange barrier
+        return (t >> 1) & 1 if per_parity_barriers else t & 1
+
+    def wait(c, name, parity):
+        bar = C[c][name]
+        return lambda: bar.done(parity)
+
+    def producer(c):
+        for t in range(n):
+            if t >= stages:
+                yield wait(c, f"kv_empty{t % stages}", ((t // stages) - 1) & 1)
+            landing.append(lambda c=c, s=t % stages: C[c][f"kv_full{s}"].arrive(1))
+
+    def qk_issuer(c):
+        for t in range(n):
+            yield wait(c, f"kv_full{t % stages}", (t // stages) & 1)
+            mma[c].append(f"s_full{t % stages}")
+
+    def pv_issuer(c):
+        for t in range(n):
+            yield wait(c, f"p_full{t % stages}", (t // stages) & 1)
+            mma[c].append(f"kv_empty{t % stages}")
+
+    def relay(c):
+        # the buffer starts empty (tile 0 may be sent); once tile t's partial has been read,
+        # tile t + 1 may be sent (on the barrier of t + 1's parity)
+        C[1 - c]["x_empty0"].arrive(1)
+        for t in range(n):
+            yield wait(c, f"x_read{xb(t)}", xpar(t))
+            C[1 - c][f"x_empty{xb(t + 1)}"].arrive(1)
+
+    def softmax(c, g):
+        B, P = C[c], C[1 - c]
+        for t in range(g, n, 2):
+            yield wait(c, f"s_full{t % stages}", (t // stages) & 1)
+            yield wait(c, f"x_empty{xb(t)}", xpar(t))
+
+            def land_partial(c=c, t=t):
+                if writing[1 - c] is not None and writing[1 - c] != t:
+                    errors.append(f"c{1 - c}: partials of tiles {writing[1 - c]} and {t} in the buffer at once")
+                buf[1 - c] = t
+                writing[1 - c] = None
+                C[1 - c][f"x_full{xb(t)}"].complete_tx(32768)
+
+            writing[1 - c] = t if writing[1 - c] is None else writing[1 - c]
+            landing.append(land_partial)
+            B[f"x_full{xb(t)}"].arrive(1, tx=32768)
+            yield wait(c, f"x_full{xb(t)}", xpar(t))
+            if buf[c] != t:
+                errors.append(f"c{c} tile {t}: read the partial of tile {buf[c]}")
+            B[f"x_read{xb(t)}"].arrive(128)
+            if t >= 1:
+                yield wait(c, f"mref{g ^ 1}", ((t - 1) >> 1) & 1)
+            B[f"mref{g}"].arrive(128)
+            B[f"p_full{t % stages}"].arrive(128)
+
+    roles = {}
+    for c in range(2):
+        roles.update({f"c{c}.producer": producer(c), f"c{c}.qk": qk_issuer(c), f"c{c}.pv": pv_issuer(c),
+                      f"c{c}.relay": relay(c), f"c{c}.wg0": softmax(c, 0), f"c{c}.wg1": softmax(c, 1)})
+    try:
+        pending = {k: next(r, None) for k, r in roles.items()}
+        while True:
+            moves = [("role", k) for k in roles if pending[k] is not None and pending[k]()]
+            moves += [("land", None)] if landing else []
+            moves += [("mma", c) for c in range(2) if mma[c]]
+            if not moves:
+                break
+            kind, k = rng.choice(moves)
+            if kind == "role":
+                pending[k] = next(roles[k], None)
+            elif kind == "land":
+                landing.pop(rng.randrange(len(landing)))()
+            else:
+                C[k][mma[k].pop(0)].arrive(1)
+    except AssertionError as e:
+        errors.append(str(e))
+    stuck = sorted(k for k in pending if pending[k] is not None)
+    return stuck, errors
+
+
+def test_one_buffer_with_barriers_per_tile_parity_runs_clean():
+    for n in (1, 2, 3, 5, 8, 13):
+        for seed in range(60):
+            stuck, errors = run_pair_one_buffer(n, seed, per_parity_barriers=True)
+            assert not stuck and not errors, (n, seed, stuck, errors[:2])
+
+
+def test_one_buffer_with_one_barrier_set_is_caught():
+    caught = 0
+    for n in (2, 3, 5, 8):
+        for seed in range(60):
+            stuck, errors = run_pair_one_buffer(n, seed, per_parity_barriers=False)
+            caught += bool(stuck or errors)
+    assert caught > 100
