@@ -31,6 +31,7 @@
 //                  O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
 //     warps 2-9  softmax, two warpgroups on every tile, each 32 of its columns
 //     warps 10-13  E4M3 -> fp16 conversion into the stage ring (one per SM sub-partition)
+//     warp 14    relays "exchange buffer read" to the peer
 //   TMEM columns: O_h [0,256), S/P double buffer [256,384), Q_h latent [384,512).
 //
 // Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all
@@ -1566,6 +1567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(b16::kThreads, 1)
 //                 O_h += P V_h     (M 128, N 256, K 64; P from TMEM, V MN-major)
 //   warps 2-9   softmax, both warpgroups on every tile, each 32 of its columns
 //   warps 10-13 convert raw tiles into the 3-deep fp16 stage ring (one per SM sub-partition)
+//   warp 14     relays "exchange buffer read" to the peer
 //
 // TMEM columns: O_h [0,256), S/P slots [256,384) (slot = tile % 2, P overwrites S
 // in place; in issue order QK(i + 2) follows PV(i)), Q_h latent [384,512).
@@ -1578,7 +1580,7 @@ constexpr int kRawChunk = kTileTok * 64;            // 64 tokens x 64 codes
 constexpr int kRawScaleOff = 5 * kRawChunk;         // then the tile's 64 fp32 scales
 constexpr int kRawStage = kRawScaleOff + kTileTok * 4;
 constexpr int kQRope = kRows * 128;                 // CTA 1: 64 rope dims of Q, fp16
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;                       // 15 warps (roles in decode_tc_e4m3_body)
 constexpr int kConvThreads = 128;
 constexpr size_t kSmemBytes = 1024 + kQRope + kStages * kStage + kXBytes + kRawStages * kRawStage;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
@@ -1770,10 +1772,12 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
       while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
-    if (lane == 1) {
+  } else if (warp == 14) {
+    if (lane == 0) {
       // relay: once all softmax threads have read the peer's partial for a tile,
       // tell the peer its next partial may overwrite our exchange buffer.  This
-      // thread has no stores in flight, so its cluster-scope release is cheap.
+      // thread has no stores in flight, so its cluster-scope release is cheap; it has
+      // a warp of its own (as a lane of the MMA warp it waited behind the issuer).
       for (int i = 0; i < ntiles; ++i) {
         if (!wait_bar<false, kRL>(smem_u32(&bar_x_read), i & 1, abort_flag)) break;
         mbar_arrive_remote(map_to_rank(smem_u32(&bar_x_empty), peer));
