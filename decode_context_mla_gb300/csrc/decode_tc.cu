@@ -1582,7 +1582,8 @@ constexpr int kRawStage = kRawScaleOff + kTileTok * 4;
 constexpr int kQRope = kRows * 128;                 // CTA 1: 64 rope dims of Q, fp16
 constexpr int kThreads = 480;                       // 15 warps (roles in decode_tc_e4m3_body)
 constexpr int kConvThreads = 128;
-constexpr size_t kSmemBytes = 1024 + kQRope + kStages * kStage + kXBytes + kRawStages * kRawStage;
+constexpr int kXBytesE4 = kRows * kTileTok * 2;     // the peer's partial score tile, fp16
+constexpr size_t kSmemBytes = 1024 + kQRope + kStages * kStage + kXBytesE4 + kRawStages * kRawStage;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 static_assert(kSmemBytes <= 227 * 1024 - 6144, "stages, Q and exchange buffer exceed shared memory");
 }  // namespace e4
@@ -1597,7 +1598,7 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
   uint8_t* sQr = smem;                                   // rope part of Q (CTA 1)
   uint8_t* sKV = smem + kQRope;                          // kStages x kStage (fp16)
   uint8_t* sX = sKV + kStages * kStage;                  // the peer's partial scores of one tile
-  uint8_t* sRaw = sX + kXBytes;                          // kRawStages x kRawStage
+  uint8_t* sRaw = sX + kXBytesE4;                        // kRawStages x kRawStage
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ uint64_t bar_raw_full[kRawStages], bar_raw_empty[kRawStages];
   __shared__ uint64_t bar_s_full[2], bar_p_full[2], bar_max[2];
@@ -1909,31 +1910,44 @@ __device__ __forceinline__ void decode_tc_e4m3_body(const TcParams& p) {
         tmem_ld16(tmem + lane_off + kColS + sb * kTileTok + 32 * g + 16,
                   *reinterpret_cast<uint32_t(*)[16]>(&own[16]));
         tmem_ld_wait();
-        // send this CTA's partial into the peer's buffer ([16 col groups][128 rows] of
-        // float4), once the peer has read the previous one
+        // Send this CTA's partial to the peer as fp16 of 2^-10 times its value, clamped to the
+        // fp16 range ([8 column groups][128 rows] of 8 halves), once the peer has read the
+        // previous one.  Both CTAs add the same two rounded parts, so their scores stay
+        // bit-identical; the rounding (2^-11 relative) keeps the output within ~2e-3 of the
+        // exact sum on N(0,1) data, and 2^-10 keeps partials of queries up to |q| ~ 400 in range.
+        uint32_t ownb[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float lo = fminf(fmaxf(__uint_as_float(own[2 * k]) * 0.0009765625f, -65504.f), 65504.f);
+          const float hi = fminf(fmaxf(__uint_as_float(own[2 * k + 1]) * 0.0009765625f, -65504.f), 65504.f);
+          ownb[k] = pack_f16(lo, hi);
+        }
         if (i >= 1) {
           ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (i - 1) & 1, abort_flag));
           if (!ok) break;
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_remote + ((8 * g + c) * kRows + row) * 16,
-                      make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]), xfull_remote);
-        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
+        for (int c = 0; c < 4; ++c)
+          st_async_v4(x_remote + ((4 * g + c) * kRows + row) * 16,
+                      make_uint4(ownb[4 * c], ownb[4 * c + 1], ownb[4 * c + 2], ownb[4 * c + 3]), xfull_remote);
+        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytesE4);
         ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), i & 1, abort_flag));
         if (!ok) break;
         float x[32];
-        const float4* xin = reinterpret_cast<const float4*>(sX);
+        const uint4* xin = reinterpret_cast<const uint4*>(sX);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 pv = xin[(8 * g + c) * kRows + row];
-          const float o0 = __uint_as_float(own[4 * c]), o1 = __uint_as_float(own[4 * c + 1]);
-          const float o2 = __uint_as_float(own[4 * c + 2]), o3 = __uint_as_float(own[4 * c + 3]);
-          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
-          x[4 * c + 0] = h ? pv.x + o0 : o0 + pv.x;
-          x[4 * c + 1] = h ? pv.y + o1 : o1 + pv.y;
-          x[4 * c + 2] = h ? pv.z + o2 : o2 + pv.z;
-          x[4 * c + 3] = h ? pv.w + o3 : o3 + pv.w;
+        for (int c = 0; c < 4; ++c) {
+          const uint4 pv = xin[(4 * g + c) * kRows + row];
+          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t ow = ownb[4 * c + q];
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pw[q]));
+            const float2 of = __half22float2(*reinterpret_cast<const __half2*>(&ow));
+            // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs, then scaled back
+            x[8 * c + 2 * q] = (h ? pf.x + of.x : of.x + pf.x) * 1024.f;
+            x[8 * c + 2 * q + 1] = (h ? pf.y + of.y : of.y + pf.y) * 1024.f;
+          }
         }
         mbar_arrive(smem_u32(&bar_x_read));
         // the key's per-token scale multiplies its score
