@@ -417,7 +417,7 @@ def measure_step(args, w: W.Workload, ws: int, local: int, with_e2e: bool) -> di
     # slot map + append (when the step appends), the decode's kernels, the merge
     # (fused: the decode's own merge kernel replaces the split merge and the LSE merge)
     launches_per_step = (2 if step.do_append else 0) + (dec_launches if not args.fused else
-                                                         (2 if path == 1 else 1 if path == 2 else 2))
+                                                         (dec_launches if path == 2 else 2))
     if not args.fused:
         launches_per_step += 1
     res = dict(acc=acc, lens=lens, ms_step=ms_step, ms_dec=ms_dec, roofline=roofline,

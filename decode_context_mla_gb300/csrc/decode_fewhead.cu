@@ -858,57 +858,104 @@ __global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, con
   if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
 }
 
-// Fused decode + merge: one block per (request, query row, quarter of the value dims)
-// merges the partials of every unit of every shard of the request (SGLang DCP docs,
-// MLA decode dataflow: the exact LSE merge; the partials of a split shard merge the
-// same way), in base 2, into o [B, R, 512] and lse [B, R] (base converted at the end).
-// A shard any unit of which needed a bad page is left out, as the unfused path writes
-// it as empty (lse = -inf).
-__global__ void __launch_bounds__(32) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre, int G,
-                                                          const float* __restrict__ ws_o,
-                                                          const float* __restrict__ ws_lse,
-                                                          const int32_t* __restrict__ ws_bad) {
-  const int b = blockIdx.x, row = blockIdx.y, t = blockIdx.z * 32 + threadIdx.x;
+// Fused decode + merge: block (b, row) merges the partials of every unit of every shard of
+// request b for that query row (SGLang DCP docs, MLA decode dataflow: the exact LSE merge; the
+// partials of a split shard merge the same way), in base 2, into o [B, R, 512] and lse [B, R]
+// (base converted at the end).  Warp 0 gathers the partials, lane l those of shard l (its
+// units' LSEs, then a warp max and sum); the block's 128 threads then form the weighted sums,
+// 4 dims each.  A shard any unit of which needed a bad page is left out, as the unfused path
+// writes it as empty (lse = -inf).
+constexpr int kMergeParts = kMaxFhShards + 88;        // shards + cluster boundaries in a request
+
+__global__ void __launch_bounds__(128) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
+                                                           int G, const float* __restrict__ ws_o,
+                                                           const float* __restrict__ ws_lse,
+                                                           const int32_t* __restrict__ ws_bad) {
+  const int b = blockIdx.x, row = blockIdx.y, t = threadIdx.x, lane = t & 31;
   const int64_t R = a.R;
-  const int nitems = a.B * a.shard_count;
-  const int T = pre[nitems];
-  float m = -INFINITY;
-  for (int pass = 0; pass < 2; ++pass) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float sum = 0.f;
-    for (int sr = 0; sr < a.shard_count; ++sr) {
-      const int item = b * a.shard_count + sr, s0 = pre[item], s1 = pre[item + 1];
-      if (s1 <= s0) continue;
-      const int k0 = fh_cluster_of(T, s0, G), k1 = fh_cluster_of(T, s1 - 1, G);
-      bool bad = false;
-      for (int k = k0; k <= k1; ++k)
-        if (fh_bound(T, k, G) != fh_bound(T, k + 1, G)) bad |= ws_bad[item + k] != 0;
-      if (bad) continue;
-      for (int k = k0; k <= k1; ++k) {
-        if (fh_bound(T, k, G) == fh_bound(T, k + 1, G)) continue;
-        const float lk = ws_lse[(int64_t)(item + k) * R + row];
-        if (pass == 0) {
-          m = fmaxf(m, lk);
-        } else if (m != -INFINITY) {
-          const float w = exp2f(lk - m);
-          sum += w;
-          const float4 v = __ldcs(reinterpret_cast<const float4*>(ws_o + ((int64_t)(item + k) * R + row) * kDL) + t);
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
-        }
+  __shared__ float w_s[kMergeParts];
+  __shared__ int slot_s[kMergeParts];
+  __shared__ int n_s;
+  if (t < 32) {
+    const int T = pre[a.B * a.shard_count];
+    int k0 = 0, k1 = -1;
+    bool use = false;
+    const int item = b * a.shard_count + lane;
+    if (lane < a.shard_count) {
+      const int s0 = pre[item], s1 = pre[item + 1];
+      if (s1 > s0) {
+        k0 = fh_cluster_of(T, s0, G);
+        k1 = fh_cluster_of(T, s1 - 1, G);
+        bool bad = false;
+        for (int k = k0; k <= k1; ++k)
+          if (fh_bound(T, k, G) != fh_bound(T, k + 1, G)) bad |= ws_bad[item + k] != 0;
+        use = !bad;
       }
     }
-    if (pass == 1) {
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
-      const float lse2 = sum > 0.f ? m + log2f(sum) : -INFINITY;
-      const int64_t orow = (int64_t)b * R + row;
-      reinterpret_cast<float4*>(a.o_part + orow * kDL)[t] =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      if (t == 0) a.lse_part[orow] = a.base2 ? lse2 : lse2 * kLn2;
+    auto live = [&](int k) { return fh_bound(T, k, G) != fh_bound(T, k + 1, G); };
+    int cnt = 0;
+    float m = -INFINITY;
+    if (use)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) {
+          m = fmaxf(m, ws_lse[(int64_t)(item + k) * R + row]);
+          ++cnt;
+        }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    float sum = 0.f;
+    if (use && m != -INFINITY)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) sum += exp2f(ws_lse[(int64_t)(item + k) * R + row] - m);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    const float lse2 = sum > 0.f ? m + log2f(sum) : -INFINITY;
+    int off = cnt;                                        // exclusive scan of the counts
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, off, d);
+      if (lane >= d) off += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, off, 31);
+    off -= cnt;
+    if (use)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) {
+          w_s[off] = lse2 == -INFINITY ? 0.f : exp2f(ws_lse[(int64_t)(item + k) * R + row] - lse2);
+          slot_s[off++] = item + k;
+        }
+    if (lane == 0) {
+      n_s = total;
+      a.lse_part[(int64_t)b * R + row] = a.base2 ? lse2 : lse2 * kLn2;
     }
   }
+  __syncthreads();
+  const int n = n_s;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int j = 0;
+  for (; j + 4 <= n; j += 4) {                            // four independent loads in flight
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = __ldcs(reinterpret_cast<const float4*>(ws_o + ((int64_t)slot_s[j + u] * R + row) * kDL) + t);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = w_s[j + u];
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
+    }
+  }
+  for (; j < n; ++j) {
+    const float w = w_s[j];
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(ws_o + ((int64_t)slot_s[j] * R + row) * kDL) + t);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  reinterpret_cast<float4*>(a.o_part + ((int64_t)b * R + row) * kDL)[t] = acc;
 }
 
 struct FhPlan {
@@ -989,8 +1036,8 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     rc = launch_status();
   }
   if (rc == DCPMLA_OK && fused) {
-    const dim3 grid((unsigned)a.B, (unsigned)a.R, 4);
-    fh_merge_all_kernel<<<grid, 32, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o, p.ws_lse, p.ws_bad);
+    fh_merge_all_kernel<<<dim3((unsigned)a.B, (unsigned)a.R), 128, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o,
+                                                                           p.ws_lse, p.ws_bad);
     rc = launch_status();
   } else if (rc == DCPMLA_OK) {
     const dim3 grid((unsigned)(a.B * a.shard_count), (unsigned)a.R);

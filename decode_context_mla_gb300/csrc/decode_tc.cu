@@ -880,6 +880,7 @@ __global__ void __launch_bounds__(1024) tc_prefix_kernel(const DecodeArgs a, int
 // each row's merge weights are formed once, then the rows stream through as float4s.
 namespace pp {
 constexpr int kCombineRows = 16;
+constexpr int kMaxMergeParts = 96;                   // partials of one row over all shards (fused)
 }
 __global__ void __launch_bounds__(256) tc_unit_combine_kernel(const TcParams p) {
   const DecodeArgs& a = p.a;
@@ -947,6 +948,120 @@ __global__ void __launch_bounds__(256) tc_unit_combine_kernel(const TcParams p) 
       acc.w = fmaf(w, v.w, acc.w);
     }
     reinterpret_cast<float4*>(a.o_part + (((int64_t)sr * a.B + b) * R + grow) * kDL)[c4] = acc;
+  }
+}
+
+// Fused decode + merge of the persistent grid: one block per (request, 128-row tile, 16 rows)
+// merges every partial of the row over all shards, in one exact LSE merge (SGLang DCP docs,
+// MLA decode dataflow; the partials of a shard cut by share boundaries merge the same way):
+// a whole item's output and LSE (p.a.o_part / p.a.lse_part, base 2 here) or the unit partials
+// of an item cut between clusters (ws_o / ws_lse).  An item that needed a bad page is left out.
+// Writes o [B, R, 512] and lse [B, R] (in the caller's base).
+__global__ void __launch_bounds__(256) tc_merge_all_kernel(const TcParams p, float* __restrict__ o,
+                                                           float* __restrict__ lse, int base2) {
+  const DecodeArgs& a = p.a;
+  const int b = blockIdx.x / p.row_tiles, rt = blockIdx.x % p.row_tiles;
+  const int r0 = blockIdx.y * pp::kCombineRows, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int64_t R = a.R;
+  const int G = p.clusters;
+  __shared__ const float* src_s[pp::kCombineRows][pp::kMaxMergeParts];
+  __shared__ float w_s[pp::kCombineRows][pp::kMaxMergeParts];
+  __shared__ int n_s[pp::kCombineRows];
+  // warp w gathers rows w and w + 8 of the group; lane l the partials of shard l
+  for (int rr = warp; rr < pp::kCombineRows; rr += 8) {
+    const int row = r0 + rr;
+    const int64_t grow = (int64_t)rt * kRows + row;
+    if (grow >= R) {                                       // rows past R pad the tile
+      if (lane == 0) n_s[rr] = 0;
+      continue;
+    }
+    const int T = p.ws_pre[p.items];
+    const int item = (b * p.row_tiles + rt) * a.shard_count + lane;
+    int k0 = 0, k1 = -1;
+    bool whole = false, use = false;
+    if (lane < a.shard_count) {
+      const int s0 = p.ws_pre[item], s1 = p.ws_pre[item + 1];
+      if (s1 > s0) {                                       // else no tiles: an empty shard
+        k0 = pp::cluster_of(T, s0, G);
+        k1 = pp::cluster_of(T, s1 - 1, G);
+        whole = k0 == k1;                                  // written by the decode itself
+        int bad = 0;
+        for (int k = k0; k <= k1 && !whole; ++k)
+          if (pp::bound(T, k, G) != pp::bound(T, k + 1, G)) bad |= p.ws_bad[item + k];
+        use = !bad;
+      }
+    }
+    auto part_lse = [&](int k) -> float {
+      return whole ? a.lse_part[((int64_t)lane * a.B + b) * R + grow] : p.ws_lse[(int64_t)(item + k) * kRows + row];
+    };
+    auto live = [&](int k) { return whole || pp::bound(T, k, G) != pp::bound(T, k + 1, G); };
+    int cnt = 0;
+    float m = -INFINITY;
+    if (use)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) {
+          m = fmaxf(m, part_lse(k));
+          ++cnt;
+        }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    float sum = 0.f;
+    if (use && m != -INFINITY)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) sum += exp2f(part_lse(k) - m);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    const float lse2 = sum > 0.f ? m + log2f(sum) : -INFINITY;
+    int off = cnt;                                         // exclusive scan of the counts
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, off, d);
+      if (lane >= d) off += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, off, 31);
+    off -= cnt;
+    if (use)
+      for (int k = k0; k <= k1; ++k)
+        if (live(k)) {
+          w_s[rr][off] = lse2 == -INFINITY ? 0.f : exp2f(part_lse(k) - lse2);
+          src_s[rr][off++] = whole ? a.o_part + (((int64_t)lane * a.B + b) * R + grow) * kDL
+                                   : p.ws_o + ((int64_t)(item + k) * kRows + row) * kDL;
+        }
+    if (lane == 0) {
+      n_s[rr] = total;
+      lse[(int64_t)b * R + grow] = base2 ? lse2 : lse2 * kLn2;
+    }
+  }
+  __syncthreads();
+  for (int e = t; e < pp::kCombineRows * (kDL / 4); e += 256) {
+    const int rr = e / (kDL / 4), c4 = e % (kDL / 4), row = r0 + rr;
+    const int64_t grow = (int64_t)rt * kRows + row;
+    if (grow >= R) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int n = n_s[rr];
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {                           // four independent loads in flight
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(src_s[rr][j + u]) + c4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = w_s[rr][j + u];
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
+    }
+    for (; j < n; ++j) {
+      const float w = w_s[rr][j];
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src_s[rr][j]) + c4);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(o + ((int64_t)b * R + grow) * kDL)[c4] = acc;
   }
 }
 
@@ -2194,9 +2309,10 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct PpPlan {
   int32_t clusters, items, row_tiles, slots;
   size_t pre_off, bad_off, lse_off, o_off, bytes;
+  size_t op_off, lp_off;              // fused: per-shard outputs [shards, B, R, 512] and LSEs
 };
 
-PpPlan plan_pp(const DecodeArgs& a, int sm_count) {
+PpPlan plan_pp(const DecodeArgs& a, int sm_count, bool fused = false) {
   PpPlan p{};
   p.row_tiles = (a.R + kRows - 1) / kRows;
   p.items = (int32_t)((int64_t)a.B * a.shard_count * p.row_tiles);
@@ -2209,12 +2325,18 @@ PpPlan plan_pp(const DecodeArgs& a, int sm_count) {
   p.lse_off = p.bad_off + align256((size_t)p.slots * 4);
   p.o_off = p.lse_off + align256((size_t)p.slots * kRows * 4);
   p.bytes = p.o_off + (size_t)p.slots * kRows * kDL * 4;
+  if (fused) {
+    const size_t rows = (size_t)a.shard_count * a.B * a.R;
+    p.op_off = align256(p.bytes);
+    p.lp_off = p.op_off + align256(rows * kDL * 4);
+    p.bytes = p.lp_off + rows * 4;
+  }
   return p;
 }
 
 // The persistent grid runs unfused bf16 calls whose tile sequence fits 32-bit indices.
 bool use_pp(const DecodeArgs& a, bool fused) {
-  if (fused || a.fp8) return false;
+  if (a.fp8 || (fused && a.shard_count + kMaxCombineParts > pp::kMaxMergeParts)) return false;
   const int64_t items = (int64_t)a.B * a.shard_count * ((a.R + kRows - 1) / kRows);
   const int64_t tiles_item = ((int64_t)a.max_pages * a.P + kTileTok - 1) / kTileTok;
   return items <= (1 << 24) && items * tiles_item <= INT32_MAX;
@@ -2314,19 +2436,28 @@ int encode_bf16_maps(TcParams& p, const DecodeArgs& a) {
   return rc;
 }
 
-int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st) {
-  const PpPlan plan = plan_pp(a, sm_count);
+// fused: the decode writes every shard's output into the workspace (base-2 LSEs) and one
+// kernel merges all partials of each row into o = a.o_part [B, R, 512], lse = a.lse_part.
+int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
+                        bool fused) {
+  const PpPlan plan = plan_pp(a, sm_count, fused);
   if (ws_bytes < plan.bytes || !ws) return DCPMLA_ERR_CAPACITY;
   static ParamCache<TcParams> cache;
-  const LaunchKey key = launch_key(a, ws, ws_bytes, 1);
+  const LaunchKey key = launch_key(a, ws, ws_bytes, fused ? 7 : 1);
   std::lock_guard<std::mutex> lk(cache.mu);
   bool fresh = false;
   TcParams* tp = cache.get(key, fresh);
   if (!tp) return DCPMLA_ERR_CAPACITY;
   TcParams& p = *tp;
   int rc = DCPMLA_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
   if (fresh) {
     p.a = a;
+    if (fused) {
+      p.a.o_part = reinterpret_cast<float*>(w + plan.op_off);
+      p.a.lse_part = reinterpret_cast<float*>(w + plan.lp_off);
+      p.a.base2 = true;
+    }
     p.box_rows = std::min(a.P, kTileTok);
     p.num_splits = 1;
     p.chunk = 0;
@@ -2334,7 +2465,6 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
     p.fused = 0;
     p.clusters = plan.clusters;
     p.items = plan.items;
-    uint8_t* w = static_cast<uint8_t*>(ws);
     p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
     p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
     p.ws_lse = reinterpret_cast<float*>(w + plan.lse_off);
@@ -2342,7 +2472,7 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
     rc = encode_bf16_maps(p, a);
     if (rc == DCPMLA_OK) rc = encode_rows_576(&p.tm_q, a.q, (uint64_t)a.B * a.R, kRows);
     if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_qr, a.q, (uint64_t)a.B * a.R, kRows);
-    if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_o, a.o_part, (uint64_t)a.R, (uint64_t)a.shard_count * a.B);
+    if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_o, p.a.o_part, (uint64_t)a.R, (uint64_t)a.shard_count * a.B);
     if (rc == DCPMLA_OK) rc = encode_out_f32(&p.tm_ws, p.ws_o, kRows, (uint64_t)plan.slots);
     if (rc != DCPMLA_OK) {
       cache.drop(tp);
@@ -2361,7 +2491,11 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
     kern<<<2 * plan.clusters, b16::kThreads, b16::kSmemBytes, st>>>(p);
     rc = launch_status();
   }
-  if (rc == DCPMLA_OK) {
+  if (rc == DCPMLA_OK && fused) {
+    tc_merge_all_kernel<<<dim3((unsigned)(a.B * plan.row_tiles), kRows / pp::kCombineRows), 256, 0, st>>>(
+        p, a.o_part, a.lse_part, a.base2 ? 1 : 0);
+    rc = launch_status();
+  } else if (rc == DCPMLA_OK) {
     tc_unit_combine_kernel<<<dim3((unsigned)plan.items, kRows / pp::kCombineRows), 256, 0, st>>>(p);
     rc = launch_status();
   }
@@ -2370,7 +2504,7 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
 }  // namespace
 
 size_t tc_workspace_bytes(const DecodeArgs& a, int sm_count, bool fused) {
-  return use_pp(a, fused) ? plan_pp(a, sm_count).bytes : plan_tc(a, sm_count, fused).bytes;
+  return use_pp(a, fused) ? plan_pp(a, sm_count, fused).bytes : plan_tc(a, sm_count, fused).bytes;
 }
 
 int tc_kernel_launches(const DecodeArgs& a, bool fused) { return use_pp(a, fused) ? 3 : 1; }
@@ -2394,7 +2528,7 @@ int launch_tc(TcParams& p, const TcPlan& plan, cudaStream_t st) {
 
 int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_count, cudaStream_t st,
                      bool fused) {
-  if (use_pp(a, fused)) return launch_decode_tc_pp(a, ws, ws_bytes, sm_count, st);
+  if (use_pp(a, fused)) return launch_decode_tc_pp(a, ws, ws_bytes, sm_count, st, fused);
   const TcPlan plan = plan_tc(a, sm_count, fused);
   if (ws_bytes < plan.bytes || (plan.bytes && !ws)) return DCPMLA_ERR_CAPACITY;
   // every refusal comes before the first enqueue: a refused call leaves the workspace alone
