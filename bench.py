@@ -222,7 +222,7 @@ DECODE_SOURCES = ["decode_context_mla_gb300/csrc/decode_fewhead.cu",
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_sample(w: W.Workload, budget_s: float, max_requests: int = 64):
+def oracle_sample(w: W.Workload, budget_s: float, max_requests: int = 256):
     """Time the fp64 oracle (striped decode + merge) on whole requests until the budget is spent."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from oracle_ref import OracleWorkload
