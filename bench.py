@@ -463,7 +463,7 @@ def run_ours(args, w: W.Workload):
         for name in W.WORKLOADS:
             if name == w.name:
                 continue
-            r = measure_step(args, W.WORKLOADS[name], ws, local, with_e2e=False)
+            r = measure_step(args, W.WORKLOADS[name], ws, local, with_e2e=True)
             per_workload[name] = {
                 "value": round(r["value"], 2), "unit": "GB/s", "ms_per_step": round(r["ms_step"], 4),
                 "kernel_ms": r["roofline"]["kernel_ms"],
@@ -474,6 +474,8 @@ def run_ours(args, w: W.Workload):
                 "attended_tokens_per_s": round(sum(r["lens"]) * W.WORKLOADS[name].Tq
                                                / (r["ms_step"] * 1e-3), 1),
                 "clocks": r["clocks"], "gpu_launches": r["launches_per_step"] * args.steps,
+                "e2e": {k: r["e2e"][k] for k in ("value", "unit", "ms_per_step", "h2d_bytes_per_step",
+                                                 "d2h_bytes_per_step")},
             }
 
     if rank == 0:
