@@ -97,6 +97,12 @@ SMALL = {
                                     lse_base="2", seed=31, L=2500),
     "fma_e4m3_p12_tq3": W.Workload("fe12p", B=2, H=32, Tq=3, c=2, P=12, kv_dtype="e4m3",
                                    lse_base="e", seed=32, L=4100),
+    # 128-row persistent grid: 96 real rows in the tile (rows past R pad it), and one request
+    # whose two shard items are each cut into dozens of cluster shares
+    "tc_r96_c3": W.Workload("tcr96", B=3, H=32, Tq=3, c=3, P=64, kv_dtype="bf16", lse_base="e",
+                            seed=33, L=5000),
+    "tc_c2_cut": W.Workload("tccut", B=1, H=128, Tq=1, c=2, P=64, kv_dtype="bf16", lse_base="2",
+                            seed=34, L=60000),
 }
 
 # cases that must run on the CUDA-core decode (asserted by test_decode_path_per_workload)
@@ -302,7 +308,7 @@ def test_decode_path_per_workload():
 
 
 FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
-               "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5",
+               "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5", "tc_r96_c3", "tc_c2_cut",
                "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
                "ilv2_c16", "tc_p8_c3", "tc_p256_tq4"]
 
