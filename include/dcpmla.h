@@ -215,9 +215,10 @@ int dcpmla_kv_append(void* const* pools, float* const* scale_pools, int32_t kv_d
  * 2e-3 (max over rows of |err|_inf / |o|_inf) of the exact result on N(0,1)
  * data.  E4M3 KV on the tensor cores: codes convert exactly to fp16, the query
  * is rounded to fp16, P to fp16 (pre-multiplied by the value scale), and the
- * two halves of the 576-d score are added after one of them is rounded to fp16
- * at 2^-10 scale (partials beyond ~6.7e7 code units saturate): within 1e-2 of
- * the result on the dequantised keys (~2e-3 on N(0,1) data).
+ * two partial sums that make up the 576-d score (CTA pair halves) are each
+ * rounded to fp16 at 2^-10 scale before they are added (partials beyond ~6.7e7
+ * code units saturate): within 1e-2 of the result on the dequantised keys
+ * (~2e-3 on N(0,1) data).
  * ------------------------------------------------------------------------ */
 int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools,
                   int32_t kv_dtype, int64_t pool_rows, const int32_t* d_page_table,
