@@ -177,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float lsum_s[2][2][4][8];   // [unit parity][warpgroup][quarter][row]
   __shared__ int seg_s[kThreads];
   __shared__ uint32_t tmem_base_s;
-  __shared__ int ubad_s[2], issued_s, q_issued_s;
+  __shared__ int ubad_s[2][2], issued_s, q_issued_s;
   __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -212,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     wctl_s.limit_kcycles = p.wait_kcycles;
     issued_s = 0;
     q_issued_s = 0;
-    ubad_s[0] = ubad_s[1] = 0;
+    ubad_s[0][0] = ubad_s[0][1] = ubad_s[1][0] = ubad_s[1][1] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -602,6 +602,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool over = false;
 #pragma unroll
         for (int n = 0; n < 8; ++n) over |= s[n] > m_ref[n] + 8.f;
+        // A warp leaves its loops at a failed wait, whose phase was still open after the CTA's
+        // abort flag had been set.  A named barrier has no time limit, so a warp that passed
+        // the same waits (the warpgroup's warps wait for the same phases) reads the flag
+        // before each named barrier, and leaves too: it saw those phases complete, after the
+        // flag was set.  Every named barrier here is the warpgroup's own.
+        if (abort_flag->abort) {
+          ok = false;
+          break;
+        }
         if (named_bar_or(1 + g, 128, over)) {
           float wm[8];
 #pragma unroll
@@ -722,9 +731,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // a unit that needed a bad page is written as empty (its partial, for a split item)
       // (tagged with the unit's ordinal: a slot is rewritten only two units later,
       // after every thread has passed the next unit's barrier)
-      if (bad) ubad_s[up] = uc + 1;
-      named_bar_sync(3, kSoftmaxThreads);
-      const bool unit_bad = ubad_s[up] == uc + 1;
+      // (each warpgroup checks every token of the tile, so its own flag is the unit's)
+      if (bad) ubad_s[up][g] = uc + 1;
+      if (abort_flag->abort) {   // as before the barrier-OR above
+        ok = false;
+        break;
+      }
+      named_bar_sync(1 + g, 128);
+      const bool unit_bad = ubad_s[up][g] == uc + 1;
       // row sums over the 128 token lanes: warp butterfly, then the 4 warps in order
 #pragma unroll
       for (int n = 0; n < 8; ++n) {

@@ -94,17 +94,23 @@ constexpr long long kWaitCycles = 2000000000LL;
 // kWaitCycles, or with kRuntimeLimit the CTA's limit_kcycles (the instantiation tests use to
 // make waits run out; kept apart because the production kernels run at their register
 // ceiling, where even this one comparison changes their code).
+//
+// A wait gives up only if its phase is still open after the abort flag is set and visible:
+// a thread that later sees the same phase completed reads the flag after that, so threads
+// that must meet at a named barrier can all tell, before it, that one of them gave up.
 template <bool kCluster, bool kRuntimeLimit = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile WaitCtl* w) {
   const long long t0 = clock64();
   while (true) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (w->abort) return false;
-    const bool out = kRuntimeLimit ? ((clock64() - t0) >> 10) >= w->limit_kcycles : clock64() - t0 > kWaitCycles;
-    if (out) {
+    bool give_up = w->abort != 0;
+    if (!give_up &&
+        (kRuntimeLimit ? ((clock64() - t0) >> 10) >= w->limit_kcycles : clock64() - t0 > kWaitCycles)) {
       w->abort = 1;
-      return false;
+      __threadfence_block();
+      give_up = true;
     }
+    if (give_up) return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   }
 }
 

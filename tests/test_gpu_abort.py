@@ -75,3 +75,52 @@ def test_wait_limit_runs_out_then_the_next_call_is_correct(name):
         _, _, o_ref, l_ref = ow.decode(b)
         assert row_rel_err(o[b].reshape(R, 512), o_ref) < tol, (name, b)
         assert lse_err(lse[b].reshape(R), l_ref) < tol, (name, b)
+
+
+@needs_cuda
+@pytest.mark.parametrize("name", list(CASES))
+def test_waits_running_out_at_any_point_end_cleanly(name):
+    """Limits from one cycle to ~0.1 ms make the waits run out at different points of the
+    pipeline (or not at all): every call returns, and it either reports DCPMLA_DERR_TIMEOUT or
+    its output matches the oracle; a call at the default limit afterwards is correct."""
+    w, fused, _ = CASES[name]
+    dw = Hn.build(w, fused=fused)
+    st = dw.step
+    st.run()
+    torch.cuda.synchronize()
+    assert dw.cache.check_errors() == 0
+    ow = OracleWorkload(w)
+    want = {b: ow.decode(b)[2:] for b in range(w.B)}
+    R = w.Tq * w.H
+    tol = TOL[w.kv_dtype]
+
+    def matches():
+        o, lse = st.o.cpu().numpy(), st.lse.cpu().numpy()
+        return all(row_rel_err(o[b].reshape(R, 512), want[b][0]) < tol and
+                   lse_err(lse[b].reshape(R), want[b][1]) < tol for b in range(w.B))
+
+    timed_out = 0
+    try:
+        for limit in (1, 1 << 12, 1 << 15, 1 << 18):
+            for _ in range(3):
+                B.dcpmla_testing_set_wait_limit(limit)
+                dw.cache.err.zero_()
+                st.o.fill_(float("nan"))
+                st.run_decode()
+                st.run_merge()
+                torch.cuda.synchronize()
+                e = dw.cache.check_errors()
+                assert e & ~B.DERR_TIMEOUT == 0, (name, limit, e)
+                if e & B.DERR_TIMEOUT:
+                    timed_out += 1
+                else:
+                    assert matches(), (name, limit)
+    finally:
+        B.dcpmla_testing_set_wait_limit(0)
+    assert timed_out > 0
+    dw.cache.err.zero_()
+    st.run_decode()
+    st.run_merge()
+    torch.cuda.synchronize()
+    assert dw.cache.check_errors() == 0
+    assert matches()
