@@ -542,35 +542,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_ref[n] = -INFINITY;
         lt[n] = 0.f;
       }
-      for (int i = 0; ok && i < x.ntiles; ++i, ++gi) {
+      for (int i = 0; i < x.ntiles; ++i, ++gi) {   // left only together, at a barrier-OR
         const int sb = gi & 1;
         const int t0 = x.j0 + i * kTok;
         const int ntok = min(kTok, x.j1 - t0);
         // this thread's page id, checked at the end of the tile (its load is in
         // flight meanwhile)
         const int gpg = tok < ntok ? __ldg(pt_row + (t0 + tok) / a.P) : 0;
-        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t own[8];
-        tmem_ld8(tmem + lane_off + kColS + (uint32_t)(sb * kRp + 8 * g), own);
-        tmem_ld_wait();
-        // the score buffer may take the QK two tiles ahead
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
-        // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
-        if (gi >= 1) {
-          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
-          if (!ok) break;
+        // A failed wait does not leave the loop at once: every warp of the warpgroup goes on
+        // to the warpgroup's barrier-OR below, skipping the work of the failed steps.  A named
+        // barrier has no time limit, so all of its threads must reach it: the softmax warps
+        // leave their loops only where a barrier-OR over the warpgroup tells every warp the
+        // same, and every named barrier here is one warpgroup's own.
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_s_full[sb]), (gi >> 1) & 1, abort_flag));
+        uint32_t own[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ok) {
+          tc_fence_after();
+          tmem_ld8(tmem + lane_off + kColS + (uint32_t)(sb * kRp + 8 * g), own);
+          tmem_ld_wait();
+          // the score buffer may take the QK two tiles ahead
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
         }
+        // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
+        if (ok && gi >= 1)
+          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
+        if (ok) {
 #pragma unroll
-        for (int v = 0; v < 2; ++v)
-          st_async_v4(x_remote + (uint32_t)(((2 * g + v) * kTok + tok) * 16),
-                      make_uint4(own[4 * v], own[4 * v + 1], own[4 * v + 2], own[4 * v + 3]), xfull_remote);
-        if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
-        ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), gi & 1, abort_flag));
-        if (!ok) break;
+          for (int v = 0; v < 2; ++v)
+            st_async_v4(x_remote + (uint32_t)(((2 * g + v) * kTok + tok) * 16),
+                        make_uint4(own[4 * v], own[4 * v + 1], own[4 * v + 2], own[4 * v + 3]), xfull_remote);
+          if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
+          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), gi & 1, abort_flag));
+        }
+        // the warpgroup leaves the loop together if any of its warps failed a wait
+        if (named_bar_or(1 + g, 128, !ok)) {
+          ok = false;
+          break;
+        }
         float s[8];
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
@@ -602,15 +612,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool over = false;
 #pragma unroll
         for (int n = 0; n < 8; ++n) over |= s[n] > m_ref[n] + 8.f;
-        // A warp leaves its loops at a failed wait, whose phase was still open after the CTA's
-        // abort flag had been set.  A named barrier has no time limit, so a warp that passed
-        // the same waits (the warpgroup's warps wait for the same phases) reads the flag
-        // before each named barrier, and leaves too: it saw those phases complete, after the
-        // flag was set.  Every named barrier here is the warpgroup's own.
-        if (abort_flag->abort) {
-          ok = false;
-          break;
-        }
+        // The same barrier-OR carries a failed wait: when it fires, a second one tells a
+        // failure (the warpgroup then leaves the loop together) from a moving max.
         if (named_bar_or(1 + g, 128, over)) {
           float wm[8];
 #pragma unroll
@@ -648,39 +651,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // ahead of PV, so PV(gi - 2) may still be in flight: wait for it first
             // (its P buffer's barrier), or the parity wait on bar_o could match the
             // phase before.
-            if (gi >= 2) {
+            if (ok && gi >= 2)
               ok = __all_sync(0xffffffffu,
                               wait_bar<false, kRL>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
-              if (!ok) break;
-            }
-            ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
+            if (ok) ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o), (gi - 1) & 1, abort_flag));
+            // on a failed wait the rescale is skipped (the output is invalid then); the
+            // warp leaves at the next decision barrier
+            if (ok) {
+              tc_fence_after();
 #pragma unroll
-            for (int mb = 0; mb < 2; ++mb) {
+              for (int mb = 0; mb < 2; ++mb) {
 #pragma unroll
-              for (int part = 0; part < 2; ++part) {   // hi rows, then lo rows
-                const uint32_t col =
-                    tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + part * 16 + 8 * g);
-                uint32_t v[8];
-                tmem_ld8(col, v);
-                tmem_ld_wait();
+                for (int part = 0; part < 2; ++part) {   // hi rows, then lo rows
+                  const uint32_t col =
+                      tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + part * 16 + 8 * g);
+                  uint32_t v[8];
+                  tmem_ld8(col, v);
+                  tmem_ld_wait();
 #pragma unroll
-                for (int n = 0; n < 8; ++n) v[n] = __float_as_uint(__uint_as_float(v[n]) * alpha[n]);
-                tmem_st8(col, v);
+                  for (int n = 0; n < 8; ++n) v[n] = __float_as_uint(__uint_as_float(v[n]) * alpha[n]);
+                  tmem_st8(col, v);
+                }
               }
+              tmem_st_wait();
             }
-            tmem_st_wait();
 #pragma unroll
             for (int n = 0; n < 8; ++n) lt[n] *= alpha[n];
           }
         }
         // P^T as bf16 hi (rows 0-15) + lo (rows 16-31); one bf16 rounding of the
         // weights alone would cost ~1e-3 relative error in O
-        if (gi >= 2) {
+        if (ok && gi >= 2)
           ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
-          if (!ok) break;
-        }
         // P^T is MN-major with a 64-byte swizzle: a token's 32 rows (hi 0-15, lo 16-31) are
         // one 64-byte line, 8 tokens an atom; this thread's 8 hi and 8 lo rows are one
         // 16-byte unit each (unit u of line t sits at u ^ ((t % 8) / 2))
@@ -698,45 +700,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 ll = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
           lp[n >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
         }
-        {
-          uint8_t* line = sP + sb * kPBuf + (tok >> 3) * 512 + (tok & 7) * 64;
-          const int sw = (tok & 7) >> 1;
-          *reinterpret_cast<uint4*>(line + ((g ^ sw) << 4)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-          *reinterpret_cast<uint4*>(line + (((2 + g) ^ sw) << 4)) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
-        }
-        if (ntok < kTok) {
-          // rows past the unit's last token hold stale data: zero this CTA's V rows
-          uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStage);
-          const int tail = kTok - ntok;
-          for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
-            const int cch = e / (tail * 8), rem = e % (tail * 8), t = ntok + rem / 8;
-            v[((t >> 3) * nck * 1024 + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+        if (ok) {
+          {
+            uint8_t* line = sP + sb * kPBuf + (tok >> 3) * 512 + (tok & 7) * 64;
+            const int sw = (tok & 7) >> 1;
+            *reinterpret_cast<uint4*>(line + ((g ^ sw) << 4)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(line + (((2 + g) ^ sw) << 4)) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
           }
+          if (ntok < kTok) {
+            // rows past the unit's last token hold stale data: zero this CTA's V rows
+            uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStage);
+            const int tail = kTok - ntok;
+            for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
+              const int cch = e / (tail * 8), rem = e % (tail * 8), t = ntok + rem / 8;
+              v[((t >> 3) * nck * 1024 + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_p_full[sb]));
         }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p_full[sb]));
         bad |= gpg < 0 || (int64_t)gpg >= a.num_pages;
       }
-      if (!ok) break;
+      // the warpgroup leaves together if any of its warps failed a wait (a failure after the
+      // last tile's barrier-OR, in the rescale or the P buffer's wait, shows here)
+      if (named_bar_or(1 + g, 128, !ok)) {
+        ok = false;
+        break;
+      }
       // ---- unit epilogue: O^T / l, partial or final output ----
-      if (x.ntiles > 0) {
+      if (ok && x.ntiles > 0) {
         // Not bar_o: when the last tile's softmax ends, the PV two tiles back may
         // still be running, and a parity wait on bar_o would then match an older
         // phase.  bar_o_full[ob] completes once per unit on this buffer.
         ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_full[ob]), (kk >> 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
+        if (ok) tc_fence_after();   // else the output is invalid; the unit ends below
       }
       // a unit that needed a bad page is written as empty (its partial, for a split item)
       // (tagged with the unit's ordinal: a slot is rewritten only two units later,
       // after every thread has passed the next unit's barrier)
       // (each warpgroup checks every token of the tile, so its own flag is the unit's)
       if (bad) ubad_s[up][g] = uc + 1;
-      if (abort_flag->abort) {   // as before the barrier-OR above
-        ok = false;
-        break;
-      }
       named_bar_sync(1 + g, 128);
       const bool unit_bad = ubad_s[up][g] == uc + 1;
       // row sums over the 128 token lanes: warp butterfly, then the 4 warps in order
@@ -765,8 +769,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float* obase = direct ? a.o_part : p.ws_o;
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
-        uint32_t hv[8], lv[8];
-        if (x.ntiles > 0) {
+        uint32_t hv[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (x.ntiles > 0 && ok) {
           const uint32_t col = tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + 8 * g);
           tmem_ld8(col, hv);
           tmem_ld8(col + 16, lv);
@@ -799,6 +803,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // a split item's units are merged by the combine kernel; it also reads this flag
       if (!direct && h == 0 && stid == 0) p.ws_bad[x.slot] = unit_bad ? 1 : 0;
       ++uc;
+      // the unit loop's condition must agree in every thread of the warpgroup
+      if (named_bar_or(1 + g, 128, !ok)) ok = false;
     }
   }
 

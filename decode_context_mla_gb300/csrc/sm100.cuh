@@ -94,10 +94,8 @@ constexpr long long kWaitCycles = 2000000000LL;
 // kWaitCycles, or with kRuntimeLimit the CTA's limit_kcycles (the instantiation tests use to
 // make waits run out; kept apart because the production kernels run at their register
 // ceiling, where even this one comparison changes their code).
-//
-// A wait gives up only if its phase is still open after the abort flag is set and visible:
-// a thread that later sees the same phase completed reads the flag after that, so threads
-// that must meet at a named barrier can all tell, before it, that one of them gave up.
+// A wait that would give up tries its phase once more after the abort flag is set (and
+// fenced): a phase that completed meanwhile still counts.
 template <bool kCluster, bool kRuntimeLimit = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile WaitCtl* w) {
   const long long t0 = clock64();
