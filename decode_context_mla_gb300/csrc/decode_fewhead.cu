@@ -612,8 +612,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool over = false;
 #pragma unroll
         for (int n = 0; n < 8; ++n) over |= s[n] > m_ref[n] + 8.f;
-        // The same barrier-OR carries a failed wait: when it fires, a second one tells a
-        // failure (the warpgroup then leaves the loop together) from a moving max.
         if (named_bar_or(1 + g, 128, over)) {
           float wm[8];
 #pragma unroll
