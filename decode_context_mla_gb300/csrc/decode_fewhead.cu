@@ -27,14 +27,15 @@
 //              then 128-token KV tiles (one 4-D box per page box, all of the CTA's
 //              chunks) into a 2-deep stage ring, and L2 prefetches of the tiles a few
 //              places further on, so that the ring's loads mostly hit L2.
-//   warp 1     lane 0 issues the QK MMAs: M 128, N 16.  QK may run ahead of PV:
-//              a score buffer is free once the softmax has loaded it.
+//   warp 1     issues the QK MMAs (one elected lane of the converged warp): M 128,
+//              N 16.  QK may run ahead of PV: a score buffer is free once the softmax
+//              has loaded it.
 //   warps 2-9  softmax, one thread per token lane, two warpgroups of 8 query
 //              rows each: base-2 online softmax with a lazily moved per-row
 //              reference max, P^T to shared memory, unit epilogue.
 //   warp 10    lane 0 relays "exchange buffer read" to the peer.
-//   warp 11    lane 0 issues the PV MMAs: M 128 (V^T MN-major), N 32 = P as a
-//              bf16 hi part (rows 0-15) and lo part (rows 16-31).
+//   warp 11    issues the PV MMAs (one elected lane): M 128 (V^T MN-major), N 32 =
+//              P as a bf16 hi part (rows 0-15) and lo part (rows 16-31).
 //
 // TMEM columns: S^T double buffer [0, 32), O^T double buffer (by unit) [64, 192):
 // buffer o, value block m (128 dims): hi rows at 64 + 64o + 32m, lo rows 16 later.
@@ -44,6 +45,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <numeric>
 
 #include "decode.cuh"
 #include "sm100.cuh"
@@ -87,7 +89,7 @@ struct FhParams {
   CUtensorMap tm_kv[2][kMaxFhShards];   // [CTA] pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, nck, box_rows / 8}
   CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
   DecodeArgs a;
-  int32_t box_rows;                  // rows per TMA box: min(P, 128)
+  int32_t box_rows;                  // rows per TMA box: gcd(P, 128)
   float* ws_o;                       // [slots, R, 512]: slot item + cluster
   float* ws_lse;                     // [slots, R] (base 2)
   int32_t* ws_bad;                   // [slots]: the unit needed a page outside the pools
@@ -417,82 +419,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       q_issued_s = q_issued;
     }
   } else if (warp == 1 || warp == kPvWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA
-      // Two issuing threads, each blocking on its own barriers: warp 1 issues the QK
-      // of each tile once its KV landed and the softmax has loaded the scores two
-      // tiles back (whose TMEM buffer it overwrites), so QK runs ahead of PV; warp
-      // kPvWarp issues each tile's PV once its P is written, which frees the tile's
-      // stage for the next load.  A commit tracks the MMAs of the thread issuing it.
-      constexpr uint32_t idesc_qk = idesc_bf16(kTok, kRp, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, true);
-      // Base descriptors; the start-address field is the low 14 bits (address >> 4),
-      // so a constant byte offset is added as (offset >> 4) without carries.
-      const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, nck * 1024);      // keys, K-major
-      const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, nck * 1024);    // values, MN-major
-      const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
-      const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);         // P^T, MN-major (32 rows per token)
-      const bool qk_role = warp == 1;
-      bool ok = true;
-      int gt = 0, kk = 0;                  // tiles and units so far
-      for (int it = it_lo; ok && it <= it_hi; ++it) {
-        Unit x;
-        if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
-        const int ntiles = x.ntiles;
-        const int qb = kk & 1, ob = kk & 1;
-        if (qk_role) {
-          ok = wait_bar<false, kRL>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag);
-          for (int i = 0; ok && i < ntiles; ++i, ++gt) {
-            const int sb = gt & 1;
-            if (gt >= 2) ok = wait_bar<false, kRL>(smem_u32(&bar_s_free[sb]), ((gt >> 1) - 1) & 1, abort_flag);
-            if (ok) ok = wait_bar<false, kRL>(smem_u32(&bar_kv_full[sb]), (gt >> 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
+    // ---------------------------------------------------------------- MMA
+    // Two issuing warps, each blocking on its own barriers: warp 1 issues the QK of
+    // each tile once its KV landed and the softmax has loaded the scores two tiles
+    // back (whose TMEM buffer it overwrites), so QK runs ahead of PV; warp kPvWarp
+    // issues each tile's PV once its P is written, which frees the tile's stage for
+    // the next load.  The whole warp runs the loop (waits, descriptors) and one
+    // elected lane issues each MMA and commit, so the operands stay warp-uniform.  A
+    // commit tracks the MMAs of the lane issuing it.
+    constexpr uint32_t idesc_qk = idesc_bf16(kTok, kRp, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, true);
+    // Base descriptors; the start-address field is the low 14 bits (address >> 4),
+    // so a constant byte offset is added as (offset >> 4) without carries.
+    const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, nck * 1024);      // keys, K-major
+    const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, nck * 1024);    // values, MN-major
+    const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
+    const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);         // P^T, MN-major (32 rows per token)
+    const bool qk_role = warp == 1;
+    bool ok = true;
+    int gt = 0, kk = 0;                  // tiles and units so far
+    for (int it = it_lo; ok && it <= it_hi; ++it) {
+      Unit x;
+      if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
+      const int ntiles = x.ntiles;
+      const int qb = kk & 1, ob = kk & 1;
+      if (qk_role) {
+        ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_q_full[qb]), (kk >> 1) & 1, abort_flag));
+        for (int i = 0; ok && i < ntiles; ++i, ++gt) {
+          const int sb = gt & 1;
+          if (gt >= 2)
+            ok = __all_sync(0xffffffffu,
+                            wait_bar<false, kRL>(smem_u32(&bar_s_free[sb]), ((gt >> 1) - 1) & 1, abort_flag));
+          if (ok) ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_kv_full[sb]), (gt >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
 #pragma unroll
-            for (int c = 0; c < 5; ++c) {
-              if (c >= nck) break;
+          for (int c = 0; c < 5; ++c) {
+            if (c >= nck) break;
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_ss(d, kA0 + (uint64_t)((sb * kStage + c * 1024 + k * 32) >> 4),
-                       qB0 + (uint64_t)((qb * kQBuf + c * kQChunk + k * 32) >> 4), idesc_qk, (c | k) != 0);
-            }
-            mma_commit(smem_u32(&bar_s_full[sb]));
+            for (int k = 0; k < 4; ++k)
+              mma_ss_warp(d, kA0 + (uint64_t)((sb * kStage + c * 1024 + k * 32) >> 4),
+                          qB0 + (uint64_t)((qb * kQBuf + c * kQChunk + k * 32) >> 4), idesc_qk, (c | k) != 0);
           }
-          if (ok) mma_commit(smem_u32(&bar_q_free[qb]));   // the unit's Q buffer may be refilled
-        } else {
-          for (int i = 0; ok && i < ntiles; ++i, ++gt) {
-            const int sb = gt & 1;
-            ok = wait_bar<false, kRL>(smem_u32(&bar_p_full[sb]), (gt >> 1) & 1, abort_flag);
-            if (ok && i == 0 && kk >= 2)
-              ok = wait_bar<false, kRL>(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int mb = 0; mb < 2; ++mb) {
-              const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * nck * 1024) >> 4);
-                const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + ks * 1024) >> 4);
-                mma_ss(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
-              }
-            }
-            mma_commit(smem_u32(&bar_kv_empty[sb]));
-            mma_commit(smem_u32(&bar_p_free[sb]));
-            mma_commit(smem_u32(&bar_o));
-            // the unit's O^T is complete: one phase of its buffer's barrier per unit
-            if (i == ntiles - 1) mma_commit(smem_u32(&bar_o_full[ob]));
-          }
+          mma_commit_warp(smem_u32(&bar_s_full[sb]));
         }
-        ++kk;
+        if (ok) mma_commit_warp(smem_u32(&bar_q_free[qb]));   // the unit's Q buffer may be refilled
+      } else {
+        for (int i = 0; ok && i < ntiles; ++i, ++gt) {
+          const int sb = gt & 1;
+          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_full[sb]), (gt >> 1) & 1, abort_flag));
+          if (ok && i == 0 && kk >= 2)
+            ok = __all_sync(0xffffffffu,
+                            wait_bar<false, kRL>(smem_u32(&bar_o_free[ob]), ((kk >> 1) - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int mb = 0; mb < 2; ++mb) {
+            const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * nck * 1024) >> 4);
+              const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + ks * 1024) >> 4);
+              mma_ss_warp(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit_warp(smem_u32(&bar_kv_empty[sb]));
+          mma_commit_warp(smem_u32(&bar_p_free[sb]));
+          mma_commit_warp(smem_u32(&bar_o));
+          // the unit's O^T is complete: one phase of its buffer's barrier per unit
+          if (i == ntiles - 1) mma_commit_warp(smem_u32(&bar_o_full[ob]));
+        }
       }
-      // drain: every MMA issued above completes before TMEM is released (one
-      // arrival per issuing thread)
-      mma_commit(smem_u32(&bar_drain));
-      const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
-      }
+      ++kk;
+    }
+    // drain: every MMA issued above completes before TMEM is released (one arrival per
+    // issuing warp)
+    mma_commit_warp(smem_u32(&bar_drain));
+    const long long t0 = clock64();
+    while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
     }
   } else if (warp == kRelayWarp) {
     if (lane == 0) {
@@ -1005,7 +1010,7 @@ FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
 bool fh_supported(const DecodeArgs& a, int sm_count) {
   if (a.fp8 || a.R > kRp || sm_count < 2) return false;
   if (a.shard_count > kMaxFhShards) return false;
-  if (!(a.P % kTok == 0 || (kTok % a.P == 0 && a.P % 8 == 0))) return false;
+  if (a.P % 8 != 0) return false;   // page boxes of gcd(P, 128) rows: whole 8-token groups
   if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
   // the tile sequence of all items fits 32-bit tile indices
   if ((int64_t)a.B * a.shard_count * (((int64_t)a.max_pages * a.P + kTok - 1) / kTok) > INT32_MAX) return false;
@@ -1029,7 +1034,7 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   int rc = DCPMLA_OK;
   if (fresh) {
     p.a = a;
-    p.box_rows = std::min(a.P, kTok);
+    p.box_rows = std::gcd(a.P, kTok);   // a box never crosses a page or a tile
     p.fused = fused ? 1 : 0;
     rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
     for (int hh = 0; hh < 2; ++hh)

@@ -221,9 +221,10 @@ __device__ __noinline__ void tc_combine_tail(const TcParams& p, int b, int bz, i
 //
 //   warp 0      TMA producer; page ids from a 32-entry window, the tile kLook - 1
 //               places ahead prefetched into L2 (each CTA half of its rows)
-//   warp 1      TMEM allocation; lane 0 issues QK of every tile
+//   warp 1      TMEM allocation; issues QK of every tile (the converged warp runs the
+//               loop, one elected lane issues each MMA: descriptors stay warp-uniform)
 //   warps 2-9   softmax, warpgroup g takes tiles i with i % 2 == g
-//   warp 10     lane 0 issues PV of every tile
+//   warp 10     issues PV of every tile (the same way)
 //   warp 11     lane 0 relays "exchange buffer read" to the peer
 //
 // TMEM columns: O_h [0,256), S/P slots [256,448) (3 x 64), Q_h dims [256h, 256h+128) [448,512).
@@ -408,18 +409,18 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // S(i) = Q_h K_h(i)^T into slot i % 3: dims [256h, 256h+128) with Q from TMEM,
     // [256h+128, 256h+256) and the rope piece with Q from shared memory.  The slot
     // is free once tile i - 3's PV completed, which its stage's release implies.
-    if (lane == 0 && ntiles > 0) {
+    if (ntiles > 0) {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
       const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
       const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
       const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
       const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
       const uint32_t tq = tmem + kColQ;
-      bool ok = wait_bar<false, kRL>(smem_u32(&bar_q_full), 0, abort_flag);
+      bool ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_q_full), 0, abort_flag));
       tc_fence_after();
       for (int i = 0; ok && i < ntiles; ++i) {
         const int st = i % kStages;
-        if (!wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag)) break;
+        if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (i / kStages) & 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d = tmem + kColS + st * kTileTok;
         const uint64_t so = (uint64_t)((st * kStage) >> 4);
@@ -427,19 +428,19 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(d, tq + cl * 32 + k * 8, kd0 + so + ((cl * kChunk + k * 32) >> 4), idesc_qk, (cl | k) != 0);
+            mma_ts_warp(d, tq + cl * 32 + k * 8, kd0 + so + ((cl * kChunk + k * 32) >> 4), idesc_qk, (cl | k) != 0);
 #pragma unroll
         for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(d, qd0 + ((cl * kQChunk + k * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + k * 32) >> 4),
+            mma_ss_warp(d, qd0 + ((cl * kQChunk + k * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + k * 32) >> 4),
                    idesc_qk, 1u);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) mma_ss(d, qr0 + ((k * 32) >> 4), kr0 + so + ((k * 32) >> 4), idesc_qk, 1u);
-        mma_commit(smem_u32(&bar_s_full[st]));
+        for (int k = 0; k < 2; ++k) mma_ss_warp(d, qr0 + ((k * 32) >> 4), kr0 + so + ((k * 32) >> 4), idesc_qk, 1u);
+        mma_commit_warp(smem_u32(&bar_s_full[st]));
       }
       // drain: every MMA issued above completes before TMEM is released
-      mma_commit(smem_u32(&bar_drain_qk));
+      mma_commit_warp(smem_u32(&bar_drain_qk));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kDrainCycles) {
       }
@@ -448,24 +449,24 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // ------------------------------------------------------------ PV issuer
     // O_h += P(i) V_h(i), P as a bf16 hi + lo pair from slot i % 3 (hi columns 0-31,
     // lo 32-63), V MN-major from the stage's four latent chunks.
-    if (lane == 0 && ntiles > 0) {
+    if (ntiles > 0) {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
       const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
       const uint32_t to = tmem + kColO;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
-        if (!wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag)) break;
+        if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (i / kStages) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * kStage) >> 4);
         const uint32_t pa = tmem + kColS + st * kTileTok;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bar_kv_empty[st]));
-        mma_commit(smem_u32(&bar_o_par[i & 1]));
-        if (i == ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // O complete
+          mma_ts_warp(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit_warp(smem_u32(&bar_kv_empty[st]));
+        mma_commit_warp(smem_u32(&bar_o_par[i & 1]));
+        if (i == ntiles - 1) mma_commit_warp(smem_u32(&bar_o_full));   // O complete
       }
-      mma_commit(smem_u32(&bar_drain_pv));
+      mma_commit_warp(smem_u32(&bar_drain_pv));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kDrainCycles) {
       }
@@ -1229,7 +1230,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     // ------------------------------------------------------------ QK issuer
     // S(gi) = Q_h K_h(gi)^T into slot gi % 3, once the unit's Q is loaded; the slot is
     // free once tile gi - 3's PV completed, which its stage's release implies.
-    if (lane == 0) {
+    {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
       const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
       const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
@@ -1241,11 +1242,11 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
       for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
         pp::Unit u;
         if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
-        if (!wait_bar<false, kRL>(smem_u32(&bar_q_full), ui & 1, abort_flag)) break;
+        if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_q_full), ui & 1, abort_flag))) break;
         tc_fence_after();
         for (int i = 0; i < u.ntiles; ++i, ++gi) {
           const int st = gi % kStages;
-          if (!wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (gi / kStages) & 1, abort_flag)) {
+          if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_kv_full[st]), (gi / kStages) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -1256,20 +1257,20 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(d, tq + cl * 32 + kk * 8, kd0 + so + ((cl * kChunk + kk * 32) >> 4), idesc_qk, (cl | kk) != 0);
+              mma_ts_warp(d, tq + cl * 32 + kk * 8, kd0 + so + ((cl * kChunk + kk * 32) >> 4), idesc_qk, (cl | kk) != 0);
 #pragma unroll
           for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(d, qd0 + ((cl * kQChunk + kk * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + kk * 32) >> 4),
+              mma_ss_warp(d, qd0 + ((cl * kQChunk + kk * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + kk * 32) >> 4),
                      idesc_qk, 1u);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) mma_ss(d, qr0 + ((kk * 32) >> 4), kr0 + so + ((kk * 32) >> 4), idesc_qk, 1u);
-          mma_commit(smem_u32(&bar_s_full[st]));
+          for (int kk = 0; kk < 2; ++kk) mma_ss_warp(d, qr0 + ((kk * 32) >> 4), kr0 + so + ((kk * 32) >> 4), idesc_qk, 1u);
+          mma_commit_warp(smem_u32(&bar_s_full[st]));
         }
         ++ui;
       }
-      mma_commit(smem_u32(&bar_drain_qk));
+      mma_commit_warp(smem_u32(&bar_drain_qk));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bar_drain_qk), 0) && clock64() - t0 < kDrainCycles) {
       }
@@ -1278,7 +1279,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     // ------------------------------------------------------------ PV issuer
     // O_h += P(gi) V_h(gi); a unit's first PV overwrites O, once the softmax has read the
     // previous unit's O; its last PV commits the unit's O.
-    if (lane == 0) {
+    {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
       const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
       const uint32_t to = tmem + kColO;
@@ -1289,8 +1290,8 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
         for (int i = 0; i < u.ntiles; ++i, ++gi) {
           const int st = gi % kStages;
-          if (!wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (gi / kStages) & 1, abort_flag) ||
-              (i == 0 && ui > 0 && !wait_bar<false, kRL>(smem_u32(&bar_o_free), (ui - 1) & 1, abort_flag))) {
+          if (!__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_full[st]), (gi / kStages) & 1, abort_flag)) ||
+              (i == 0 && ui > 0 && !__all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_o_free), (ui - 1) & 1, abort_flag)))) {
             ok = false;
             break;
           }
@@ -1299,14 +1300,14 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           const uint32_t pa = tmem + kColS + st * kTileTok;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(to, pa + kk * 8, vd + (((kk & 3) * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bar_kv_empty[st]));
-          mma_commit(smem_u32(&bar_o_par[gi & 1]));
-          if (i == u.ntiles - 1) mma_commit(smem_u32(&bar_o_full));   // the unit's O is complete
+            mma_ts_warp(to, pa + kk * 8, vd + (((kk & 3) * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_warp(smem_u32(&bar_kv_empty[st]));
+          mma_commit_warp(smem_u32(&bar_o_par[gi & 1]));
+          if (i == u.ntiles - 1) mma_commit_warp(smem_u32(&bar_o_full));   // the unit's O is complete
         }
         ++ui;
       }
-      mma_commit(smem_u32(&bar_drain_pv));
+      mma_commit_warp(smem_u32(&bar_drain_pv));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&bar_drain_pv), 0) && clock64() - t0 < kDrainCycles) {
       }

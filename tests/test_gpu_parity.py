@@ -62,11 +62,16 @@ SMALL = {
                           seed=20, L=3001),
     "fh_chunked": W.scaled(W.WORKLOADS["long"], B=2, L=300000),
     # page sizes above the 128-token tile and between the tested ones: the token-major kernel
-    # copies a page box of 8-token groups for all of a CTA's chunks at once
+    # copies a page box of gcd(P, 128) rows (whole 8-token groups) for all of a CTA's chunks at
+    # once, so a box never crosses a page or a tile (P = 24 and P = 40: sixteen boxes a tile)
     "fh_p256": W.Workload("fh256", B=2, H=16, Tq=1, c=2, P=256, kv_dtype="bf16", lse_base="e",
                           seed=23, L=2333),
     "fh_p32_tq4": W.Workload("fh32", B=3, H=4, Tq=4, c=4, P=32, kv_dtype="bf16", lse_base="2",
                              seed=24, lengths_mix=(1, 4000, 6000, 5, 200)),
+    "fh_p24_c3": W.Workload("fh24", B=3, H=16, Tq=1, c=3, P=24, kv_dtype="bf16", lse_base="e",
+                            seed=35, lengths_mix=(2, 500, 3000, 1, 70)),
+    "fh_p40_tq2": W.Workload("fh40", B=2, H=8, Tq=2, c=2, P=40, kv_dtype="bf16", lse_base="2",
+                             seed=36, L=4321),
     # interleave size I > 1 (tokens to shards in runs of I) on each decode kernel
     "ilv16_long": W.scaled(W.WORKLOADS["long"], B=2, L=40000, interleave=16),
     "ilv2_c3_tq2": W.Workload("il2", B=3, H=8, Tq=2, c=3, P=16, kv_dtype="bf16", lse_base="2",
