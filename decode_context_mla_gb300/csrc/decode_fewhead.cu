@@ -64,7 +64,7 @@ constexpr int kStage = 5 * kChunk;             // room for CTA 1's five chunks
 // 128-byte-swizzle atom, so one 4-D TMA box lands all of a page box's chunks; for the MMAs the
 // 8-token groups of a chunk are nck KB apart and a chunk's groups start c KB in.
 constexpr int kStages = 2;
-constexpr int kLook = 4;                       // page-id lookahead (tiles); L2 prefetch kLook - 1 ahead
+constexpr int kLook = 3;                       // page-id lookahead (tiles); L2 prefetch kLook - 1 ahead
 constexpr int kQChunk = kRp * 128;             // Q^T chunk [16 rows x 64 dims]
 constexpr int kQBuf = 5 * kQChunk;
 constexpr int kPChunk = 2 * kRp * 128;         // P^T chunk [32 rows (hi, lo) x 64 tokens]
