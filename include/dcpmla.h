@@ -238,8 +238,11 @@ int dcpmla_decode_workspace_size(int32_t B, int32_t Tq, int32_t H, int32_t P, in
 /* Which decode kernels dcpmla_decode runs for the same arguments as
  * dcpmla_decode_workspace_size, on the current device (host only, no launch):
  *   *path = DCPMLA_PATH_TC_FEWHEAD: tensor cores with the KV tokens as the MMA's
- *           M dimension (at most 16 query rows H*Tq, bf16 KV);
- *           DCPMLA_PATH_TC_ROWS: tensor cores on 128-row query tiles;
+ *           M dimension (at most 16 query rows H*Tq, at least 16 in the batch,
+ *           bf16 KV, at most 8 shards in the call, P a multiple of 8);
+ *           DCPMLA_PATH_TC_ROWS: tensor cores on 128-row query tiles (at most 8
+ *           shards in the call, P a multiple of 64 or a divisor of 64 that is a
+ *           multiple of 8);
  *           DCPMLA_PATH_CUDA_CORE: CUDA-core kernel (other shapes);
  *   *kernel_launches = kernels one dcpmla_decode call enqueues (memsets excluded).
  * Either output pointer may be NULL. */
