@@ -415,9 +415,15 @@ def measure_step(args, w: W.Workload, ws: int, local: int, with_e2e: bool) -> di
     e2e = run_e2e(args, w, dw, stream, acc, ws) if with_e2e else None
 
     # slot map + append (when the step appends), the decode's kernels, the merge
-    # (fused: the decode's own merge kernel replaces the split merge and the LSE merge)
-    launches_per_step = (2 if step.do_append else 0) + (dec_launches if not args.fused else
-                                                         (dec_launches if path == 2 else 2))
+    # (fused: the decode's own merge kernel replaces the split merge and the LSE merge on
+    # the bf16 tensor-core paths; E4M3 on the 128-row path decodes, then runs the LSE merge)
+    if not args.fused:
+        dec_step = dec_launches
+    elif path == 2:
+        dec_step = dec_launches + (1 if w.kv_dtype == "e4m3" else 0)
+    else:
+        dec_step = 2
+    launches_per_step = (2 if step.do_append else 0) + dec_step
     if not args.fused:
         launches_per_step += 1
     res = dict(acc=acc, lens=lens, ms_step=ms_step, ms_dec=ms_dec, roofline=roofline,

@@ -199,17 +199,24 @@ int dcpmla_decode(const void* d_q, void* const* pools, float* const* scale_pools
   return launch_decode_fma(a, d_workspace, ws_bytes, sm, (cudaStream_t)stream);
 }
 
-// Fused decode + merge of all c shards.  The tensor-core kernels merge in-kernel
-// (token-major: a merge kernel over every unit of the request; 128-row tiles: the
-// last CTA of a request's row tile); the CUDA-core path decodes into the
-// workspace and merges with the LSE-merge kernel.
+// Fused decode + merge of all c shards.  The bf16 tensor-core kernels merge without
+// per-shard outputs (token-major: a merge kernel over every unit of the request; 128-row
+// tiles: a merge kernel over the persistent grid's partials, or the last CTA of a
+// request's row tile); E4M3 on the tensor cores and the CUDA-core path decode into
+// per-shard partials in the workspace and merge them with the LSE-merge kernel (for
+// E4M3 that measured faster than merging in the decode's last CTAs: 6.49 against
+// 6.73 ms on the FP8 verification batch).
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+bool merge_in_decode(const DecodeArgs& a, int sm) {
+  return fh_supported(a, sm) || (tc_supported(a) && !a.fp8);
+}
+
 size_t merged_ws(const DecodeArgs& a, int sm, size_t* part_off) {
   if (fh_supported(a, sm)) return fh_workspace_bytes(a, sm);
-  if (tc_supported(a)) return tc_workspace_bytes(a, sm, true);
-  const size_t f = align256(fma_workspace_bytes(a, sm));
+  if (tc_supported(a) && !a.fp8) return tc_workspace_bytes(a, sm, true);
+  const size_t f = align256(tc_supported(a) ? tc_workspace_bytes(a, sm, false) : fma_workspace_bytes(a, sm));
   if (part_off) *part_off = f;
   const size_t rows = (size_t)a.shard_count * a.B * a.R;
   return f + align256(rows * kDL * 4) + rows * 4;
@@ -246,7 +253,7 @@ int dcpmla_decode_merged(const void* d_q, void* const* pools, float* const* scal
   if (ws_bytes < need || (need && !d_workspace)) return DCPMLA_ERR_CAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
   if (fh_supported(a, sm)) return launch_decode_fh(a, d_workspace, ws_bytes, sm, s, true);
-  if (tc_supported(a)) return launch_decode_tc(a, d_workspace, ws_bytes, sm, s, true);
+  if (merge_in_decode(a, sm)) return launch_decode_tc(a, d_workspace, ws_bytes, sm, s, true);
   uint8_t* w = static_cast<uint8_t*>(d_workspace);
   const size_t rows = (size_t)c * B * a.R;
   float* o_part = reinterpret_cast<float*>(w + part_off);
@@ -254,7 +261,8 @@ int dcpmla_decode_merged(const void* d_q, void* const* pools, float* const* scal
   DecodeArgs ap = a;
   ap.o_part = o_part;
   ap.lse_part = lse_part;
-  st = launch_decode_fma(ap, d_workspace, part_off, sm, s);
+  st = tc_supported(ap) ? launch_decode_tc(ap, d_workspace, part_off, sm, s, false)
+                        : launch_decode_fma(ap, d_workspace, part_off, sm, s);
   if (st != DCPMLA_OK) return st;
   return dcpmla_lse_merge(o_part, lse_part, c, (int64_t)B * a.R, lse_base, d_o, d_lse, d_err, stream);
 }

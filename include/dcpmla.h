@@ -258,10 +258,11 @@ int dcpmla_decode_path(int32_t B, int32_t Tq, int32_t H, int32_t P, int32_t c, i
  * c shards of every request as dcpmla_decode does and writes the merged result
  * directly: d_o fp32 [B, Tq, H, 512] = sum_r b^(lse_r - lse) o_r and d_lse fp32
  * [B, Tq, H] = log_b sum_r b^(lse_r), in lse_base; there is no per-shard output.
- * The tensor-core paths merge inside the decode (the token-major path in one
- * merge kernel over every partial of the request, the 128-row path in the last
- * CTA of each request's row tile); the CUDA-core path decodes into the
- * workspace and then runs the LSE merge.  A shard that needed a bad page id is
+ * The bf16 tensor-core paths write no per-shard output (the token-major path and
+ * the persistent 128-row grid end in one merge kernel over every partial of the
+ * request, the non-persistent 128-row kernel merges in the last CTA of each
+ * request's row tile); E4M3 on the tensor cores and the CUDA-core path decode
+ * into per-shard partials in the workspace and then run the LSE merge.  A shard that needed a bad page id is
  * left out of the merge (DCPMLA_DERR_PAGE is set), like its empty partial in
  * the unfused path.  Arguments as in dcpmla_decode; d_workspace: at least
  * dcpmla_decode_merged_workspace_size() bytes for the same shape.

@@ -315,7 +315,7 @@ def test_decode_path_per_workload():
 FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
                "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5", "tc_r96_c3", "tc_c2_cut",
                "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
-               "ilv2_c16", "tc_p8_c3", "tc_p256_tq4"]
+               "ilv2_c16", "tc_p8_c3", "tc_p256_tq4", "tc_e4m3_p8", "ilv8_fp8", "fp8_h16_tq4", "fh_p24_c3"]
 
 
 @needs_cuda
