@@ -89,7 +89,7 @@ struct FhParams {
   CUtensorMap tm_kv[2][kMaxFhShards];   // [CTA] pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, nck, box_rows / 8}
   CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
   DecodeArgs a;
-  int32_t box_rows;                  // rows per TMA box: gcd(P, 128)
+  int32_t box_rows;                  // rows per TMA box: gcd(P, 16)
   float* ws_o;                       // [slots, R, 512]: slot item + cluster
   float* ws_lse;                     // [slots, R] (base 2)
   int32_t* ws_bad;                   // [slots]: the unit needed a page outside the pools
@@ -1010,7 +1010,7 @@ FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
 bool fh_supported(const DecodeArgs& a, int sm_count) {
   if (a.fp8 || a.R > kRp || sm_count < 2) return false;
   if (a.shard_count > kMaxFhShards) return false;
-  if (a.P % 8 != 0) return false;   // page boxes of gcd(P, 128) rows: whole 8-token groups
+  if (a.P % 8 != 0) return false;   // page boxes of gcd(P, 16) rows: whole 8-token groups
   if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
   // the tile sequence of all items fits 32-bit tile indices
   if ((int64_t)a.B * a.shard_count * (((int64_t)a.max_pages * a.P + kTok - 1) / kTok) > INT32_MAX) return false;
@@ -1034,7 +1034,9 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   int rc = DCPMLA_OK;
   if (fresh) {
     p.a = a;
-    p.box_rows = std::gcd(a.P, kTok);   // a box never crosses a page or a tile
+    // a box never crosses a page or a tile; boxes of 16 rows (8 a tile) land sooner than
+    // larger ones (64-token pages: 0.874 ms on the long workload against 0.900 with 64-row boxes)
+    p.box_rows = std::gcd(a.P, 16);
     p.fused = fused ? 1 : 0;
     rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
     for (int hh = 0; hh < 2; ++hh)

@@ -62,7 +62,7 @@ SMALL = {
                           seed=20, L=3001),
     "fh_chunked": W.scaled(W.WORKLOADS["long"], B=2, L=300000),
     # page sizes above the 128-token tile and between the tested ones: the token-major kernel
-    # copies a page box of gcd(P, 128) rows (whole 8-token groups) for all of a CTA's chunks at
+    # copies a page box of gcd(P, 16) rows (whole 8-token groups) for all of a CTA's chunks at
     # once, so a box never crosses a page or a tile (P = 24 and P = 40: sixteen boxes a tile)
     "fh_p256": W.Workload("fh256", B=2, H=16, Tq=1, c=2, P=256, kv_dtype="bf16", lse_base="e",
                           seed=23, L=2333),
