@@ -41,6 +41,7 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <numeric>
 
 #include "decode.cuh"
 #include "sm100.cuh"
@@ -60,13 +61,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxCombineParts = 80;                // clusters one item may span (<= SM pairs)
 
 struct TcParams {
-  CUtensorMap tm_kv[kMaxTcShards];    // bf16 pool as [pool_rows, 576], box {64, box_rows};
-                                      // E4M3 pool as [pool_rows, 576] bytes, box {64, box_rows}
-  CUtensorMap tm_kv3[kMaxTcShards];   // bf16 pool as {64, pool_rows, 9 chunks}, box {64, 64, 4}
+  CUtensorMap tm_kv[kMaxTcShards];    // E4M3 pool as [pool_rows, 576] bytes, box {64, box_rows}
+  CUtensorMap tm_kv3[kMaxTcShards];   // bf16 pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, 4, box_rows / 8}
   CUtensorMap tm_rope[kMaxTcShards];  // bf16 pool as [pool_rows, 576], box {32, box_rows}, 64-byte swizzle
   DecodeArgs a;
-  int32_t box_rows;                   // rows per TMA box: min(P, 64)
-  int32_t use3d;                      // 1: one 3-D box per 4 chunks (bf16, needs box_rows == 64)
+  int32_t box_rows;                   // rows per TMA box: bf16 gcd(P, 16), E4M3 min(P, 64)
   int32_t num_splits, chunk, row_tiles;
   float* ws_o;
   float* ws_lse;
@@ -231,6 +230,10 @@ __device__ __noinline__ void tc_combine_tail(const TcParams& p, int b, int bz, i
 namespace b16 {
 constexpr int kStages = 3;                          // KV stages = S/P slots: tile i uses i % 3
 constexpr int kChunk = kTileTok * 128;              // 64 tokens x 64 dims, 128-byte swizzle
+// The latent part of a stage is row-group major: [8-token group][chunk][8 tokens x 128 B], each
+// 1 KB piece a 128-byte-swizzle atom, so one 4-D TMA box lands a page box's rows for all four
+// chunks; for the MMAs the 8-token groups are 4 KB apart and a chunk's groups start c KB in.
+constexpr int kGroup = 4 * 1024;                    // one 8-token group of the four chunks
 constexpr int kRopeOff = 4 * kChunk;                // then 64 tokens x 32 rope dims, 64-byte swizzle
 constexpr int kStage = kRopeOff + kTileTok * 64;    // 36 KB
 constexpr int kQChunk = kRows * 128;                // Q in shared memory: 2 latent chunks
@@ -334,13 +337,11 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // the L2 prefetch distance leaves it (one read of the page table per 32 pages, all
     // lanes at once).  Every page id was range-checked above.
     if (ntiles > 0) {
-      const CUtensorMap* kvmap = &p.tm_kv[sr];
-      const CUtensorMap* kvmap3 = &p.tm_kv3[sr];
+      const CUtensorMap* kvmap = &p.tm_kv3[sr];         // row groups, all four chunks
       const CUtensorMap* ropemap = &p.tm_rope[sr];
       if (lane == 0) {
         prefetch_tmap(kvmap);
         prefetch_tmap(ropemap);
-        if (p.use3d) prefetch_tmap(kvmap3);
       }
       const int box = p.box_rows;
       const uint8_t* pool = static_cast<const uint8_t*>(a.kv.pool[r]);
@@ -391,12 +392,8 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         if (has) {
           const int y = g * a.P + tok % a.P;
           const uint32_t dst = smem_u32(sKV + st * kStage);
-          if (p.use3d) {
-            tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
-          } else {
-            for (int cl = 0; cl < 4; ++cl)
-              tma_load_2d(dst + cl * kChunk + lane * box * 128, kvmap, (int)(4 * h + cl) * 64, y, full);
-          }
+          // the box's rows (whole 8-token groups) of this CTA's four latent chunks in one copy
+          tma_load_4d(dst + lane * (box >> 3) * kGroup, kvmap, 0, 0, (int)(4 * h), y >> 3, full);
           tma_load_2d(dst + kRopeOff + lane * box * 64, ropemap, 512 + 32 * (int)h, y, full);
         }
         issued = i + 1;
@@ -411,7 +408,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // is free once tile i - 3's PV completed, which its stage's release implies.
     if (ntiles > 0) {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
-      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, kGroup);            // K-major keys
       const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
       const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
       const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
@@ -428,12 +425,12 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts_warp(d, tq + cl * 32 + k * 8, kd0 + so + ((cl * kChunk + k * 32) >> 4), idesc_qk, (cl | k) != 0);
+            mma_ts_warp(d, tq + cl * 32 + k * 8, kd0 + so + ((cl * 1024 + k * 32) >> 4), idesc_qk, (cl | k) != 0);
 #pragma unroll
         for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss_warp(d, qd0 + ((cl * kQChunk + k * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + k * 32) >> 4),
+            mma_ss_warp(d, qd0 + ((cl * kQChunk + k * 32) >> 4), kd0 + so + (((cl + 2) * 1024 + k * 32) >> 4),
                    idesc_qk, 1u);
 #pragma unroll
         for (int k = 0; k < 2; ++k) mma_ss_warp(d, qr0 + ((k * 32) >> 4), kr0 + so + ((k * 32) >> 4), idesc_qk, 1u);
@@ -451,7 +448,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
     // lo 32-63), V MN-major from the stage's four latent chunks.
     if (ntiles > 0) {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
-      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), 1024, kGroup);          // MN-major values
       const uint32_t to = tmem + kColO;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
@@ -461,7 +458,7 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         const uint32_t pa = tmem + kColS + st * kTileTok;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts_warp(to, pa + k * 8, vd + (((k & 3) * 2048) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+          mma_ts_warp(to, pa + k * 8, vd + (((k & 3) * 2 * kGroup) >> 4), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
         mma_commit_warp(smem_u32(&bar_kv_empty[st]));
         mma_commit_warp(smem_u32(&bar_o_par[i & 1]));
         if (i == ntiles - 1) mma_commit_warp(smem_u32(&bar_o_full));   // O complete
@@ -661,7 +658,8 @@ __device__ __forceinline__ void decode_tc_bf16_body(const TcParams& p) {
         const int tail = kTileTok - ntok;
         for (int e = row; e < 4 * tail * 8; e += kWgThreads) {
           const int cch = e / (tail * 8), rem = e % (tail * 8);
-          v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+          const int t = ntok + rem / 8;
+          v[((t >> 3) * kGroup + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async();
       }
@@ -1146,8 +1144,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     for (int it = it0; ok && it < p.items && __ldg(p.ws_pre + it) < t_hi; ++it) {
       pp::Unit u;
       if (!pp::unit_of(p, it, t_lo, t_hi, k, u)) continue;
-      const CUtensorMap* kvmap = &p.tm_kv[u.sr];
-      const CUtensorMap* kvmap3 = &p.tm_kv3[u.sr];
+      const CUtensorMap* kvmap = &p.tm_kv3[u.sr];       // row groups, all four chunks
       const CUtensorMap* ropemap = &p.tm_rope[u.sr];
       const uint8_t* pool = static_cast<const uint8_t*>(a.kv.pool[u.r]);
       const int32_t* pt_row = a.pt + (int64_t)u.b * a.max_pages;
@@ -1156,7 +1153,6 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         unit_bad_s[ui % pp::kUnitFlags] = 0;
         prefetch_tmap(kvmap);
         prefetch_tmap(ropemap);
-        if (p.use3d) prefetch_tmap(kvmap3);
         // this unit's query rows (contiguous), each CTA of the pair half of them
         const int64_t q0 = (int64_t)u.b * R + (int64_t)u.rt * kRows;
         const uint32_t half = (uint32_t)min((int64_t)kRows, R - (int64_t)u.rt * kRows) * (kDK * 2 / 2);
@@ -1204,12 +1200,8 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
         if (has) {
           const int y = g * a.P + tok % a.P;
           const uint32_t dst = smem_u32(sKV + st * kStage);
-          if (p.use3d) {
-            tma_load_3d(dst, kvmap3, 0, y, (int)(4 * h), full);
-          } else {
-            for (int cl = 0; cl < 4; ++cl)
-              tma_load_2d(dst + cl * kChunk + lane * box * 128, kvmap, (int)(4 * h + cl) * 64, y, full);
-          }
+          // the box's rows (whole 8-token groups) of this CTA's four latent chunks in one copy
+          tma_load_4d(dst + lane * (box >> 3) * kGroup, kvmap, 0, 0, (int)(4 * h), y >> 3, full);
           tma_load_2d(dst + kRopeOff + lane * box * 64, ropemap, 512 + 32 * (int)h, y, full);
         }
         issued = gi + 1;
@@ -1232,7 +1224,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     // free once tile gi - 3's PV completed, which its stage's release implies.
     {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, kTileTok, false, false);
-      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, 1024);              // K-major keys
+      const uint64_t kd0 = desc_sw128(smem_u32(sKV), 16, kGroup);            // K-major keys
       const uint64_t kr0 = desc_sw64(smem_u32(sKV + kRopeOff), 16, 512);    // rope keys
       const uint64_t qd0 = desc_sw128(smem_u32(sQ), 16, 1024);               // Q latent part
       const uint64_t qr0 = desc_sw64(smem_u32(sQ + kQRopeOff), 16, 512);     // Q rope part
@@ -1257,12 +1249,12 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts_warp(d, tq + cl * 32 + kk * 8, kd0 + so + ((cl * kChunk + kk * 32) >> 4), idesc_qk, (cl | kk) != 0);
+              mma_ts_warp(d, tq + cl * 32 + kk * 8, kd0 + so + ((cl * 1024 + kk * 32) >> 4), idesc_qk, (cl | kk) != 0);
 #pragma unroll
           for (int cl = 0; cl < 2; ++cl)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss_warp(d, qd0 + ((cl * kQChunk + kk * 32) >> 4), kd0 + so + (((cl + 2) * kChunk + kk * 32) >> 4),
+              mma_ss_warp(d, qd0 + ((cl * kQChunk + kk * 32) >> 4), kd0 + so + (((cl + 2) * 1024 + kk * 32) >> 4),
                      idesc_qk, 1u);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) mma_ss_warp(d, qr0 + ((kk * 32) >> 4), kr0 + so + ((kk * 32) >> 4), idesc_qk, 1u);
@@ -1281,7 +1273,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
     // previous unit's O; its last PV commits the unit's O.
     {   // the whole warp; one elected lane issues
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, 256, false, true);
-      const uint64_t vd0 = desc_sw128(smem_u32(sKV), kChunk, 1024);          // MN-major values
+      const uint64_t vd0 = desc_sw128(smem_u32(sKV), 1024, kGroup);          // MN-major values
       const uint32_t to = tmem + kColO;
       int gi = 0, ui = 0;
       bool ok = true;
@@ -1300,7 +1292,7 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           const uint32_t pa = tmem + kColS + st * kTileTok;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts_warp(to, pa + kk * 8, vd + (((kk & 3) * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_warp(to, pa + kk * 8, vd + (((kk & 3) * 2 * kGroup) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit_warp(smem_u32(&bar_kv_empty[st]));
           mma_commit_warp(smem_u32(&bar_o_par[gi & 1]));
           if (i == u.ntiles - 1) mma_commit_warp(smem_u32(&bar_o_full));   // the unit's O is complete
@@ -1523,7 +1515,8 @@ __device__ __forceinline__ void decode_tc_bf16_persist_body(const TcParams& p) {
           const int tail = kTileTok - ntok;
           for (int e = row; e < 4 * tail * 8; e += kWgThreads) {
             const int cch = e / (tail * 8), rem = e % (tail * 8);
-            v[(cch * kChunk + (ntok + rem / 8) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+            const int t = ntok + rem / 8;
+            v[((t >> 3) * kGroup + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
         }
@@ -2226,21 +2219,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The same pool viewed as {64 elements, rows, 9 column chunks} (a chunk is 128 B of
-// a row): one box {64, 64 rows, 4 chunks} lands as four [64 x 128 B] chunk tiles.
-int encode_rows_chunks(CUtensorMap* m, const void* base, uint64_t rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return DCPMLA_ERR_CUDA;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, 9};
-  cuuint64_t strides[2] = {(cuuint64_t)kDK * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTileTok, 4};
-  cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DCPMLA_OK : DCPMLA_ERR_CUDA;
-}
-
 // E4M3 pool as [rows, 576] bytes; a box {box_cols codes, box_rows} lands unswizzled.
 int encode_rows_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -2418,22 +2396,21 @@ bool tc_supported(const DecodeArgs& a) {
   if (a.shard_count > kMaxTcShards) return false;
   if (!(a.P % kTileTok == 0 || (kTileTok % a.P == 0 && a.P % 8 == 0))) return false;
   if ((int64_t)a.B * a.R > INT32_MAX || a.pool_rows > INT32_MAX) return false;
+  if (!a.fp8 && a.pool_rows % 8 != 0) return false;   // bf16 tiles arrive in 8-row groups
   return true;
 }
 
 namespace {
 // Tensor maps shared by both bf16 launch paths.
+// A page box (gcd(P, 16) rows: 16-row boxes land sooner than whole 64-row pages) of this
+// CTA's four latent chunks is one 4-D copy in row groups; its rope piece a 2-D copy.
 int encode_bf16_maps(TcParams& p, const DecodeArgs& a) {
   int rc = DCPMLA_OK;
   for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
     const void* pool = a.kv.pool[a.shard_begin + i];
-    rc = encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+    rc = tma_encode_kv_rowgroups(&p.tm_kv3[i], pool, (uint64_t)a.pool_rows, 4u, (uint32_t)p.box_rows / 8);
     if (rc == DCPMLA_OK) rc = encode_rows_rope(&p.tm_rope[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
   }
-  p.use3d = p.box_rows == kTileTok;
-  for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
-    if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
-      p.use3d = 0;   // fall back to one 2-D box per chunk
   return rc;
 }
 
@@ -2459,7 +2436,7 @@ int launch_decode_tc_pp(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_c
       p.a.lse_part = reinterpret_cast<float*>(w + plan.lp_off);
       p.a.base2 = true;
     }
-    p.box_rows = std::min(a.P, kTileTok);
+    p.box_rows = std::gcd(a.P, 16);
     p.num_splits = 1;
     p.chunk = 0;
     p.row_tiles = plan.row_tiles;
@@ -2545,23 +2522,18 @@ int launch_decode_tc(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   int rc = DCPMLA_OK;
   if (fresh) {
     p.a = a;
-    p.box_rows = std::min(a.P, kTileTok);
+    p.box_rows = a.fp8 ? std::min(a.P, kTileTok) : std::gcd(a.P, 16);
     p.num_splits = plan.splits;
     p.chunk = plan.chunk;
     p.row_tiles = plan.row_tiles;
     p.fused = fused ? 1 : 0;
-    for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i) {
-      const void* pool = a.kv.pool[a.shard_begin + i];
-      rc = a.fp8 ? encode_rows_e4m3(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, 64, (uint32_t)p.box_rows)
-                 : encode_rows_576(&p.tm_kv[i], pool, (uint64_t)a.pool_rows, (uint32_t)p.box_rows);
+    if (a.fp8) {
+      for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
+        rc = encode_rows_e4m3(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows, 64,
+                              (uint32_t)p.box_rows);
+    } else {
+      rc = encode_bf16_maps(p, a);
     }
-    for (int i = 0; rc == DCPMLA_OK && !a.fp8 && i < a.shard_count; ++i)
-      rc = encode_rows_rope(&p.tm_rope[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
-                            (uint32_t)p.box_rows);
-    p.use3d = !a.fp8 && p.box_rows == kTileTok;
-    for (int i = 0; rc == DCPMLA_OK && p.use3d && i < a.shard_count; ++i)
-      if (encode_rows_chunks(&p.tm_kv3[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows) != DCPMLA_OK)
-        p.use3d = 0;   // fall back to one 2-D box per chunk
     if (plan.splits > 1 || fused) {
       uint8_t* w = static_cast<uint8_t*>(ws);
       p.ws_cnt = reinterpret_cast<uint32_t*>(w + plan.cnt_off);
