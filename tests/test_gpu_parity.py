@@ -309,6 +309,12 @@ def test_decode_path_per_workload():
         kv = B.KV_BF16 if w.kv_dtype == "bf16" else B.KV_E4M3
         got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, kv, max(w.pages_per_request()))
         assert got == (B.PATH_CUDA_CORE, 1), name
+    # page sizes that are multiples of 8 but neither divide nor are divided by the tile stay on
+    # the token-major kernel (page boxes of gcd(P, 16) rows)
+    for name in ("fh_p24_c3", "fh_p40_tq2", "fh_p256", "fh_short_p8"):
+        w = SMALL[name]
+        got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
+        assert got == (B.PATH_TC_FEWHEAD, 2), name
 
 
 
