@@ -108,6 +108,10 @@ SMALL = {
                             seed=33, L=5000),
     "tc_c2_cut": W.Workload("tccut", B=1, H=128, Tq=1, c=2, P=64, kv_dtype="bf16", lse_base="2",
                             seed=34, L=60000),
+    # persistent grid with items that have no tiles (contexts shorter than c: empty shards)
+    # beside items cut by share boundaries
+    "tc_empty_c8": W.Workload("tcempty", B=4, H=128, Tq=1, c=8, P=64, kv_dtype="bf16", lse_base="2",
+                              seed=37, lengths_mix=(2, 9000, 20000, 1, 6)),
 }
 
 # cases that must run on the CUDA-core decode (asserted by test_decode_path_per_workload)
