@@ -8,39 +8,38 @@
 // position j*c + r).  vLLM GLM-5.3 serving post, footnote arithmetic: scores
 // over the 576-d key, values over the 512-d latent.
 //
-//   S^T [128 tokens x 16 rows]  = K [128 x 576] Q^T          (M = tokens, N = rows)
-//   O^T [512 dims x 16 rows]   += V^T [512 x 128] P^T         (M = dims,  N = rows)
+//   S^T [64 tokens x 16 rows]    = K [64 x 576] Q^T           (M = tokens, N = rows)
+//   O^T [512 dims x 16 rows]    += V^T [512 x 64] P^T          (M = dims,  N = rows)
 //
-// One CLUSTER of two CTAs streams one work unit at a time: a run of 128-token
-// tiles of one (request, shard).  CTA h = 0 owns key dims [0, 256), CTA 1 owns
-// [256, 576); each computes a partial S^T over its dims and the partials are
-// exchanged through distributed shared memory, so both CTAs hold the same
-// scores.  The latent dims a CTA owns are its half of the value dims.
+// Every CTA works alone on 64-token tiles over all 576 key dims, so no partial score
+// crosses between SMs.  The score MMA has M = 64: its rows land in TMEM lanes 0-15 of
+// each 32-lane quarter (row r at lane 32 (r / 16) + r % 16).
 //
-// The grid is persistent: the 128-token tiles of all (request, shard) items form one
-// sequence, and cluster k of G takes the contiguous share [T k / G, T (k + 1) / G), so
-// every cluster streams the same amount of KV with as few item switches as possible.
+// The grid is persistent: the 64-token tiles of all (request, shard) items form one
+// sequence, and CTA k of G takes the contiguous share [T k / G, T (k + 1) / G), so
+// every CTA streams the same amount of KV with as few item switches as possible.
 // An item cut by a share boundary writes fp32 partials that a small second kernel
 // merges.
 //
 //   warp 0     TMA producer: Q^T of the unit (one 16-row box per 64-dim chunk),
-//              then 128-token KV tiles (one 4-D box per page box, all of the CTA's
-//              chunks) into a 2-deep stage ring, and L2 prefetches of the tiles a few
+//              then 64-token KV tiles (one 4-D box per page box, all nine chunks)
+//              into a 2-deep stage ring, and L2 prefetches of the tiles a few
 //              places further on, so that the ring's loads mostly hit L2.
-//   warp 1     issues the QK MMAs (one elected lane of the converged warp): M 128,
+//   warp 1     issues the QK MMAs (one elected lane of the converged warp): M 64,
 //              N 16.  QK may run ahead of PV: a score buffer is free once the softmax
 //              has loaded it.
-//   warps 2-9  softmax, one thread per token lane, two warpgroups of 8 query
-//              rows each: base-2 online softmax with a lazily moved per-row
-//              reference max, P^T to shared memory, unit epilogue.
-//   warp 10    lane 0 relays "exchange buffer read" to the peer.
-//   warp 11    issues the PV MMAs (one elected lane): M 128 (V^T MN-major), N 32 =
-//              P as a bf16 hi part (rows 0-15) and lo part (rows 16-31).
+//   warps 2-9  softmax, two warpgroups of 8 query rows each; in each warp lanes 0-15
+//              hold the quarter's 16 tokens: base-2 online softmax with a lazily moved
+//              per-row reference max, P^T to shared memory, unit epilogue (one value
+//              dim per lane).
+//   warp 10    issues the PV MMAs (one elected lane): M 128 (V^T MN-major, four
+//              value blocks), N 32 = P as a bf16 hi part (rows 0-15) and lo part
+//              (rows 16-31).
 //
-// TMEM columns: S^T double buffer [0, 32), O^T double buffer (by unit) [64, 192):
-// buffer o, value block m (128 dims): hi rows at 64 + 64o + 32m, lo rows 16 later.
+// TMEM columns: S^T double buffer [0, 32), O^T double buffer (by unit) [64, 320):
+// buffer o, value block m (128 dims): hi rows at 64 + 128o + 32m, lo rows 16 later.
 // Every mbarrier wait is bounded; a timeout sets DCPMLA_DERR_TIMEOUT, all roles
-// drain, both CTAs meet at the final cluster barrier, TMEM is freed.
+// drain, TMEM is freed.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -56,41 +55,39 @@ namespace {
 using namespace sm100;
 
 constexpr int kMaxFhShards = 8;
-constexpr int kTok = 128;                      // tokens per tile = MMA M of the score product
+constexpr int kTok = 64;                       // tokens per tile = MMA M of the score product
 constexpr int kRp = 16;                        // query rows per tile (MMA N); rows >= R are padding
-constexpr int kChunk = kTok * 128;             // one 64-dim column chunk of a tile: 16 KB
-constexpr int kStage = 5 * kChunk;             // room for CTA 1's five chunks
+constexpr int kNck = 9;                        // 64-dim column chunks of a 576-dim key row
+constexpr int kChunk = kTok * 128;             // one 64-dim column chunk of a tile: 8 KB
+constexpr int kStage = kNck * kChunk;          // 72 KB
 // A stage is row-group major: [8-token group g][chunk c][8 tokens x 128 B], each 1 KB piece a
 // 128-byte-swizzle atom, so one 4-D TMA box lands all of a page box's chunks; for the MMAs the
-// 8-token groups of a chunk are nck KB apart and a chunk's groups start c KB in.
+// 8-token groups of a chunk are 9 KB apart and a chunk's groups start c KB in.
 constexpr int kStages = 2;
 constexpr int kLook = 3;                       // page-id lookahead (tiles); L2 prefetch kLook - 1 ahead
 constexpr int kQChunk = kRp * 128;             // Q^T chunk [16 rows x 64 dims]
-constexpr int kQBuf = 5 * kQChunk;
-constexpr int kPChunk = 2 * kRp * 128;         // P^T chunk [32 rows (hi, lo) x 64 tokens]
-constexpr int kPBuf = 2 * kPChunk;             // 128 tokens
-constexpr int kXBytes = kTok * kRp * 4;        // one fp32 partial S^T tile
+constexpr int kQBuf = kNck * kQChunk;
+constexpr int kPBuf = kTok * 64;               // P^T of a tile: a 64-byte line (32 rows) per token
 constexpr int kMaxItems = 2048;                // (request, shard) pairs per launch
+constexpr int kMaxCtas = 160;                  // CTAs of the persistent grid
 constexpr int kSoftmaxThreads = 256;
-constexpr int kRelayWarp = 10;
-constexpr int kPvWarp = 11;
+constexpr int kPvWarp = 10;
 constexpr int kThreads = 32 * (kPvWarp + 1);
-constexpr uint32_t kColS = 0, kColO = 64, kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColO = 64, kTmemCols = 512;
 
 constexpr int kOffKV = 0;
 constexpr int kOffQ = kOffKV + kStages * kStage;
 constexpr int kOffP = kOffQ + 2 * kQBuf;
-constexpr int kOffX = kOffP + 2 * kPBuf;
-constexpr int kOffPre = kOffX + kXBytes;
+constexpr int kOffPre = kOffP + 2 * kPBuf;
 constexpr size_t kSmemBytes = 1024 + kOffPre + (kMaxItems + 1) * 4;
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffX % 1024 == 0, "1 KB aligned buffers");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffPre % 1024 == 0, "1 KB aligned buffers");
 
 struct FhParams {
-  CUtensorMap tm_kv[2][kMaxFhShards];   // [CTA] pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, nck, box_rows / 8}
+  CUtensorMap tm_kv[kMaxFhShards];   // pool as {64, 8, 9 chunks, rows / 8}, box {64, 8, 9, box_rows / 8}
   CUtensorMap tm_q;                  // Q as [B * R, 576] bf16, box {64, 16}
   DecodeArgs a;
   int32_t box_rows;                  // rows per TMA box: gcd(P, 16)
-  float* ws_o;                       // [slots, R, 512]: slot item + cluster
+  float* ws_o;                       // [slots, R, 512]: slot item + CTA
   float* ws_lse;                     // [slots, R] (base 2)
   int32_t* ws_bad;                   // [slots]: the unit needed a page outside the pools
   int32_t* ws_pre;                   // [B * shard_count + 1]: first tile of each (request, shard)
@@ -99,22 +96,21 @@ struct FhParams {
 };
 static_assert(sizeof(FhParams) <= 4096, "kernel parameter space");
 
-
 // Tokens of request b on shard r (0 for a length the launch rejects).
 __device__ __forceinline__ int shard_tokens(const DecodeArgs& a, int L, int r) {
   if (L < a.Tq || (int64_t)L > (int64_t)a.max_pages * a.P * a.c) return 0;
   return shard_len(L, r, a.c, a.I);
 }
 
-// Work split.  All (request, shard) items' 128-token tiles form one sequence of T
-// tiles; cluster k of G takes tiles [T k / G, T (k + 1) / G), so every cluster streams
+// Work split.  All (request, shard) items' 64-token tiles form one sequence of T
+// tiles; CTA k of G takes tiles [T k / G, T (k + 1) / G), so every CTA streams
 // the same amount of KV.  A unit is the part of one item inside a cluster's share: an
 // item inside one share is written straight to the output, the others to workspace
 // slot item + k (unique: a later cluster starts at the same or a later item) and a
 // merge kernel combines them.
 struct Unit {
   int item, b, sr, r, L;
-  int j0, j1, ntiles;   // shard-local token range and its 128-token tiles
+  int j0, j1, ntiles;   // shard-local token range and its 64-token tiles
   int slot;             // workspace slot of its partial
   bool whole;           // every tile of the item: no merge
 };
@@ -159,8 +155,7 @@ __device__ __forceinline__ int fh_cluster_of(int T, int t, int G) {
 
 // kRL: waits give up after the launch's wait_kcycles instead of the fixed limit (tests only)
 template <bool kRL>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_fh_bf16_kernel(const __grid_constant__ FhParams p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_fh_bf16_kernel(const __grid_constant__ FhParams p) {
   const DecodeArgs& a = p.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -168,12 +163,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sKV = smem + kOffKV;
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sP = smem + kOffP;
-  uint8_t* sX = smem + kOffX;
   int* sPre = reinterpret_cast<int*>(smem + kOffPre);
   __shared__ uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ uint64_t bar_q_full[2], bar_q_free[2];
   __shared__ uint64_t bar_s_full[2], bar_s_free[2], bar_p_full[2], bar_p_free[2], bar_o_free[2], bar_o_full[2];
-  __shared__ uint64_t bar_x_full, bar_x_empty, bar_x_read;
   __shared__ uint64_t bar_o, bar_drain;
   __shared__ __align__(16) float red_s[2][2][4][8];     // [tile parity][warpgroup][quarter][row]
   __shared__ __align__(16) float lsum_s[2][2][4][8];   // [unit parity][warpgroup][quarter][row]
@@ -183,10 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ WaitCtl wctl_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t h = cluster_ctarank();
-  const uint32_t peer = h ^ 1u;
-  const int nck = h ? 5 : 4;
-  const int G = (int)(gridDim.x >> 1), cl = (int)(blockIdx.x >> 1);
+  const int G = (int)gridDim.x, cl = (int)blockIdx.x;
   const int nitems = a.B * a.shard_count;
   const int64_t R = a.R;
 
@@ -205,9 +195,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_o_free[s]), kSoftmaxThreads);
       mbar_init(smem_u32(&bar_o_full[s]), 1);
     }
-    mbar_init(smem_u32(&bar_x_full), 1);
-    mbar_init(smem_u32(&bar_x_empty), 1);                // the peer's relay thread
-    mbar_init(smem_u32(&bar_x_read), kSoftmaxThreads / 32);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 2);                  // both MMA issuers
     wctl_s.abort = 0;
@@ -242,10 +229,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 0) {
-    constexpr int kPer = kThreads / 32;
+    constexpr int kPer = (kThreads + 31) / 32;   // segments per lane (the tail lanes hold zeros)
     int tot = 0;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) tot += seg_s[lane * kPer + k];
+    for (int k = 0; k < kPer; ++k) {
+      const int q = lane * kPer + k;
+      tot += q < kThreads ? seg_s[q] : 0;
+    }
     int incl = tot;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -255,9 +245,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int run = incl - tot;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int v = seg_s[lane * kPer + k];
-      seg_s[lane * kPer + k] = run;
-      run += v;
+      const int q = lane * kPer + k;
+      if (q < kThreads) {
+        const int v = seg_s[q];
+        seg_s[q] = run;
+        run += v;
+      }
     }
   }
   __syncthreads();
@@ -272,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (blockIdx.x == 0)
     for (int it = tid; it <= nitems; it += kThreads) p.ws_pre[it] = sPre[it];
-  // this cluster's share of the tile sequence, and the items it meets
+  // this CTA's share of the tile sequence, and the items it meets
   const int T = sPre[nitems];
   const int t_lo = fh_bound(T, cl, G), t_hi = fh_bound(T, cl + 1, G);
   int it_lo = 0, it_hi = -1;
@@ -292,10 +285,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     it_hi = lo;
   }
-
-  // both CTAs' barriers are initialised before either touches the other's
-  cluster_arrive();
-  cluster_wait();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   volatile WaitCtl* abort_flag = &wctl_s;
@@ -304,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
-      for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[h][i]);
+      for (int i = 0; i < a.shard_count; ++i) prefetch_tmap(&p.tm_kv[i]);
     }
     bool ok = true;
     int gi = 0, kk = 0, issued = 0, q_issued = 0;
@@ -348,17 +337,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Unit x;
       if (!fh_unit(a, sPre, it, t_lo, t_hi, cl, x)) continue;
       const int qb = kk & 1;
-      const CUtensorMap* kvmap = &p.tm_kv[h][x.sr];
+      const CUtensorMap* kvmap = &p.tm_kv[x.sr];
       bool okq = true;
       if (lane == 0) {
         if (kk >= 2) okq = wait_bar<false, kRL>(smem_u32(&bar_q_free[qb]), ((kk >> 1) - 1) & 1, abort_flag);
         if (okq) {
           q_issued = kk + 1;
           const uint32_t qf = smem_u32(&bar_q_full[qb]);
-          mbar_arrive_expect_tx(qf, (uint32_t)(nck * kQChunk));
-          for (int c = 0; c < nck; ++c)
-            tma_load_2d(smem_u32(sQ + qb * kQBuf + c * kQChunk), &p.tm_q, (int)(4 * h + c) * 64,
-                        (int)(x.b * R), qf);
+          mbar_arrive_expect_tx(qf, (uint32_t)(kNck * kQChunk));
+          for (int c = 0; c < kNck; ++c)
+            tma_load_2d(smem_u32(sQ + qb * kQBuf + c * kQChunk), &p.tm_q, c * 64, (int)(x.b * R), qf);
         }
       }
       ok = __shfl_sync(0xffffffffu, (int)okq, 0) != 0;
@@ -384,24 +372,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, (int)okw, 0) != 0;
         if (!ok) break;
         const uint32_t full = smem_u32(&bar_kv_full[st]);
-        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * nck));
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(nbox * box * 128 * kNck));
         __syncwarp();
         if (lane < nbox) {
-          // the box's rows (whole 8-token groups) and this CTA's chunks in one copy
-          tma_load_4d(smem_u32(sKV + st * kStage + lane * (box >> 3) * nck * 1024), kvmap, 0, 0, (int)(4 * h), y >> 3,
-                      full);
+          // the box's rows (whole 8-token groups) and all nine chunks in one copy
+          tma_load_4d(smem_u32(sKV + st * kStage + lane * (box >> 3) * kNck * 1024), kvmap, 0, 0, 0, y >> 3, full);
         }
         issued = gi + 1;
         // L2 prefetch of the tile kLook - 1 places ahead: a box's rows are contiguous
-        // in the pool, and each CTA prefetches half of them
+        // in the pool
         if (fr[kLook - 1] > 0) {
           int g = fg[kLook - 1];
           if (g < 0 || (int64_t)g >= a.num_pages) g = 0;   // reported when the tile is loaded
           const int64_t py = (int64_t)g * a.P + fo[kLook - 1];
-          const uint32_t half = (uint32_t)fr[kLook - 1] * (kDK * 2 / 2);   // a multiple of 16 bytes
           const uint8_t* src =
               static_cast<const uint8_t*>(a.kv.pool[a.shard_begin + fs[kLook - 1]]) + py * (kDK * 2);
-          bulk_prefetch_l2(src + h * half, half);
+          bulk_prefetch_l2(src, (uint32_t)fr[kLook - 1] * (kDK * 2));   // a multiple of 16 bytes
         }
 #pragma unroll
         for (int k = 0; k + 1 < kLook; ++k) {
@@ -431,10 +417,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv = idesc_bf16(128, 2 * kRp, true, true);
     // Base descriptors; the start-address field is the low 14 bits (address >> 4),
     // so a constant byte offset is added as (offset >> 4) without carries.
-    const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, nck * 1024);      // keys, K-major
-    const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, nck * 1024);    // values, MN-major
-    const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);         // Q^T, K-major
-    const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);         // P^T, MN-major (32 rows per token)
+    const uint64_t kA0 = desc_sw128(smem_u32(sKV), 16, kNck * 1024);      // keys, K-major
+    const uint64_t vA0 = desc_sw128(smem_u32(sKV), 1024, kNck * 1024);    // values, MN-major
+    const uint64_t qB0 = desc_sw128(smem_u32(sQ), 16, 1024);              // Q^T, K-major
+    const uint64_t pB0 = desc_sw64(smem_u32(sP), 8192, 512);              // P^T, MN-major (32 rows per token)
     const bool qk_role = warp == 1;
     bool ok = true;
     int gt = 0, kk = 0;                  // tiles and units so far
@@ -455,8 +441,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d = tmem + kColS + (uint32_t)(sb * kRp);
 #pragma unroll
-          for (int c = 0; c < 5; ++c) {
-            if (c >= nck) break;
+          for (int c = 0; c < kNck; ++c) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_ss_warp(d, kA0 + (uint64_t)((sb * kStage + c * 1024 + k * 32) >> 4),
@@ -475,11 +460,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            const uint32_t d = tmem + kColO + (uint32_t)(ob * 64 + mb * 32);
+          for (int mb = 0; mb < 4; ++mb) {
+            const uint32_t d = tmem + kColO + (uint32_t)(ob * 128 + mb * 32);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * nck * 1024) >> 4);
+            for (int ks = 0; ks < kTok / 16; ++ks) {
+              const uint64_t ad = vA0 + (uint64_t)((sb * kStage + 2 * mb * 1024 + ks * 2 * kNck * 1024) >> 4);
               const uint64_t bd = pB0 + (uint64_t)((sb * kPBuf + ks * 1024) >> 4);
               mma_ss_warp(d, ad, bd, idesc_pv, (i == 0 && ks == 0) ? 0u : 1u);
             }
@@ -499,29 +484,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const long long t0 = clock64();
     while (!mbar_try_wait(smem_u32(&bar_drain), 0) && clock64() - t0 < kDrainCycles) {
     }
-  } else if (warp == kRelayWarp) {
-    if (lane == 0) {
-      // relay: once all softmax warps have read the peer's partial for a tile,
-      // tell the peer its next partial may overwrite this CTA's exchange buffer
-      const int total = t_hi - t_lo;   // the cluster's share of tiles
-      const uint32_t xe_peer = map_to_rank(smem_u32(&bar_x_empty), peer);
-      for (int gi = 0; gi < total; ++gi) {
-        if (!wait_bar<false, kRL>(smem_u32(&bar_x_read), gi & 1, abort_flag)) break;
-        mbar_arrive_remote(xe_peer);
-      }
-    }
   } else {
     // -------------------------------------------------------------- softmax
-    // Warps 2..9: warpgroup g handles query rows [8g, 8g + 8); the thread's TMEM
-    // lane is its token within the tile (for S^T) and its value dim (for O^T).
+    // Warps 2..9: warpgroup g handles query rows [8g, 8g + 8).  For S^T (M = 64) lanes
+    // 0-15 of warp quarter q hold tokens 16q + lane; for O^T (M = 128) every lane holds
+    // value dim 32q + lane of each block.
     const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
-    const int tok = quarter * 32 + lane;
-    const int stid = g * 128 + tok;                          // 0..255
+    const bool live = lane < 16;                             // a token lane of the score tile
+    const int tok = quarter * 16 + (lane & 15);              // its token within the tile
+    const int dl = quarter * 32 + lane;                      // its value dim within a block
+    const int stid = g * 128 + dl;                           // 0..255
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
-    const uint32_t x_remote = map_to_rank(smem_u32(sX), peer);
-    const uint32_t xfull_remote = map_to_rank(smem_u32(&bar_x_full), peer);
     bool ok = true;
     int gi = 0, kk = 0, uc = 0;
     for (int it = it_lo; ok && it <= it_hi; ++it) {
@@ -551,9 +526,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int sb = gi & 1;
         const int t0 = x.j0 + i * kTok;
         const int ntok = min(kTok, x.j1 - t0);
+        const bool in_tile = live && tok < ntok;
         // this thread's page id, checked at the end of the tile (its load is in
         // flight meanwhile)
-        const int gpg = tok < ntok ? __ldg(pt_row + (t0 + tok) / a.P) : 0;
+        const int gpg = in_tile ? __ldg(pt_row + (t0 + tok) / a.P) : 0;
         // A failed wait does not leave the loop at once: every warp of the warpgroup goes on
         // to the warpgroup's barrier-OR below, skipping the work of the failed steps.  A named
         // barrier has no time limit, so all of its threads must reach it: the softmax warps
@@ -570,54 +546,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
         }
-        // exchange the partial with the peer: [warpgroup][4-row unit][token] of 16 B
-        if (ok && gi >= 1)
-          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_empty), (gi - 1) & 1, abort_flag));
-        if (ok) {
-#pragma unroll
-          for (int v = 0; v < 2; ++v)
-            st_async_v4(x_remote + (uint32_t)(((2 * g + v) * kTok + tok) * 16),
-                        make_uint4(own[4 * v], own[4 * v + 1], own[4 * v + 2], own[4 * v + 3]), xfull_remote);
-          if (stid == 0) mbar_arrive_expect_tx(smem_u32(&bar_x_full), kXBytes);
-          ok = __all_sync(0xffffffffu, wait_bar<true, kRL>(smem_u32(&bar_x_full), gi & 1, abort_flag));
-        }
-        // the warpgroup leaves the loop together if any of its warps failed a wait
-        if (named_bar_or(1 + g, 128, !ok)) {
-          ok = false;
-          break;
-        }
-        float s[8];
-#pragma unroll
-        for (int v = 0; v < 2; ++v) {
-          const float4 pv = reinterpret_cast<const float4*>(sX)[(2 * g + v) * kTok + tok];
-          const float o0 = __uint_as_float(own[4 * v]), o1 = __uint_as_float(own[4 * v + 1]);
-          const float o2 = __uint_as_float(own[4 * v + 2]), o3 = __uint_as_float(own[4 * v + 3]);
-          // the sum is taken as (CTA 0 part) + (CTA 1 part) in both CTAs
-          s[4 * v + 0] = h ? pv.x + o0 : o0 + pv.x;
-          s[4 * v + 1] = h ? pv.y + o1 : o1 + pv.y;
-          s[4 * v + 2] = h ? pv.z + o2 : o2 + pv.z;
-          s[4 * v + 3] = h ? pv.w + o3 : o3 + pv.w;
-        }
-        // this warp has read the peer's partial (the relay tells the peer)
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_x_read));
         // causal / tail / padding-row mask, base-2 scaling
         const bool full_vis = all_rows && ntok == kTok && shard_pos(t0 + kTok - 1, x.r, a.c, a.I) <= qpos_min;
         const int64_t kpos = shard_pos(t0 + tok, x.r, a.c, a.I);
+        float s[8];
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-          const bool vis = full_vis || (rvalid[n] && tok < ntok && kpos <= qpos[n]);
-          s[n] = vis ? s[n] * qscale : -INFINITY;
+          const bool vis = live && (full_vis || (rvalid[n] && in_tile && kpos <= qpos[n]));
+          s[n] = vis ? __uint_as_float(own[n]) * qscale : -INFINITY;
         }
         // Lazy reference max: a row moves it only when this tile's max exceeds it
         // by more than 8 (every weight 2^(s - m_ref) stays <= 256); rows that move
         // it after O holds data rescale their O^T columns and partial sums.  Whether
-        // any row of the warpgroup moves is one barrier-OR; only then is the tile's
-        // exact per-row max formed (warp reduction, then across the 4 warps).
-        bool over = false;
+        // any row of the warpgroup moves (or any of its warps failed a wait) is one
+        // barrier-OR; only then is the tile's exact per-row max formed (warp
+        // reduction, then across the 4 warps).
+        bool over = !ok;
 #pragma unroll
         for (int n = 0; n < 8; ++n) over |= s[n] > m_ref[n] + 8.f;
         if (named_bar_or(1 + g, 128, over)) {
+          // the warpgroup leaves the loop together if any of its warps failed a wait
+          if (named_bar_or(1 + g, 128, !ok)) {
+            ok = false;
+            break;
+          }
           float wm[8];
 #pragma unroll
           for (int n = 0; n < 8; ++n) wm[n] = warp_max_f32(s[n]);
@@ -663,11 +615,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (ok) {
               tc_fence_after();
 #pragma unroll
-              for (int mb = 0; mb < 2; ++mb) {
+              for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {   // hi rows, then lo rows
                   const uint32_t col =
-                      tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + part * 16 + 8 * g);
+                      tmem + lane_off + kColO + (uint32_t)(ob * 128 + mb * 32 + part * 16 + 8 * g);
                   uint32_t v[8];
                   tmem_ld8(col, v);
                   tmem_ld_wait();
@@ -704,19 +656,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           lp[n >> 1] = *reinterpret_cast<const uint32_t*>(&ll);
         }
         if (ok) {
-          {
+          if (live) {
             uint8_t* line = sP + sb * kPBuf + (tok >> 3) * 512 + (tok & 7) * 64;
             const int sw = (tok & 7) >> 1;
             *reinterpret_cast<uint4*>(line + ((g ^ sw) << 4)) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
             *reinterpret_cast<uint4*>(line + (((2 + g) ^ sw) << 4)) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
           }
           if (ntok < kTok) {
-            // rows past the unit's last token hold stale data: zero this CTA's V rows
+            // rows past the unit's last token hold stale data: zero their value chunks
             uint4* v = reinterpret_cast<uint4*>(sKV + sb * kStage);
             const int tail = kTok - ntok;
-            for (int e = stid; e < 4 * tail * 8; e += kSoftmaxThreads) {
+            for (int e = stid; e < 8 * tail * 8; e += kSoftmaxThreads) {
               const int cch = e / (tail * 8), rem = e % (tail * 8), t = ntok + rem / 8;
-              v[((t >> 3) * nck * 1024 + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
+              v[((t >> 3) * kNck * 1024 + cch * 1024 + (t & 7) * 128) / 16 + rem % 8] = make_uint4(0, 0, 0, 0);
             }
           }
           fence_proxy_async();
@@ -746,7 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (bad) ubad_s[up][g] = uc + 1;
       named_bar_sync(1 + g, 128);
       const bool unit_bad = ubad_s[up][g] == uc + 1;
-      // row sums over the 128 token lanes: warp butterfly, then the 4 warps in order
+      // row sums over the token lanes: warp butterfly, then the 4 warps in order
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
         float v = lt[n];
@@ -771,10 +723,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int64_t orow0 = direct ? ((int64_t)x.sr * a.B + x.b) * R : (int64_t)x.slot * R;
       float* obase = direct ? a.o_part : p.ws_o;
 #pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
+      for (int mb = 0; mb < 4; ++mb) {
         uint32_t hv[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (x.ntiles > 0 && ok) {
-          const uint32_t col = tmem + lane_off + kColO + (uint32_t)(ob * 64 + mb * 32 + 8 * g);
+          const uint32_t col = tmem + lane_off + kColO + (uint32_t)(ob * 128 + mb * 32 + 8 * g);
           tmem_ld8(col, hv);
           tmem_ld8(col + 16, lv);
           tmem_ld_wait();
@@ -785,10 +737,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (row >= R) continue;
           const float val =
               (x.ntiles > 0 && !empty_out) ? (__uint_as_float(hv[n]) + __uint_as_float(lv[n])) * inv[n] : 0.f;
-          obase[(orow0 + row) * kDL + h * 256 + mb * 128 + tok] = val;
+          obase[(orow0 + row) * kDL + mb * 128 + dl] = val;
         }
       }
-      if (h == 0 && quarter == 0 && lane == 0) {
+      if (quarter == 0 && lane == 0) {
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
           const int row = 8 * g + n;
@@ -804,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ++kk;
       }
       // a split item's units are merged by the combine kernel; it also reads this flag
-      if (!direct && h == 0 && stid == 0) p.ws_bad[x.slot] = unit_bad ? 1 : 0;
+      if (!direct && stid == 0) p.ws_bad[x.slot] = unit_bad ? 1 : 0;
       ++uc;
       // the unit loop's condition must agree in every thread of the warpgroup
       if (named_bar_or(1 + g, 128, !ok)) ok = false;
@@ -824,13 +776,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // the peer may still be writing into this CTA's exchange buffer or barriers
-  cluster_arrive();
-  cluster_wait();
+  __syncthreads();
   if (wctl_s.abort && tid == 0) set_err(a.err, DCPMLA_DERR_TIMEOUT);
 }
 
-// Merge of the (request, shard) items split between clusters: one block per (item,
+// Merge of the (request, shard) items split between CTAs: one block per (item,
 // query row), 128 threads x 4 value dims.  The exact LSE merge of the partials (base 2):
 // lse = log2 sum_k 2^lse_k, o = sum_k 2^(lse_k - lse) o_k.  An item with no tiles (an
 // empty shard or a rejected length) is written as empty, and so is one any partial of
@@ -888,7 +838,7 @@ __global__ void __launch_bounds__(128) fh_combine_kernel(const DecodeArgs a, con
 // units' LSEs, then a warp max and sum); the block's 128 threads then form the weighted sums,
 // 4 dims each.  A shard any unit of which needed a bad page is left out, as the unfused path
 // writes it as empty (lse = -inf).
-constexpr int kMergeParts = kMaxFhShards + 88;        // shards + cluster boundaries in a request
+constexpr int kMergeParts = kMaxFhShards + kMaxCtas;  // shards + share boundaries in a request
 
 __global__ void __launch_bounds__(128) fh_merge_all_kernel(const DecodeArgs a, const int32_t* __restrict__ pre,
                                                            int G, const float* __restrict__ ws_o,
@@ -982,7 +932,7 @@ __global__ void __launch_bounds__(128) fh_merge_all_kernel(const DecodeArgs a, c
 }
 
 struct FhPlan {
-  int32_t clusters, slots;
+  int32_t ctas, slots;
   size_t pre_off, bad_off, lse_off, o_off, bytes;
 };
 
@@ -991,12 +941,12 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
   FhPlan p{};
   const int64_t items = (int64_t)a.B * a.shard_count;
-  // one cluster per SM pair, but no more clusters than tiles can exist: a shard holds at most
-  // max_pages * P of a request's tokens (small problems then launch few clusters and the
+  // one CTA per SM, but no more CTAs than tiles can exist: a shard holds at most
+  // max_pages * P of a request's tokens (small problems then launch few CTAs and the
   // combine walks few shares)
   const int64_t tiles_max = items * (((int64_t)a.max_pages * a.P + kTok - 1) / kTok);
-  p.clusters = (int32_t)std::max<int64_t>(1, std::min<int64_t>(sm_count / 2, tiles_max));
-  p.slots = (int32_t)(items + p.clusters);   // partial of item it in cluster k: slot it + k
+  p.ctas = (int32_t)std::max<int64_t>(1, std::min<int64_t>(std::min(sm_count, kMaxCtas), tiles_max));
+  p.slots = (int32_t)(items + p.ctas);   // partial of item it in CTA k: slot it + k
   p.pre_off = 0;
   p.bad_off = align256((size_t)(items + 1) * 4);
   p.lse_off = p.bad_off + align256((size_t)p.slots * 4);
@@ -1008,7 +958,7 @@ FhPlan plan_fh(const DecodeArgs& a, int sm_count) {
 }  // namespace
 
 bool fh_supported(const DecodeArgs& a, int sm_count) {
-  if (a.fp8 || a.R > kRp || sm_count < 2) return false;
+  if (a.fp8 || a.R > kRp || sm_count < 1) return false;
   if (a.shard_count > kMaxFhShards) return false;
   if (a.P % 8 != 0) return false;   // page boxes of gcd(P, 16) rows: whole 8-token groups
   if ((int64_t)a.B * a.shard_count > kMaxItems) return false;
@@ -1039,10 +989,9 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
     p.box_rows = std::gcd(a.P, 16);
     p.fused = fused ? 1 : 0;
     rc = tma_encode_bf16_2d(&p.tm_q, a.q, (uint64_t)kDK, (uint64_t)a.B * a.R, 64, kRp);
-    for (int hh = 0; hh < 2; ++hh)
-      for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
-        rc = tma_encode_kv_rowgroups(&p.tm_kv[hh][i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows,
-                                     hh ? 5u : 4u, (uint32_t)p.box_rows / 8);
+    for (int i = 0; rc == DCPMLA_OK && i < a.shard_count; ++i)
+      rc = tma_encode_kv_rowgroups(&p.tm_kv[i], a.kv.pool[a.shard_begin + i], (uint64_t)a.pool_rows, (uint32_t)kNck,
+                                   (uint32_t)p.box_rows / 8);
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.ws_pre = reinterpret_cast<int32_t*>(w + plan.pre_off);
     p.ws_bad = reinterpret_cast<int32_t*>(w + plan.bad_off);
@@ -1057,16 +1006,16 @@ int launch_decode_fh(const DecodeArgs& a, void* ws, size_t ws_bytes, int sm_coun
   const auto kern = p.wait_kcycles == kDefaultWaitKcycles ? decode_fh_bf16_kernel<false> : decode_fh_bf16_kernel<true>;
   rc = ensure_smem_attr((const void*)kern, (int)kSmemBytes);
   if (rc == DCPMLA_OK) {
-    kern<<<2 * plan.clusters, kThreads, kSmemBytes, st>>>(p);
+    kern<<<plan.ctas, kThreads, kSmemBytes, st>>>(p);
     rc = launch_status();
   }
   if (rc == DCPMLA_OK && fused) {
-    fh_merge_all_kernel<<<dim3((unsigned)a.B, (unsigned)a.R), 128, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o,
+    fh_merge_all_kernel<<<dim3((unsigned)a.B, (unsigned)a.R), 128, 0, st>>>(a, p.ws_pre, plan.ctas, p.ws_o,
                                                                            p.ws_lse, p.ws_bad);
     rc = launch_status();
   } else if (rc == DCPMLA_OK) {
     const dim3 grid((unsigned)(a.B * a.shard_count), (unsigned)a.R);
-    fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, plan.clusters, p.ws_o, p.ws_lse, p.ws_bad);
+    fh_combine_kernel<<<grid, 128, 0, st>>>(a, p.ws_pre, plan.ctas, p.ws_o, p.ws_lse, p.ws_bad);
     rc = launch_status();
   }
   return rc;
