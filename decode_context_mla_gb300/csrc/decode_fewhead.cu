@@ -547,13 +547,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fh_bf16_kernel(const __gri
           if (lane == 0) mbar_arrive(smem_u32(&bar_s_free[sb]));
         }
         // causal / tail / padding-row mask, base-2 scaling
+        // (a tile every row sees whole, the common case, skips the per-token position)
         const bool full_vis = all_rows && ntok == kTok && shard_pos(t0 + kTok - 1, x.r, a.c, a.I) <= qpos_min;
-        const int64_t kpos = shard_pos(t0 + tok, x.r, a.c, a.I);
         float s[8];
+        if (full_vis) {
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          const bool vis = live && (full_vis || (rvalid[n] && in_tile && kpos <= qpos[n]));
-          s[n] = vis ? __uint_as_float(own[n]) * qscale : -INFINITY;
+          for (int n = 0; n < 8; ++n) s[n] = live ? __uint_as_float(own[n]) * qscale : -INFINITY;
+        } else {
+          const int64_t kpos = shard_pos(t0 + tok, x.r, a.c, a.I);
+#pragma unroll
+          for (int n = 0; n < 8; ++n) {
+            const bool vis = live && rvalid[n] && in_tile && kpos <= qpos[n];
+            s[n] = vis ? __uint_as_float(own[n]) * qscale : -INFINITY;
+          }
         }
         // Lazy reference max: a row moves it only when this tile's max exceeds it
         // by more than 8 (every weight 2^(s - m_ref) stays <= 256); rows that move
@@ -635,9 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fh_bf16_kernel(const __gri
           }
         }
         // P^T as bf16 hi (rows 0-15) + lo (rows 16-31); one bf16 rounding of the
-        // weights alone would cost ~1e-3 relative error in O
-        if (ok && gi >= 2)
-          ok = __all_sync(0xffffffffu, wait_bar<false, kRL>(smem_u32(&bar_p_free[sb]), ((gi >> 1) - 1) & 1, abort_flag));
+        // weights alone would cost ~1e-3 relative error in O.  P buffer sb was last read
+        // by PV(gi - 2), which had completed before this tile's KV load was issued (the
+        // load waited for that PV's commit on the stage's empty barrier), and this
+        // tile's scores come after that load: no wait is needed here.
         // P^T is MN-major with a 64-byte swizzle: a token's 32 rows (hi 0-15, lo 16-31) are
         // one 64-byte line, 8 tokens an atom; this thread's 8 hi and 8 lo rows are one
         // 16-byte unit each (unit u of line t sits at u ^ ((t % 8) / 2))
