@@ -61,9 +61,13 @@ SMALL = {
     "fh_p128": W.Workload("fhp", B=2, H=16, Tq=1, c=2, P=128, kv_dtype="bf16", lse_base="2",
                           seed=20, L=3001),
     "fh_chunked": W.scaled(W.WORKLOADS["long"], B=2, L=300000),
-    # page sizes above the 128-token tile and between the tested ones: the token-major kernel
-    # copies a page box of gcd(P, 16) rows (whole 8-token groups) for all of a CTA's chunks at
-    # once, so a box never crosses a page or a tile (P = 24 and P = 40: sixteen boxes a tile)
+    # a few tiles per CTA of the persistent grid: most (request, shard) items are cut by share
+    # boundaries, many units hold one 64-token tile, 8-token pages (eight page boxes a tile)
+    "fh_many_cuts": W.Workload("fhm", B=24, H=16, Tq=1, c=2, P=8, kv_dtype="bf16", lse_base="e",
+                               seed=37, lengths_mix=(8, 2000, 6000, 1, 300)),
+    # page sizes above the 64-token tile and between the tested ones: the token-major kernel
+    # copies a page box of gcd(P, 16) rows (whole 8-token groups) for all nine chunks at once,
+    # so a box never crosses a page or a tile (P = 24 and P = 40: eight boxes a tile)
     "fh_p256": W.Workload("fh256", B=2, H=16, Tq=1, c=2, P=256, kv_dtype="bf16", lse_base="e",
                           seed=23, L=2333),
     "fh_p32_tq4": W.Workload("fh32", B=3, H=4, Tq=4, c=4, P=32, kv_dtype="bf16", lse_base="2",
@@ -315,7 +319,7 @@ def test_decode_path_per_workload():
         assert got == (B.PATH_CUDA_CORE, 1), name
     # page sizes that are multiples of 8 but neither divide nor are divided by the tile stay on
     # the token-major kernel (page boxes of gcd(P, 16) rows)
-    for name in ("fh_p24_c3", "fh_p40_tq2", "fh_p256", "fh_short_p8"):
+    for name in ("fh_p24_c3", "fh_p40_tq2", "fh_p256", "fh_short_p8", "fh_many_cuts"):
         w = SMALL[name]
         got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
         assert got == (B.PATH_TC_FEWHEAD, 2), name
@@ -325,7 +329,8 @@ def test_decode_path_per_workload():
 FUSED_CASES = ["tiny", "dsv3_s", "long_s", "bimodal_s", "fp8_s", "c1", "c3_p5_tq2", "c16_short",
                "fma_e4m3_c16_tq4", "fma_e4m3_c3_p5", "tc_r96_c3", "tc_c2_cut",
                "dsv3_split", "h64_tq2_p16", "fh_tq2_c3", "fh_short_p8", "fh_chunked", "ilv4_dsv3",
-               "ilv2_c16", "tc_p8_c3", "tc_p256_tq4", "tc_e4m3_p8", "ilv8_fp8", "fp8_h16_tq4", "fh_p24_c3"]
+               "ilv2_c16", "tc_p8_c3", "tc_p256_tq4", "tc_e4m3_p8", "ilv8_fp8", "fp8_h16_tq4", "fh_p24_c3",
+               "fh_many_cuts"]
 
 
 @needs_cuda
