@@ -229,15 +229,25 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// HiCache index filter: order-preserving compaction in three launches.
+// HiCache index filter: order-preserving compaction in one pass (a chained scan with
+// decoupled look-back: Merrill and Garland, "Single-pass Parallel Prefix Scan with
+// Decoupled Look-back", NVIDIA technical report NVR-2016-002).
 // ---------------------------------------------------------------------------
-constexpr int kFilterBlock = 1024;   // indices per block (256 threads x 4)
+constexpr int kFilterWarps = 8;
+constexpr int kFilterRounds = 16;                                  // 32-index rounds per warp
+constexpr int kFilterBlock = kFilterWarps * kFilterRounds * 32;    // 4096 indices per block
+// A block's status word: flag in bits 62-63 (0 not yet, 1 its own count, 2 the inclusive
+// count of every block up to it), the count in bits 0-61.
+constexpr uint64_t kStatAgg = 1ull << 62, kStatInc = 2ull << 62, kStatVal = (1ull << 62) - 1;
+constexpr long long kLookbackSpins = 1ll << 22;                     // per predecessor window
 
-// owner and local slot of widened-page slot i (i >= 0); 32-bit division when i fits
-__device__ __forceinline__ void owner_local(int64_t i, int32_t c, int32_t I, int32_t& own, int64_t& loc) {
+// owner and local slot of widened-page slot i (i >= 0); 32-bit division when i fits, and a
+// shift and a mask when c is a power of two (cs = log2 c, else -1)
+__device__ __forceinline__ void owner_local(int64_t i, int32_t c, int32_t cs, int32_t I, int32_t& own, int64_t& loc) {
   if ((uint64_t)i <= 0xFFFFFFFFull) {
-    const uint32_t u = (uint32_t)i, q = I == 1 ? u : u / (uint32_t)I, w = q / (uint32_t)c;
-    own = (int32_t)(q - w * (uint32_t)c);
+    const uint32_t u = (uint32_t)i, q = I == 1 ? u : u / (uint32_t)I;
+    const uint32_t w = cs >= 0 ? q >> cs : q / (uint32_t)c;
+    own = (int32_t)(cs >= 0 ? q & (uint32_t)(c - 1) : q - w * (uint32_t)c);
     loc = (int64_t)w * I + (u - q * (uint32_t)I);
   } else {
     const int64_t q = i / I, w = q / c;
@@ -245,93 +255,111 @@ __device__ __forceinline__ void owner_local(int64_t i, int32_t c, int32_t I, int
     loc = w * I + (i - q * I);
   }
 }
-__device__ __forceinline__ bool owned(int64_t i, int32_t c, int32_t I, int32_t rank) {
+__device__ __forceinline__ bool owned(int64_t i, int32_t c, int32_t cs, int32_t I, int32_t rank) {
   if (i < 0) return false;
   int32_t o;
   int64_t l;
-  owner_local(i, c, I, o, l);
+  owner_local(i, c, cs, I, o, l);
   return o == rank;
 }
 
-__global__ void __launch_bounds__(256) filter_count_kernel(const int64_t* __restrict__ idx, int64_t n, int32_t c,
-                                                           int32_t I, int32_t rank, uint32_t* counts,
-                                                           int32_t* err) {
-  __shared__ uint32_t warp_n[8];
-  const int64_t base = (int64_t)blockIdx.x * kFilterBlock;
-  uint32_t k = 0;
-  bool neg = false;
-  for (int e = threadIdx.x; e < kFilterBlock; e += 256) {
-    const int64_t i = base + e;
-    if (i >= n) break;
-    const int64_t v = __ldg(idx + i);
-    neg |= v < 0;
-    k += owned(v, c, I, rank) ? 1u : 0u;
-  }
-  if (neg) set_err(err, DCPMLA_DERR_POSITION);
-  k = __reduce_add_sync(0xffffffffu, k);
-  if ((threadIdx.x & 31) == 0) warp_n[threadIdx.x >> 5] = k;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t t = 0;
-    for (int w = 0; w < 8; ++w) t += warp_n[w];
-    counts[blockIdx.x] = t;
-  }
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
 }
 
-// Exclusive scan of the block counts in place (one block); the total goes to *count.
-__global__ void __launch_bounds__(1024) filter_scan_kernel(uint32_t* counts, int64_t nblocks, int64_t* count) {
-  __shared__ uint32_t part[1024];
-  const int t = threadIdx.x;
-  const int64_t per = (nblocks + 1023) / 1024;
-  const int64_t b0 = min(nblocks, (int64_t)t * per), b1 = min(nblocks, b0 + per);
-  uint32_t s = 0;
-  for (int64_t b = b0; b < b1; ++b) s += counts[b];
-  part[t] = s;
-  __syncthreads();
-  for (int d = 1; d < 1024; d <<= 1) {   // inclusive Hillis-Steele scan of the parts
-    const uint32_t v = t >= d ? part[t - d] : 0u;
-    __syncthreads();
-    part[t] += v;
-    __syncthreads();
-  }
-  uint32_t run = part[t] - s;
-  for (int64_t b = b0; b < b1; ++b) {
-    const uint32_t v = counts[b];
-    counts[b] = run;
-    run += v;
-  }
-  if (t == 1023) *count = (int64_t)part[1023];
-}
-
-__global__ void __launch_bounds__(256) filter_scatter_kernel(const int64_t* __restrict__ idx, int64_t n, int32_t c,
-                                                             int32_t I, int32_t rank,
-                                                             const uint32_t* __restrict__ offsets,
-                                                             int64_t* __restrict__ out) {
-  __shared__ uint32_t warp_n[8];
-  const int64_t base = (int64_t)blockIdx.x * kFilterBlock;
+// One pass over the list.  Blocks take tiles in the order they start (a ticket), so a block
+// waits only for blocks already running.  Each warp takes 512 consecutive indices (16 rounds
+// of 32, in order); the block publishes its count, then warp 0 looks back over the status
+// words of the 32 tiles before it at a time, summing counts until a tile that already holds
+// its inclusive prefix, publishes its own inclusive prefix and the block writes its kept
+// slots there.  A look-back that waits past its limit sets DCPMLA_DERR_TIMEOUT (and the
+// outputs are invalid); it never blocks for good.
+__global__ void __launch_bounds__(kFilterWarps * 32) filter_onepass_kernel(
+    const int64_t* __restrict__ idx, int64_t n, int32_t c, int32_t cs, int32_t I, int32_t rank, uint64_t* status,
+    unsigned int* ticket, int64_t* __restrict__ out, int64_t* count, int32_t* err) {
+  __shared__ uint32_t warp_n[kFilterWarps];
+  __shared__ uint64_t prefix_s;
+  __shared__ int tile_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // each warp takes 128 consecutive indices (4 rounds of 32), in order
-  int64_t v[4];
-  bool keep[4];
-  uint32_t mine = 0;
+  if (threadIdx.x == 0) tile_s = (int)atomicAdd(ticket, 1u);
+  __syncthreads();
+  const int tile = tile_s;
+  const int64_t base = (int64_t)tile * kFilterBlock + warp * (kFilterRounds * 32);
+  int64_t v[kFilterRounds];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t i = base + warp * 128 + k * 32 + lane;
-    v[k] = i < n ? __ldg(idx + i) : -1;
-    keep[k] = i < n && owned(v[k], c, I, rank);
-    mine += __popc(__ballot_sync(0xffffffffu, keep[k]));
+  for (int k = 0; k < kFilterRounds; ++k) {
+    const int64_t i = base + k * 32 + lane;
+    v[k] = i < n ? __ldcs(idx + i) : -1;   // past the list: dropped, not reported
   }
+  uint32_t keep = 0, mine = 0;   // bit k: round k's index is kept
+  bool neg = false;
+#pragma unroll
+  for (int k = 0; k < kFilterRounds; ++k) {
+    neg |= v[k] < 0 && base + k * 32 + lane < n;
+    const bool kp = owned(v[k], c, cs, I, rank);
+    keep |= kp ? 1u << k : 0u;
+    mine += __popc(__ballot_sync(0xffffffffu, kp));
+  }
+  if (__any_sync(0xffffffffu, neg) && lane == 0) set_err(err, DCPMLA_DERR_POSITION);
   if (lane == 0) warp_n[warp] = mine;
   __syncthreads();
-  uint32_t pos = offsets[blockIdx.x];
+  if (warp == 0) {
+    uint32_t total = 0;
+#pragma unroll
+    for (int w = 0; w < kFilterWarps; ++w) total += warp_n[w];
+    uint64_t prefix = 0;
+    if (tile == 0) {
+      if (lane == 0) st_release_u64(status, kStatInc | total);
+    } else {
+      if (lane == 0) st_release_u64(status + tile, kStatAgg | total);
+      // look back in windows of 32 predecessors (lane l: tile - 1 - l), nearest first
+      int j = tile - 1;
+      bool timed_out = false;
+      while (j >= 0) {
+        const int t = j - lane;
+        uint64_t sw = t >= 0 ? ld_acquire_u64(status + t) : kStatInc;
+        long long spins = 0;
+        while (!__all_sync(0xffffffffu, (sw >> 62) != 0)) {
+          if (++spins > kLookbackSpins) {
+            timed_out = true;
+            break;
+          }
+          if ((sw >> 62) == 0) sw = ld_acquire_u64(status + t);
+        }
+        if (timed_out) break;
+        const uint32_t inc = __ballot_sync(0xffffffffu, (sw >> 62) == 2);
+        const int first = inc ? __ffs(inc) - 1 : 32;            // the nearest inclusive tile
+        uint64_t add = lane <= first ? (sw & kStatVal) : 0;
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) add += __shfl_xor_sync(0xffffffffu, add, d);
+        prefix += add;
+        if (inc) break;
+        j -= 32;
+      }
+      if (timed_out && lane == 0) set_err(err, DCPMLA_DERR_TIMEOUT);
+      if (lane == 0) st_release_u64(status + tile, kStatInc | (prefix + total));
+    }
+    if (lane == 0) {
+      prefix_s = prefix;
+      if ((int64_t)(tile + 1) * kFilterBlock >= n) *count = (int64_t)(prefix + total);   // the last tile
+    }
+  }
+  __syncthreads();
+  uint64_t pos = prefix_s;
   for (int w = 0; w < warp; ++w) pos += warp_n[w];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep[k]);
-    if (keep[k]) {
+  for (int k = 0; k < kFilterRounds; ++k) {
+    const bool kp = (keep >> k) & 1u;
+    const uint32_t bal = __ballot_sync(0xffffffffu, kp);
+    if (kp) {
       int32_t o;
       int64_t l;
-      owner_local(v[k], c, I, o, l);
+      owner_local(v[k], c, cs, I, o, l);
       out[pos + __popc(bal & ((1u << lane) - 1u))] = l;
     }
     pos += __popc(bal);
@@ -445,7 +473,7 @@ int dcpmla_kv_append_e4m3(void* const* pools, float* const* scale_pools, int64_t
 
 int dcpmla_hicache_filter_workspace_size(int64_t n, size_t* out) {
   if (n < 0 || !out) return DCPMLA_ERR_INVALID;
-  *out = (size_t)((n + kFilterBlock - 1) / kFilterBlock) * 4;
+  *out = (size_t)((n + kFilterBlock - 1) / kFilterBlock + 1) * 8;   // status words and the ticket
   return DCPMLA_OK;
 }
 
@@ -457,12 +485,14 @@ int dcpmla_hicache_filter(const int64_t* d_idx, int64_t n, int32_t c, int32_t in
   if (n == 0) return cudaMemsetAsync(d_count, 0, sizeof(int64_t), st) == cudaSuccess ? DCPMLA_OK : DCPMLA_ERR_CUDA;
   if (!d_idx || !d_out) return DCPMLA_ERR_INVALID;
   const int64_t nb = (n + kFilterBlock - 1) / kFilterBlock;
-  if ((size_t)nb * 4 > ws_bytes || !d_workspace) return DCPMLA_ERR_CAPACITY;
+  if ((size_t)(nb + 1) * 8 > ws_bytes || !d_workspace) return DCPMLA_ERR_CAPACITY;
   if (nb > INT32_MAX || n > (int64_t)UINT32_MAX) return DCPMLA_ERR_UNSUPPORTED;
-  uint32_t* counts = static_cast<uint32_t*>(d_workspace);
-  filter_count_kernel<<<(unsigned)nb, 256, 0, st>>>(d_idx, n, c, interleave, rank, counts, d_err);
-  filter_scan_kernel<<<1, 1024, 0, st>>>(counts, nb, d_count);
-  filter_scatter_kernel<<<(unsigned)nb, 256, 0, st>>>(d_idx, n, c, interleave, rank, counts, d_out);
+  uint64_t* status = static_cast<uint64_t*>(d_workspace);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(status + nb);
+  if (cudaMemsetAsync(d_workspace, 0, (size_t)(nb + 1) * 8, st) != cudaSuccess) return DCPMLA_ERR_CUDA;
+  const int32_t cs = (c & (c - 1)) == 0 ? __builtin_ctz((unsigned)c) : -1;
+  filter_onepass_kernel<<<(unsigned)nb, kFilterWarps * 32, 0, st>>>(d_idx, n, c, cs, interleave, rank, status,
+                                                                    ticket, d_out, d_count, d_err);
   return launch_status();
 }
 

@@ -349,7 +349,9 @@ int dcpmla_kv_append_e4m3(void* const* pools, float* const* scale_pools, int64_t
  * interleave size, floor(i / c) for interleave 1) to d_out (int64, room for n)
  * and their number to *d_count (device int64).  A negative index sets
  * DCPMLA_DERR_POSITION and is dropped.  d_workspace: at least
- * dcpmla_hicache_filter_workspace_size(n) bytes (ERR_CAPACITY otherwise).
+ * dcpmla_hicache_filter_workspace_size(n) bytes (ERR_CAPACITY otherwise); the
+ * call clears it.  One pass: blocks wait (bounded) for their predecessors'
+ * counts; a wait that runs out sets DCPMLA_DERR_TIMEOUT (outputs invalid).
  * ------------------------------------------------------------------------ */
 int dcpmla_hicache_filter_workspace_size(int64_t n, size_t* out);
 int dcpmla_hicache_filter(const int64_t* d_idx, int64_t n, int32_t c, int32_t interleave, int32_t rank,
