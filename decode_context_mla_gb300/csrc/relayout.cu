@@ -151,6 +151,19 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 u, float (&f)[8]) {
   }
 }
 
+// x / scale rounded to nearest: Markstein's correction of x * RN(1 / scale) (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev.
+// 34, 1990): with y = RN(1 / b) and q = RN(a y), the residual a - b q is exact in one FMA and
+// RN(q + (a - b q) y) is RN(a / b) when no intermediate underflows or overflows.  `fast` is
+// false when the reciprocal of the scale would overflow (a subnormal scale); the IEEE division
+// serves there.
+__device__ __forceinline__ float div_scale(float a, float b, float y, bool fast) {
+  if (!fast) return __fdiv_rn(a, b);
+  const float q = __fmul_rn(a, y);
+  const float r = __fmaf_rn(-q, b, a);
+  return __fmaf_rn(r, y, q);
+}
+
 __global__ void __launch_bounds__(256) append_e4m3_kernel(
     ShardPtrs dst, int64_t pool_rows, int32_t c, const int32_t* __restrict__ owner,
     const int64_t* __restrict__ phys, const uint8_t* __restrict__ ckv, int64_t ckv_stride_b,
@@ -164,7 +177,8 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
     if (lane == 0) set_err(err, DCPMLA_DERR_SLOT);
     return;
   }
-  float lat[16], rope[16];
+  // 16 latent dims and 2 rope dims per lane
+  float lat[16];
   {
     const uint4* src = reinterpret_cast<const uint4*>(ckv + row * ckv_stride_b) + 2 * lane;
     float a[8], b[8];
@@ -176,25 +190,16 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
       lat[8 + i] = b[i];
     }
   }
-  float amax = 0.f;
+  const uint32_t rp = __ldg(reinterpret_cast<const uint32_t*>(krope + row * krope_stride_b) + lane);
+  const float rope0 = __uint_as_float(rp << 16), rope1 = __uint_as_float(rp & 0xFFFF0000u);
+  float amax = fmaxf(fabsf(rope0), fabsf(rope1));
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(lat[i]));
-  if (lane < 4) {
-    const uint4* src = reinterpret_cast<const uint4*>(krope + row * krope_stride_b) + 2 * lane;
-    float a[8], b[8];
-    unpack_bf16x8(__ldg(src), a);
-    unpack_bf16x8(__ldg(src + 1), b);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      rope[i] = a[i];
-      rope[8 + i] = b[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(rope[i]));
-  }
   // non-negative floats order like their bit patterns
   amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
   const float scale = __fdiv_rn(amax, 448.f);
+  const bool fast = scale >= 1.17549435e-38f;   // a normal scale: its reciprocal is finite
+  const float ys = fast ? __frcp_rn(scale) : 0.f;
   uint8_t* prow = static_cast<uint8_t*>(dst.pool[r]) + s * kDK;
   uint32_t w[4];
 #pragma unroll
@@ -203,28 +208,18 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
     if (scale > 0.f) {
       float y[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = fminf(fmaxf(__fdiv_rn(lat[i + m], scale), -448.f), 448.f);
+      for (int m = 0; m < 4; ++m) y[m] = fminf(fmaxf(div_scale(lat[i + m], scale, ys, fast), -448.f), 448.f);
       w[k] = (uint32_t)e4m3x2(y[0], y[1]) | ((uint32_t)e4m3x2(y[2], y[3]) << 16);
     } else {
       w[k] = 0u;
     }
   }
   reinterpret_cast<uint4*>(prow)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
-  if (lane < 4) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = 4 * k;
-      if (scale > 0.f) {
-        float y[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) y[m] = fminf(fmaxf(__fdiv_rn(rope[i + m], scale), -448.f), 448.f);
-        w[k] = (uint32_t)e4m3x2(y[0], y[1]) | ((uint32_t)e4m3x2(y[2], y[3]) << 16);
-      } else {
-        w[k] = 0u;
-      }
-    }
-    reinterpret_cast<uint4*>(prow + kDL)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  uint16_t rw = 0;
+  if (scale > 0.f)
+    rw = e4m3x2(fminf(fmaxf(div_scale(rope0, scale, ys, fast), -448.f), 448.f),
+                fminf(fmaxf(div_scale(rope1, scale, ys, fast), -448.f), 448.f));
+  reinterpret_cast<uint16_t*>(prow + kDL)[lane] = rw;
   if (lane == 0) dst.scale[r][s] = scale;
 }
 

@@ -133,6 +133,36 @@ def test_relayout_flags_bad_pages_and_lengths():
 
 
 @needs_cuda
+def test_e4m3_quantising_append_many_rows_bit_exact():
+    """16384 rows over a wide range of magnitudes: every code and scale matches the oracle's
+    IEEE division (the kernel divides by Markstein's correction of a reciprocal product)."""
+    c, P, n = 2, 64, 16384
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(n, O.D_K, generator=g) * torch.exp(torch.randn(n, 1, generator=g) * 8)
+    rows = x.to(torch.bfloat16)
+    pages = n // (P * c) * 2
+    pools = [torch.full((pages * P, O.D_K), SENT, dtype=torch.uint8, device="cuda") for _ in range(c)]
+    spools = [torch.full((pages * P,), -1.0, device="cuda") for _ in range(c)]
+    pt = torch.arange(pages, dtype=torch.int32).view(1, -1)
+    pos = torch.arange(n, dtype=torch.int64)
+    req = torch.zeros(n, dtype=torch.int32)
+    owner = torch.empty(n, dtype=torch.int32, device="cuda")
+    phys = torch.empty(n, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dcpmla_slot_map(pt.cuda(), pages, c, P, req.cuda(), pos.cuda(), None, owner, phys, err)
+    rows_d = rows.cuda()
+    B.dcpmla_kv_append_e4m3(pools, spools, owner, phys, rows_d[:, :512], rows_d[:, 512:], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    codes, scales = O.quantize_e4m3_rows(bits(rows))
+    own, ph = O.striped_slots(pt.numpy()[0], pos.numpy(), c, P, 1)
+    for r in range(c):
+        sel = own == r
+        assert np.array_equal(pools[r].cpu().numpy()[ph[sel]], codes[sel])
+        assert np.array_equal(spools[r].cpu().numpy()[ph[sel]].view(np.uint32), scales[sel].view(np.uint32))
+
+
+@needs_cuda
 @pytest.mark.parametrize("I", [1, 4])
 def test_e4m3_quantising_append_bit_exact(I):
     c, P, n = 4, 16, 333
@@ -149,6 +179,9 @@ def test_e4m3_quantising_append_bit_exact(I):
     x[11, 0] = 448.0
     x[12, :] = 2.0 * mids.repeat(O.D_K // len(mids))
     x[12, 1] = -896.0
+    x[13, :] = 1e-37                                       # a subnormal scale (no finite reciprocal)
+    x[13, 3] = -2e-37
+    x[14, :] = 1e-40                                       # bf16 subnormals
     rows = x.to(torch.bfloat16)
     pages = 40
     pools = [torch.full((pages * P, O.D_K), SENT, dtype=torch.uint8, device="cuda") for _ in range(c)]
