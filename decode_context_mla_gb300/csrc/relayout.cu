@@ -171,26 +171,27 @@ __global__ void __launch_bounds__(256) append_e4m3_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (row >= n) return;
+  // the row's values (16 latent and 2 rope dims a lane) and its destination, all in flight at once
+  const uint4* src = reinterpret_cast<const uint4*>(ckv + row * ckv_stride_b) + 2 * lane;
+  const uint4 l0 = __ldg(src), l1 = __ldg(src + 1);
+  const uint32_t rp = __ldg(reinterpret_cast<const uint32_t*>(krope + row * krope_stride_b) + lane);
   const int32_t r = __ldg(owner + row);
   const int64_t s = __ldg(phys + row);
   if (r < 0 || r >= c || s < 0 || s >= pool_rows) {   // uniform across the warp
     if (lane == 0) set_err(err, DCPMLA_DERR_SLOT);
     return;
   }
-  // 16 latent dims and 2 rope dims per lane
   float lat[16];
   {
-    const uint4* src = reinterpret_cast<const uint4*>(ckv + row * ckv_stride_b) + 2 * lane;
     float a[8], b[8];
-    unpack_bf16x8(__ldg(src), a);
-    unpack_bf16x8(__ldg(src + 1), b);
+    unpack_bf16x8(l0, a);
+    unpack_bf16x8(l1, b);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       lat[i] = a[i];
       lat[8 + i] = b[i];
     }
   }
-  const uint32_t rp = __ldg(reinterpret_cast<const uint32_t*>(krope + row * krope_stride_b) + lane);
   const float rope0 = __uint_as_float(rp << 16), rope1 = __uint_as_float(rp & 0xFFFF0000u);
   float amax = fmaxf(fabsf(rope0), fabsf(rope1));
 #pragma unroll
