@@ -275,7 +275,7 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
 // its inclusive prefix, publishes its own inclusive prefix and the block writes its kept
 // slots there.  A look-back that waits past its limit sets DCPMLA_DERR_TIMEOUT (and the
 // outputs are invalid); it never blocks for good.
-__global__ void __launch_bounds__(kFilterWarps * 32) filter_onepass_kernel(
+__global__ void __launch_bounds__(kFilterWarps * 32, 4) filter_onepass_kernel(
     const int64_t* __restrict__ idx, int64_t n, int32_t c, int32_t cs, int32_t I, int32_t rank, uint64_t* status,
     unsigned int* ticket, int64_t* __restrict__ out, int64_t* count, int32_t* err) {
   __shared__ uint32_t warp_n[kFilterWarps];
@@ -286,11 +286,13 @@ __global__ void __launch_bounds__(kFilterWarps * 32) filter_onepass_kernel(
   __syncthreads();
   const int tile = tile_s;
   const int64_t base = (int64_t)tile * kFilterBlock + warp * (kFilterRounds * 32);
+  // the values are read again (from L1) for the kept entries once the prefix is known, so
+  // none is held across the look-back
   int64_t v[kFilterRounds];
 #pragma unroll
   for (int k = 0; k < kFilterRounds; ++k) {
     const int64_t i = base + k * 32 + lane;
-    v[k] = i < n ? __ldcs(idx + i) : -1;   // past the list: dropped, not reported
+    v[k] = i < n ? __ldg(idx + i) : -1;   // past the list: dropped, not reported
   }
   uint32_t keep = 0, mine = 0;   // bit k: round k's index is kept
   bool neg = false;
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(kFilterWarps * 32) filter_onepass_kernel(
     if (kp) {
       int32_t o;
       int64_t l;
-      owner_local(v[k], c, cs, I, o, l);
+      owner_local(__ldg(idx + base + k * 32 + lane), c, cs, I, o, l);
       out[pos + __popc(bal & ((1u << lane) - 1u))] = l;
     }
     pos += __popc(bal);
