@@ -147,7 +147,38 @@ def _compare_pools(dw, ow: OracleWorkload):
 @needs_cuda
 @pytest.mark.parametrize("name", list(SMALL))
 def test_step_parity_small(name):
-    w = SMALL[name]
+    _check_step(SMALL[name], name)
+
+
+def _fewhead_sweep(n=10, seed=2024):
+    """Seeded random shapes inside the token-major kernel's limits (at most 16 query rows, at
+    least 16 in the batch, P a multiple of 8, at most 8 shards), mixed long and short lengths."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(n):
+        Tq = int(rng.choice([1, 2, 3, 4]))
+        H = int(rng.choice([h for h in (1, 2, 4, 5, 8, 16) if h * Tq <= 16]))
+        Bn = max(int(rng.integers(1, 7)), -(-16 // (H * Tq)))
+        cases.append(W.Workload(f"fhsw{k}", B=Bn, H=H, Tq=Tq, c=int(rng.choice([1, 2, 3, 4, 5, 8])),
+                                P=int(rng.choice([8, 16, 24, 32, 48, 64, 96, 128])), kv_dtype="bf16",
+                                lse_base=str(rng.choice(["e", "2"])), seed=100 + k,
+                                lengths_mix=(int(rng.integers(0, Bn + 1)), 1000, 9000, Tq, 400)))
+    return cases
+
+
+FEWHEAD_SWEEP = _fewhead_sweep()
+
+
+@needs_cuda
+@pytest.mark.parametrize("w", FEWHEAD_SWEEP, ids=[w.name for w in FEWHEAD_SWEEP])
+def test_fewhead_random_shapes(w):
+    """The token-major kernel on seeded random shapes: path check, then the full step parity."""
+    got = B.dcpmla_decode_path(w.B, w.Tq, w.H, w.P, w.c, w.c, B.KV_BF16, max(w.pages_per_request()))
+    assert got == (B.PATH_TC_FEWHEAD, 2), (w, got)
+    _check_step(w, w.name)
+
+
+def _check_step(w, name):
     dw = Hn.build(w, fill_byte=SENTINEL)
     dw.step.run()
     torch.cuda.synchronize()
