@@ -151,17 +151,33 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 u, float (&f)[8]) {
   }
 }
 
-// x / scale rounded to nearest: Markstein's correction of x * RN(1 / scale) (P. Markstein,
-// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev.
-// 34, 1990): with y = RN(1 / b) and q = RN(a y), the residual a - b q is exact in one FMA and
-// RN(q + (a - b q) y) is RN(a / b) when no intermediate underflows or overflows.  `fast` is
-// false when the reciprocal of the scale would overflow (a subnormal scale); the IEEE division
-// serves there.
+// Whether v lies within one binary32 step of a point where rounding to E4M3 changes direction
+// (a midpoint between two E4M3 values): below 2^-6 E4M3 steps by 2^-9, from there on it keeps
+// three fraction bits, and below 2^-10 everything rounds to zero.
+__device__ __forceinline__ bool near_e4m3_midpoint(float v) {
+  const uint32_t u = __float_as_uint(v) & 0x7FFFFFFFu;
+  const int e = (int)(u >> 23) - 127;
+  if (e < -10) return false;
+  const int drop = e >= -6 ? 20 : 14 - e;                  // binary32 bits below the E4M3 step
+  const uint32_t sig = (u & 0x7FFFFFu) | 0x800000u;
+  const uint32_t low = sig & ((1u << drop) - 1u), half = 1u << (drop - 1);
+  return low + 1u >= half && low <= half + 1u;
+}
+
+// x / scale for the E4M3 code, with the code of the correctly rounded quotient.  Markstein's
+// correction of a reciprocal product (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990): with y = RN(1 / b), q = RN(a y)
+// lies within two steps of a / b, and q + RN(a - b q) y (one FMA) within 2.5e-7 of a step, so
+// its rounding is RN(a / b) or a neighbour.  Two neighbouring binary32 values round to
+// different E4M3 codes only if one of them is an E4M3 midpoint, so where the result is within a
+// step of one the IEEE division decides.  `fast` is false when the reciprocal of the scale
+// would overflow (a subnormal scale); the IEEE division serves there too.
 __device__ __forceinline__ float div_scale(float a, float b, float y, bool fast) {
   if (!fast) return __fdiv_rn(a, b);
   const float q = __fmul_rn(a, y);
   const float r = __fmaf_rn(-q, b, a);
-  return __fmaf_rn(r, y, q);
+  const float qc = __fmaf_rn(r, y, q);
+  return near_e4m3_midpoint(qc) ? __fdiv_rn(a, b) : qc;
 }
 
 __global__ void __launch_bounds__(256) append_e4m3_kernel(
